@@ -1,0 +1,294 @@
+// C ABI of libmoe: argument validation, dispatch, error reporting.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = {0};
+
+int fail(int code, const char* fmt, const char* detail = nullptr) {
+  if (detail) std::snprintf(g_err, sizeof(g_err), fmt, detail);
+  else std::snprintf(g_err, sizeof(g_err), "%s", fmt);
+  return code;
+}
+
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) {
+    g_err[0] = 0;
+    return MOE_OK;
+  }
+  std::snprintf(g_err, sizeof(g_err), "%s: %s", where, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+}  // namespace
+
+const DeviceInfo& device_info() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.device != dev) {
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, dev) == cudaSuccess) {
+      d.sms = p.multiProcessorCount;
+      d.major = p.major;
+      d.minor = p.minor;
+      d.smem_optin = p.sharedMemPerBlockOptin;
+      d.device = dev;
+    }
+  }
+  return d;
+}
+
+static int check_device() {
+  const DeviceInfo& d = device_info();
+  if (d.device < 0) return fail(MOE_ERR_CUDA, "no CUDA device");
+  if (d.major != 10) return fail(MOE_ERR_UNSUPPORTED, "libmoe is built for sm_103a (Blackwell datacenter) only");
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_last_error_string(void) { return g_err; }
+
+int moe_get_error(const uint32_t* dev_err, void* stream, uint32_t* bits) {
+  if (!dev_err || !bits) return fail(MOE_ERR_ARG, "moe_get_error: NULL pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(e, "moe_get_error(sync)");
+  e = cudaMemcpy(bits, dev_err, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return cuda_status(e, "moe_get_error(copy)");
+}
+
+int moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err, void* stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return fail(MOE_ERR_ARG, "moe_route: bad shape");
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !w) return fail(MOE_ERR_ARG, "moe_route: NULL pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_route(logits, T, E, k, ids, w, dev_err, static_cast<cudaStream_t>(stream)), "moe_route");
+}
+
+size_t moe_permute_workspace_size(int T, int k, int E) {
+  (void)T;
+  (void)k;
+  (void)E;
+  return 0;
+}
+
+int moe_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
+                const uint16_t* x, int H, int act_fmt, void* x_perm, uint8_t* x_perm_scale, void* ws,
+                size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || static_cast<int64_t>(T) * k >= (1LL << 31))
+    return fail(MOE_ERR_ARG, "moe_permute: bad shape");
+  if (!offsets || (T > 0 && (!ids || !perm || !inv))) return fail(MOE_ERR_ARG, "moe_permute: NULL pointer");
+  if (act_fmt != MOE_FMT_NONE) {
+    if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "moe_permute: act_fmt");
+    if (H <= 0 || H % 128) return fail(MOE_ERR_ARG, "moe_permute: H must be a positive multiple of 128");
+    if (T > 0 && (!x || !x_perm || !aligned(x, 16) || !aligned(x_perm, 16)))
+      return fail(MOE_ERR_ARG, "moe_permute: x / x_perm NULL or not 16-byte aligned");
+    if (act_fmt == MOE_FMT_MXFP8 && T > 0 && !x_perm_scale) return fail(MOE_ERR_ARG, "moe_permute: x_perm_scale");
+  }
+  if (int r = check_device()) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_permute(ids, T, k, E, offsets, perm, inv, dev_err, s);
+  if (e == cudaSuccess && act_fmt != MOE_FMT_NONE) e = launch_gather(x, perm, T * k, k, H, act_fmt, x_perm, x_perm_scale, s);
+  return cuda_status(e, "moe_permute");
+}
+
+int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols, void* rows, void* stream) {
+  if (A < 0 || cols <= 0 || (fmt != MOE_FMT_BF16 && fmt != MOE_FMT_F32)) return fail(MOE_ERR_ARG, "moe_unpermute: bad args");
+  if ((cols * (fmt == MOE_FMT_F32 ? 4 : 2)) % 16) return fail(MOE_ERR_ARG, "moe_unpermute: row bytes must be a multiple of 16");
+  if (A == 0) return MOE_OK;
+  if (!rows_perm || !inv || !rows || !aligned(rows_perm, 16) || !aligned(rows, 16))
+    return fail(MOE_ERR_ARG, "moe_unpermute: NULL or misaligned pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_unpermute(rows_perm, fmt, inv, A, cols, rows, static_cast<cudaStream_t>(stream)),
+                     "moe_unpermute");
+}
+
+int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
+                  uint16_t* scales_k, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "moe_w2_repack: bad shape");
+  if (rows == 0) return MOE_OK;
+  if (!codes || !scales || !codes_k || !scales_k || !aligned(codes, 4) || !aligned(codes_k, 4) ||
+      !aligned(scales, 2) || !aligned(scales_k, 2))
+    return fail(MOE_ERR_ARG, "moe_w2_repack: NULL or misaligned pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_w2_repack(codes, scales, rows, K, codes_k, scales_k, static_cast<cudaStream_t>(stream)),
+                     "moe_w2_repack");
+}
+
+int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out_bf16,
+                   void* stream) {
+  if (rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "moe_dequant_w2: bad shape");
+  if (rows == 0) return MOE_OK;
+  if (!codes_k || !scales_k || !out_bf16 || !aligned(codes_k, 4)) return fail(MOE_ERR_ARG, "moe_dequant_w2: pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_dequant_w2(codes_k, scales_k, rows, K, out_bf16, static_cast<cudaStream_t>(stream)),
+                     "moe_dequant_w2");
+}
+
+int moe_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K, float* out_f32, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "moe_dequant_mxfp4: bad shape");
+  if (rows == 0) return MOE_OK;
+  if (!e2m1 || !e8m0 || !out_f32 || !aligned(e2m1, 16)) return fail(MOE_ERR_ARG, "moe_dequant_mxfp4: pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_dequant_mxfp4(e2m1, e8m0, rows, K, out_f32, static_cast<cudaStream_t>(stream)),
+                     "moe_dequant_mxfp4");
+}
+
+int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* experts, int n_experts, int rows, int K,
+                    uint8_t* ws, size_t ws_bytes, const int32_t* ws_slots, uint32_t* dev_err, void* stream) {
+  if (n_experts < 0 || rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "mxfp4_to_fp8_ws: bad shape");
+  if (n_experts == 0 || rows == 0) return MOE_OK;
+  if (!e2m1 || !e8m0 || !experts || !ws || !ws_slots || !aligned(e2m1, 16) || !aligned(ws, 16))
+    return fail(MOE_ERR_ARG, "mxfp4_to_fp8_ws: NULL or misaligned pointer");
+  if (ws_bytes < static_cast<size_t>(rows) * K) return fail(MOE_ERR_WS_SMALL, "mxfp4_to_fp8_ws: workspace below one slot");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_mxfp4_to_fp8(e2m1, e8m0, experts, n_experts, rows, K, ws, ws_bytes, ws_slots, dev_err,
+                                         static_cast<cudaStream_t>(stream)),
+                     "mxfp4_to_fp8_ws");
+}
+
+static int check_mm(const char* who, int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale,
+                    const int32_t* offsets, int E, int N, int K, const void* out, int out_fmt,
+                    const uint8_t* out_scale) {
+  if (stage != MOE_STAGE_FC1_SWIGLU && stage != MOE_STAGE_FC2) return fail(MOE_ERR_ARG, "%s: bad stage", who);
+  if (mode < MOE_MODE_AUTO || mode > MOE_MODE_GEMM) return fail(MOE_ERR_ARG, "%s: bad mode", who);
+  if (E < 1 || E > 1024 || N <= 0 || K <= 0 || N % 128 || K % 128 || K > 8192)
+    return fail(MOE_ERR_ARG, "%s: bad shape (N, K multiples of 128, K <= 8192, 1 <= E <= 1024)", who);
+  if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "%s: act_fmt", who);
+  if (act_fmt == MOE_FMT_MXFP8 && !act_scale) return fail(MOE_ERR_ARG, "%s: act_scale is NULL", who);
+  if (!act || !offsets || !out || !aligned(act, 16)) return fail(MOE_ERR_ARG, "%s: NULL or misaligned pointer", who);
+  if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32 && out_fmt != MOE_FMT_MXFP8)
+    return fail(MOE_ERR_ARG, "%s: out_fmt", who);
+  if (out_fmt == MOE_FMT_MXFP8 && (stage != MOE_STAGE_FC1_SWIGLU || !out_scale))
+    return fail(MOE_ERR_ARG, "%s: MXFP8 output is for FC1 with out_scale", who);
+  return check_device();
+}
+
+int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, const int32_t* act_row,
+              int act_row_div, const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
+              const int32_t* expert_slot, int E, int N, int K, void* out, int out_fmt, uint8_t* out_scale, void* ws,
+              size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (int r = check_mm("moe_w2_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
+    return r;
+  if (!codes_k || !scales_k || !aligned(codes_k, 16) || !aligned(scales_k, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_mm: weights NULL or not 16-byte aligned");
+  if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm: act_row_div < 1");
+  MMArgs a{};
+  a.stage = stage;
+  a.act = act;
+  a.act_fmt = act_fmt;
+  a.act_scale = act_scale;
+  a.act_row = act_row;
+  a.act_row_div = act_row ? act_row_div : 1;
+  a.wkind = kW2;
+  a.wq = codes_k;
+  a.wscale = scales_k;
+  a.wslot_of = nullptr;  // 2-bit weights are indexed by expert
+  a.select_map = expert_slot;
+  a.select = expert_slot ? 1 : 0;
+  a.offsets = offsets;
+  a.expert_begin = 0;
+  a.expert_end = E;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.out_fmt = out_fmt;
+  a.out_scale = out_scale;
+  a.dev_err = dev_err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_gemv(a, s), "moe_w2_mm");
+}
+
+int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, const int32_t* act_row,
+                 int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
+                 const int32_t* ws_slot_of_expert, const int32_t* offsets, const int32_t* expert_slot,
+                 int expert_begin, int expert_end, int E, int N, int K, void* out, int out_fmt, uint8_t* out_scale,
+                 void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (int r = check_mm("moe_mxfp4_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
+    return r;
+  if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_row_div < 1");
+  if (expert_begin < 0 || expert_end > E || expert_begin > expert_end)
+    return fail(MOE_ERR_ARG, "moe_mxfp4_mm: bad expert range");
+  const bool use_fp8 = fp8_ws != nullptr;
+  if (use_fp8 == (e2m1 != nullptr)) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: give exactly one of e2m1 / fp8_ws");
+  MMArgs a{};
+  a.stage = stage;
+  a.act = act;
+  a.act_fmt = act_fmt;
+  a.act_scale = act_scale;
+  a.act_row = act_row;
+  a.act_row_div = act_row ? act_row_div : 1;
+  if (use_fp8) {
+    if (!ws_slot_of_expert || !aligned(fp8_ws, 16)) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: FP8 workspace args");
+    a.wkind = kFP8;
+    a.wq = fp8_ws;
+    a.wscale = nullptr;
+    a.wslot_of = ws_slot_of_expert;
+    a.select_map = ws_slot_of_expert;
+    a.select = 2;
+  } else {
+    if (!e8m0 || !aligned(e2m1, 16) || !aligned(e8m0, 16)) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: MXFP4 weights");
+    a.wkind = kMXFP4;
+    a.wq = e2m1;
+    a.wscale = e8m0;
+    a.wslot_of = expert_slot;
+    a.select_map = expert_slot;
+    a.select = expert_slot ? 2 : 0;
+  }
+  a.offsets = offsets;
+  a.expert_begin = expert_begin;
+  a.expert_end = expert_end;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.out_fmt = out_fmt;
+  a.out_scale = out_scale;
+  a.dev_err = dev_err;
+  return cuda_status(launch_gemv(a, static_cast<cudaStream_t>(stream)), "moe_mxfp4_mm");
+}
+
+int moe_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H, void* out,
+                int out_fmt, void* stream) {
+  if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 128) return fail(MOE_ERR_ARG, "moe_combine: bad shape");
+  if ((y_fmt != MOE_FMT_BF16 && y_fmt != MOE_FMT_F32) || (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32))
+    return fail(MOE_ERR_ARG, "moe_combine: format");
+  if (T == 0) return MOE_OK;
+  if (!y || !w || !inv || !out || !aligned(y, 16) || !aligned(out, 16))
+    return fail(MOE_ERR_ARG, "moe_combine: NULL or misaligned pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_combine(y, y_fmt, w, inv, T, k, H, out, out_fmt, static_cast<cudaStream_t>(stream)),
+                     "moe_combine");
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+// Weight-format kernels: the one-time 2-bit repack into the kernel layout,
+// exact dequantisation exports, and the MXFP4 -> FP8 workspace conversion
+// ("国产GPU完成MoE大模型Day-0适配" §四).  All elementwise and HBM-bound:
+// consecutive threads own consecutive 32-element groups, so every load and
+// store is a contiguous vector access.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+MOE_D uint32_t rotl(uint32_t w, int r) { return __funnelshift_l(w, w, r); }
+
+// Canonical word (16 codes, element i at bits 2i, 2i+1; code c is the c-th
+// entry of {-4,-1,1,4}) -> w2k word: element 2q+h gets its "|entry| = 4" bit
+// at (8+16h-2q) mod 32 and its "entry < 0" bit at (15+16h-2q) mod 32.
+MOE_D uint32_t w2_repack_word(uint32_t w) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t c = (w >> (2 * i)) & 3u;
+    const uint32_t big = (c == 0u || c == 3u) ? 1u : 0u;
+    const uint32_t neg = (c < 2u) ? 1u : 0u;
+    const int q = i >> 1, h = i & 1;
+    const int pm = (8 + 16 * h - 2 * q + 32) & 31;
+    const int ps = (15 + 16 * h - 2 * q + 32) & 31;
+    out |= (big << pm) | (neg << ps);
+  }
+  return out;
+}
+
+__global__ void w2_repack_kernel(const uint32_t* __restrict__ codes, const __half* __restrict__ scales,
+                                 int64_t nwords, int64_t nscales, uint32_t* __restrict__ codes_k,
+                                 uint16_t* __restrict__ scales_k) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nwords; i += stride)
+    codes_k[i] = w2_repack_word(codes[i]);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nscales; i += stride)
+    scales_k[i] = f32_to_bf16_rne(__half2float(scales[i]));
+}
+
+// Exact dequantised value of w2k element (word w, element 2q+h) with bf16
+// scale bits sb: entry * scale.
+MOE_D float w2k_value(uint32_t w, int q, int h, uint32_t sb) {
+  const uint32_t r = rotl(w, 2 * q);
+  const uint32_t bits = h ? (r & 0x81000000u) : ((r << 16) & 0x81000000u);
+  const float quarter = __uint_as_float(bits | 0x3E800000u);  // entry / 4
+  return quarter * 4.0f * bf16_bits_to_f32(sb);
+}
+
+__global__ void dequant_w2_kernel(const uint32_t* __restrict__ codes_k, const uint16_t* __restrict__ scales_k,
+                                  int64_t ngroups, uint16_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < ngroups; gi += stride) {
+    const uint32_t sb = scales_k[gi];
+    uint16_t* o = out + gi * 32;
+#pragma unroll
+    for (int wd = 0; wd < 2; ++wd) {
+      const uint32_t w = codes_k[gi * 2 + wd];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) o[wd * 16 + 2 * q + h] = f32_to_bf16_rne(w2k_value(w, q, h, sb));
+    }
+  }
+}
+
+__global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ e2m1, const uint8_t* __restrict__ e8m0,
+                                     int64_t ngroups, float* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < ngroups; gi += stride) {
+    const uint32_t b = e8m0[gi];
+    const float sc = (b == 255u) ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(b) - 127);
+    const uint4 v = reinterpret_cast<const uint4*>(e2m1)[gi];
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+    float* o = out + gi * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = e2m1x2_to_f32x2((ws[i] >> (8 * j)) & 0xffu);
+        o[i * 8 + j * 2] = f.x * sc;
+        o[i * 8 + j * 2 + 1] = f.y * sc;
+      }
+  }
+}
+
+// One thread per 32-element block: 16 bytes of E2M1 + one E8M0 byte in,
+// 32 E4M3 bytes out.
+__global__ void mxfp4_to_fp8_kernel(const uint8_t* __restrict__ e2m1, const uint8_t* __restrict__ e8m0,
+                                    const int32_t* __restrict__ experts, int n_experts, int64_t groups_per_mat,
+                                    uint8_t* __restrict__ ws, uint64_t ws_bytes, const int32_t* __restrict__ ws_slots,
+                                    uint32_t* dev_err) {
+  const int64_t total = groups_per_mat * n_experts;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool nan_seen = false, overflow = false;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
+    const int xi = static_cast<int>(i / groups_per_mat);
+    const int64_t gi = i - static_cast<int64_t>(xi) * groups_per_mat;
+    const int64_t src = experts[xi];
+    const int64_t slot = ws_slots[xi];
+    const uint64_t end = static_cast<uint64_t>(slot + 1) * static_cast<uint64_t>(groups_per_mat) * 32u;
+    if (slot < 0 || src < 0 || end > ws_bytes) {
+      overflow = true;
+      continue;
+    }
+    const int64_t sg = src * groups_per_mat + gi;
+    const uint32_t b = e8m0[sg];
+    const uint4 v = reinterpret_cast<const uint4*>(e2m1)[sg];
+    uint32_t o[8];
+    if (b == 255u) {
+      nan_seen = true;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = 0x7f7f7f7fu;
+    } else {
+      const float sc = exp2i(static_cast<int>(b) - 127);
+      const uint32_t wsw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f0 = e2m1x2_to_f32x2(wsw[k] & 0xffu);
+        const float2 f1 = e2m1x2_to_f32x2((wsw[k] >> 8) & 0xffu);
+        const float2 f2 = e2m1x2_to_f32x2((wsw[k] >> 16) & 0xffu);
+        const float2 f3 = e2m1x2_to_f32x2(wsw[k] >> 24);
+        const uint32_t a0 = f32x2_to_e4m3x2(f0.x * sc, f0.y * sc);
+        const uint32_t a1 = f32x2_to_e4m3x2(f1.x * sc, f1.y * sc);
+        const uint32_t a2 = f32x2_to_e4m3x2(f2.x * sc, f2.y * sc);
+        const uint32_t a3 = f32x2_to_e4m3x2(f3.x * sc, f3.y * sc);
+        o[2 * k] = a0 | (a1 << 16);
+        o[2 * k + 1] = a2 | (a3 << 16);
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(ws + (slot * groups_per_mat + gi) * 32);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  if (nan_seen) set_err(dev_err, MOE_DEVERR_NAN_SCALE);
+  if (overflow) set_err(dev_err, MOE_DEVERR_OVERFLOW);
+}
+
+int grid_for(int64_t work, int threads) {
+  const int64_t want = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(device_info().sms) * 16;
+  return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+}  // namespace
+
+cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
+                             uint16_t* scales_k, cudaStream_t s) {
+  const int64_t nwords = rows * (K / 16), nsc = rows * (K / 32);
+  if (nwords == 0) return cudaSuccess;
+  w2_repack_kernel<<<grid_for(nwords, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes),
+                                                         reinterpret_cast<const __half*>(scales), nwords, nsc,
+                                                         reinterpret_cast<uint32_t*>(codes_k), scales_k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out,
+                              cudaStream_t s) {
+  const int64_t ng = rows * (K / 32);
+  if (ng == 0) return cudaSuccess;
+  dequant_w2_kernel<<<grid_for(ng, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes_k), scales_k, ng,
+                                                      out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K, float* out,
+                                 cudaStream_t s) {
+  const int64_t ng = rows * (K / 32);
+  if (ng == 0) return cudaSuccess;
+  dequant_mxfp4_kernel<<<grid_for(ng, 256), 256, 0, s>>>(e2m1, e8m0, ng, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_to_fp8(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* experts, int n_experts,
+                                int rows, int K, uint8_t* ws, size_t ws_bytes, const int32_t* ws_slots,
+                                uint32_t* dev_err, cudaStream_t s) {
+  const int64_t gpm = static_cast<int64_t>(rows) * (K / 32);
+  const int64_t work = gpm * n_experts;
+  if (work == 0) return cudaSuccess;
+  mxfp4_to_fp8_kernel<<<grid_for(work, 256), 256, 0, s>>>(e2m1, e8m0, experts, n_experts, gpm, ws,
+                                                          static_cast<uint64_t>(ws_bytes), ws_slots, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

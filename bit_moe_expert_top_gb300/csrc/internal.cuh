@@ -1,0 +1,69 @@
+// Internal launch interface between the C-ABI layer (abi.cu) and the kernel
+// translation units.  Plain types only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct DeviceInfo {
+  int device = -1;
+  int sms = 0;
+  int major = 0, minor = 0;
+  size_t smem_optin = 0;
+};
+// Cached properties of the current device.
+const DeviceInfo& device_info();
+
+// ---- route / permute / combine (route_permute.cu)
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
+                         cudaStream_t s);
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
+                           uint32_t* dev_err, cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, int H, int act_fmt, void* x_perm,
+                          uint8_t* x_perm_scale, cudaStream_t s);
+cudaError_t launch_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols, void* rows,
+                             cudaStream_t s);
+cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H,
+                           void* out, int out_fmt, cudaStream_t s);
+
+// ---- weight formats (convert.cu)
+cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
+                             uint16_t* scales_k, cudaStream_t s);
+cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out,
+                              cudaStream_t s);
+cudaError_t launch_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K, float* out,
+                                 cudaStream_t s);
+cudaError_t launch_mxfp4_to_fp8(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* experts, int n_experts,
+                                int rows, int K, uint8_t* ws, size_t ws_bytes, const int32_t* ws_slots,
+                                uint32_t* dev_err, cudaStream_t s);
+
+// ---- expert matmuls on CUDA cores (gemv.cu)
+enum WeightKind { kW2 = 0, kMXFP4 = 1, kFP8 = 2 };
+
+struct MMArgs {
+  int stage;  // MOE_STAGE_*
+  const void* act;
+  int act_fmt;
+  const uint8_t* act_scale;
+  const int32_t* act_row;
+  int act_row_div;
+  int wkind;                  // WeightKind
+  const uint8_t* wq;          // codes / nibbles / e4m3 bytes, [slots][rows][K*bits/8]
+  const void* wscale;         // bf16 (w2k) or E8M0 [slots][rows][K/32]; NULL for FP8
+  const int32_t* wslot_of;    // expert -> weight slot (nullable: slot = e)
+  const int32_t* select_map;  // per-expert map read by `select`
+  int select;                 // 0: all experts; 1: experts with select_map[e] < 0 (the
+                              // 2-bit pass skips delta-cached experts); 2: select_map[e] >= 0
+  const int32_t* offsets;
+  int expert_begin, expert_end;
+  int E, N, K;
+  void* out;
+  int out_fmt;
+  uint8_t* out_scale;
+  uint32_t* dev_err;
+};
+cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,375 @@
+// Routing, grouping, activation gather (bf16 / MXFP8) and the weighted
+// combine.  All HBM-bound or latency-bound; deterministic, no global atomics
+// on data (only the error word).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ routing
+// Order used by the top-k: larger logit first, equal logits -> lower expert id
+// first, NaN after every number (NaNs among themselves by id).
+MOE_D bool route_better(float v1, int i1, float v2, int i2) {
+  const bool n1 = v1 != v1, n2 = v2 != v2;
+  if (n1 != n2) return n2;
+  if (!n1 && v1 != v2) return v1 > v2;
+  return i1 < i2;
+}
+
+// One warp per token; the token's logits are staged in shared memory and the
+// top-k is taken by k rounds of a warp-wide arg-best.
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                    int32_t* __restrict__ ids, float* __restrict__ w,
+                                                    uint32_t* dev_err) {
+  extern __shared__ float s_route[];  // [8 warps][E] values, then [8][E] taken flags (as float bits)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float* vals = s_route + warp * E;
+  unsigned char* taken = reinterpret_cast<unsigned char*>(s_route + 8 * E) + warp * E;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  bool any_nan = false;
+  for (int e = lane; e < E; e += 32) {
+    float v = row[e];
+    any_nan |= (v != v);
+    vals[e] = v;
+    taken[e] = 0;
+  }
+  if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_err(dev_err, MOE_DEVERR_NAN_LOGIT);
+  __syncwarp();
+  float my_sel = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.f;
+    int bi = 0x7fffffff;
+    bool have = false;
+    for (int e = lane; e < E; e += 32) {
+      if (taken[e]) continue;
+      float v = vals[e];
+      if (!have || route_better(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+        have = true;
+      }
+    }
+    // warp arg-best; lanes without a candidate carry id = INT_MAX and lose
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      bool oh = __shfl_xor_sync(0xffffffffu, have, o);
+      if (oh && (!have || route_better(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+        have = true;
+      }
+    }
+    if (lane == (bi & 31)) taken[bi] = 1;
+    if (lane == j) {
+      my_sel = bv;
+      my_id = bi;
+    }
+    __syncwarp();
+  }
+  // softmax over the selected logits, relative to the largest (slot 0)
+  float l = (my_sel != my_sel) ? -INFINITY : my_sel;
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);
+  float z = (lane < k) ? expf(l - l0) : 0.f;
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, z, j);
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = my_id;
+    w[static_cast<size_t>(t) * k + lane] = z / s;
+  }
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
+                         cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(8) * E * 4 + static_cast<size_t>(8) * E;
+  static bool attr_set = false;  // benign race: idempotent attribute write
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  route_kernel<<<(T + 7) / 8, 256, smem, s>>>(logits, T, E, k, ids, w, dev_err);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ grouping
+// Single CTA of 32 warps.  Warp w owns a contiguous chunk of assignments and
+// keeps its own per-expert count (hist[w][e]); a warp-level match_any turns a
+// tile of 32 ids into groups whose leader updates the count, so each count
+// has one writer.  Exclusive scans over warps and experts give every warp the
+// first output row of each of its groups; the second walk writes perm/inv in
+// increasing assignment order within each expert (stable).
+constexpr int kPermWarps = 32;
+
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ ids, int A, int E,
+                                                       int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                       int32_t* __restrict__ inv, uint32_t* dev_err) {
+  extern __shared__ int s_perm[];
+  int* hist = s_perm;                    // [32][E]
+  int* tot = s_perm + kPermWarps * E;    // [E]
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int chunk = (A + kPermWarps - 1) / kPermWarps;
+  chunk = (chunk + 31) & ~31;
+  const int beg = warp * chunk;
+  const int end = min(A, beg + chunk);
+
+  for (int i = tid; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+
+  bool bad = false;
+  for (int base = beg; base < end; base += 32) {
+    const int a = base + lane;
+    int e = (a < end) ? ids[a] : -1;
+    if (a < end && (e < 0 || e >= E)) {
+      bad = true;
+      e = -1;
+    }
+    const int key = (e >= 0) ? e : (E + lane);  // invalid lanes form singleton groups
+    const unsigned m = __match_any_sync(0xffffffffu, key);
+    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+    __syncwarp();
+  }
+  if (bad) set_err(dev_err, MOE_DEVERR_BAD_ID);
+  __syncthreads();
+
+  // per-expert exclusive scan over warps; totals
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+
+  // exclusive scan of tot over experts (E <= 1024: one element per thread)
+  int v = (tid < E) ? tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sums[lane];
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_sums[lane] = wi - ws;  // exclusive
+  }
+  __syncthreads();
+  const int excl = incl - v + warp_sums[warp];
+  if (tid < E) {
+    offsets[tid] = excl;
+    tot[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+  }
+  __syncthreads();
+  for (int i = tid; i < kPermWarps * E; i += blockDim.x) hist[i] += tot[i % E];
+  __syncthreads();
+
+  for (int base = beg; base < end; base += 32) {
+    const int a = base + lane;
+    int e = (a < end) ? ids[a] : -1;
+    if (a < end && (e < 0 || e >= E)) e = -1;
+    const int key = (e >= 0) ? e : (E + lane);
+    const unsigned m = __match_any_sync(0xffffffffu, key);
+    int pos = -1;
+    if (e >= 0) pos = hist[warp * E + e] + __popc(m & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+    __syncwarp();
+    if (a < end) {
+      inv[a] = pos;
+      if (pos >= 0) perm[pos] = a;
+    }
+  }
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
+                           uint32_t* dev_err, cudaStream_t s) {
+  const int A = T * k;
+  const size_t smem = static_cast<size_t>(kPermWarps + 1) * E * sizeof(int);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  permute_kernel<<<1, 1024, smem, s>>>(ids, A, E, offsets, perm, inv, dev_err);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gather
+__global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
+                                   int H, uint16_t* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int vec = H / 8;  // uint4 per row
+  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(perm[p] / k) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(p) * H);
+    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// MXFP8 quantisation fused into the gather: each lane takes 8 consecutive
+// elements, 4 lanes form one block of 32 (block max by two shuffles).
+__global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
+                                    int H, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  const int lane = threadIdx.x & 31;
+  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
+    const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
+    for (int base = 0; base < H; base += 256) {
+      const int e0 = base + lane * 8;
+      const bool ok = e0 < H;
+      float f[8];
+      float amax = 0.f;
+      if (ok) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(src + e0));
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[2 * i] = __uint_as_float(wv[i] << 16);
+          f[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
+          amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      if (ok) {
+        const int X = mx_scale_exp(amax);
+        const float inv = exp2i(-X);
+        uint32_t packed[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t lo = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+          uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+          packed[i] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
+        if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
+      }
+    }
+  }
+}
+
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, int H, int act_fmt, void* x_perm,
+                          uint8_t* x_perm_scale, cudaStream_t s) {
+  if (A == 0) return cudaSuccess;
+  const int blocks = min((A + 7) / 8, device_info().sms * 8);
+  if (act_fmt == MOE_FMT_BF16) {
+    gather_bf16_kernel<<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint16_t*>(x_perm));
+  } else {
+    gather_mxfp8_kernel<<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), x_perm_scale);
+  }
+  return cudaGetLastError();
+}
+
+__global__ void unpermute_kernel(const uint8_t* __restrict__ src, const int32_t* __restrict__ inv, int A,
+                                 int row_bytes, uint8_t* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  for (int a = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); a < A; a += gridDim.x * (blockDim.x >> 5)) {
+    const int p = inv[a];
+    if (p < 0) continue;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<size_t>(p) * row_bytes);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(a) * row_bytes);
+    for (int i = lane; i < row_bytes / 16; i += 32) d4[i] = s4[i];
+  }
+}
+
+cudaError_t launch_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols, void* rows,
+                             cudaStream_t s) {
+  if (A == 0) return cudaSuccess;
+  const int row_bytes = cols * (fmt == MOE_FMT_F32 ? 4 : 2);
+  const int blocks = min((A + 7) / 8, device_info().sms * 8);
+  unpermute_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(rows_perm), inv, A, row_bytes,
+                                          static_cast<uint8_t*>(rows));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per output row (token); each lane owns 8 consecutive columns per
+// 256-column step and accumulates the k rows in ascending slot order.
+template <bool kYF32, bool kOutF32>
+__global__ void combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
+                               const int32_t* __restrict__ inv, int T, int k, int H, void* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += gridDim.x * (blockDim.x >> 5)) {
+    for (int base = 0; base < H; base += 256) {
+      const int c0 = base + lane * 8;
+      if (c0 >= H) continue;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int p = inv[static_cast<size_t>(t) * k + j];
+        if (p < 0) continue;
+        const float wj = w[static_cast<size_t>(t) * k + j];
+        float v[8];
+        if (kYF32) {
+          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) +
+                                                              static_cast<size_t>(p) * H + c0);
+          float4 a = __ldg(src), b = __ldg(src + 1);
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+          v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+          uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                         static_cast<size_t>(p) * H + c0));
+          const uint32_t wv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(wv[i] << 16);
+            v[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+      }
+      if (kOutF32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<size_t>(t) * H + c0);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          o[i] = static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i])) |
+                 (static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i + 1])) << 16);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + static_cast<size_t>(t) * H + c0) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
+cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H,
+                           void* out, int out_fmt, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = min((T + 7) / 8, device_info().sms * 8);
+  const bool yf = y_fmt == MOE_FMT_F32, of = out_fmt == MOE_FMT_F32;
+  if (yf && of) combine_kernel<true, true><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else if (yf) combine_kernel<true, false><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else if (of) combine_kernel<false, true><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else combine_kernel<false, false><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,224 @@
+"""One routed-expert FFN layer driven through libmoe's C ABI.
+
+``MoELayer`` owns the device copies of a layer's expert weights (torch
+allocations) and chains the library calls of one step:
+
+    moe_route -> moe_permute -> FC1+SwiGLU -> FC2 -> moe_combine
+
+with the weight path chosen by the layer's format:
+
+* ``w2``    2-bit codebook experts (``moe_w2_mm``);
+* ``mixed`` 2-bit base plus an FP4 delta cache: experts with a cache slot go
+            through ``moe_mxfp4_mm``, the others through ``moe_w2_mm``;
+* ``fp8``   MXFP4 experts converted per expert batch into a reused FP8
+            workspace ring (``mxfp4_to_fp8_ws`` on a side stream) ahead of the
+            FP8 matmuls on the main stream, the conversion of the next batch
+            overlapping the matmuls of the current one ("国产GPU完成MoE大模型
+            Day-0适配" §四).
+
+No arithmetic happens here: every step runs in the library's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+@dataclass
+class StepBuffers:
+    ids: torch.Tensor
+    w: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    inv: torch.Tensor
+    h: torch.Tensor
+    h_scale: Optional[torch.Tensor]
+    y: torch.Tensor
+    out: torch.Tensor
+    x_perm: Optional[torch.Tensor]
+    x_perm_scale: Optional[torch.Tensor]
+    dev_err: torch.Tensor
+
+
+class MoELayer:
+    def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
+                 w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
+                 out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO):
+        """Weights are canonical host arrays (see synth.py / include/moe.h):
+        w2 = (codes1, scales1, codes2, scales2) stacked over experts;
+        mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
+        expert_slot int32 [E] (mixed): cache slot of each expert, -1 if none."""
+        self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
+        self.device = torch.device(device)
+        self.out_fmt, self.mode = out_fmt, mode
+        dev = self.device
+        if fmt in ("w2", "mixed"):
+            c1, s1, c2, s2 = w2
+            self.c1k = torch.empty(c1.shape, dtype=torch.uint8, device=dev)
+            self.s1k = torch.empty(s1.shape, dtype=torch.int16, device=dev)
+            self.c2k = torch.empty(c2.shape, dtype=torch.uint8, device=dev)
+            self.s2k = torch.empty(s2.shape, dtype=torch.int16, device=dev)
+            for src_c, src_s, dc, ds, K in ((c1, s1, self.c1k, self.s1k, H), (c2, s2, self.c2k, self.s2k, I)):
+                tc = _dev(src_c, dev)
+                ts = _dev(src_s.view(np.int16), dev)
+                rows = src_c.shape[0] * src_c.shape[1]
+                L.moe_w2_repack(tc, ts, rows, K, dc, ds)
+                del tc, ts
+        if fmt in ("mixed", "fp8"):
+            q1, s1, q2, s2 = mx
+            self.q1, self.e1 = _dev(q1, dev), _dev(s1, dev)
+            self.q2, self.e2 = _dev(q2, dev), _dev(s2, dev)
+        self.expert_slot = None
+        if fmt == "mixed":
+            self.expert_slot = _dev(np.asarray(expert_slot, dtype=np.int32), dev)
+        if fmt == "fp8":
+            self.batch = fp8_batch
+            self.ring = fp8_ring
+            nslots = fp8_batch * fp8_ring
+            self.ws1 = torch.empty((nslots, 2 * I, H), dtype=torch.uint8, device=dev)
+            self.ws2 = torch.empty((nslots, H, I), dtype=torch.uint8, device=dev)
+            e = np.arange(E)
+            slot = ((e // fp8_batch) % fp8_ring) * fp8_batch + (e % fp8_batch)
+            self.ws_slot = _dev(slot.astype(np.int32), dev)
+            self.batch_experts = [_dev(np.arange(b, min(E, b + fp8_batch), dtype=np.int32), dev)
+                                  for b in range(0, E, fp8_batch)]
+            self.batch_slots = [self.ws_slot[b:min(E, b + fp8_batch)].contiguous() for b in range(0, E, fp8_batch)]
+            self.conv_stream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize(dev)
+
+    # ------------------------------------------------------------ buffers
+    def buffers(self, T: int) -> StepBuffers:
+        dev, E, H, I, k = self.device, self.E, self.H, self.I, self.k
+        A = T * k
+        fp8 = self.fmt == "fp8"
+        return StepBuffers(
+            ids=torch.empty((T, k), dtype=torch.int32, device=dev),
+            w=torch.empty((T, k), dtype=torch.float32, device=dev),
+            offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            perm=torch.empty(A, dtype=torch.int32, device=dev),
+            inv=torch.empty(A, dtype=torch.int32, device=dev),
+            h=torch.empty((A, I), dtype=torch.uint8 if fp8 else torch.int16, device=dev),
+            h_scale=torch.empty((A, I // 32), dtype=torch.uint8, device=dev) if fp8 else None,
+            y=torch.empty((A, H), dtype=torch.int16, device=dev),
+            out=torch.empty((T, H), dtype=torch.float32 if self.out_fmt == L.FMT_F32 else torch.int16, device=dev),
+            x_perm=torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else None,
+            x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
+            dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
+        )
+
+    # ------------------------------------------------------------ one step
+    def step(self, x: torch.Tensor, logits: torch.Tensor, b: StepBuffers, ev: Optional[list] = None) -> torch.Tensor:
+        """x: bf16 bit patterns int16 [T, H]; logits float32 [T, E].
+
+        ``ev``: if given, a CUDA event pair is recorded around every expert
+        matmul launch and appended as (label, start, end)."""
+        T = x.shape[0]
+        self._ev = ev
+        E, H, I, k = self.E, self.H, self.I, self.k
+        L.moe_route(logits, k, b.ids, b.w, b.dev_err)
+        if self.fmt == "fp8":
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
+                          x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
+            self._fp8_experts(b)
+        else:
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+            with self._timed("w2_fc1"):
+                L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
+                            L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
+                            mode=self.mode, dev_err=b.dev_err)
+            if self.fmt == "mixed":
+                with self._timed("mx_fc1"):
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
+                                   e2m1=self.q1, e8m0=self.e1, act_row=b.perm, act_row_div=k,
+                                   expert_slot=self.expert_slot, mode=self.mode, dev_err=b.dev_err)
+            with self._timed("w2_fc2"):
+                L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                            expert_slot=self.expert_slot, mode=self.mode, dev_err=b.dev_err)
+            if self.fmt == "mixed":
+                with self._timed("mx_fc2"):
+                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                                   e2m1=self.q2, e8m0=self.e2, expert_slot=self.expert_slot, mode=self.mode,
+                                   dev_err=b.dev_err)
+        L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
+        return b.out
+
+    class _Timer:
+        def __init__(self, ev, label):
+            self.ev, self.label = ev, label
+
+        def __enter__(self):
+            if self.ev is not None:
+                self.s = torch.cuda.Event(enable_timing=True)
+                self.s.record()
+
+        def __exit__(self, *exc):
+            if self.ev is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                self.ev.append((self.label, self.s, e))
+
+    def _timed(self, label):
+        return MoELayer._Timer(getattr(self, "_ev", None), label)
+
+    def _fp8_experts(self, b: StepBuffers):
+        E, H, I = self.E, self.H, self.I
+        main = torch.cuda.current_stream(self.device)
+        conv = self.conv_stream
+        nb = len(self.batch_experts)
+        converted = [torch.cuda.Event() for _ in range(nb)]
+        consumed = [torch.cuda.Event() for _ in range(nb)]
+        conv.wait_stream(main)  # routing / grouping done before the first matmul needs it
+
+        def convert(i):
+            if i >= self.ring:
+                conv.wait_event(consumed[i - self.ring])  # ring slot free again
+            L.mxfp4_to_fp8_ws(self.q1, self.e1, self.batch_experts[i], 2 * I, H, self.ws1, self.batch_slots[i],
+                              dev_err=b.dev_err, stream=conv)
+            L.mxfp4_to_fp8_ws(self.q2, self.e2, self.batch_experts[i], H, I, self.ws2, self.batch_slots[i],
+                              dev_err=b.dev_err, stream=conv)
+            converted[i].record(conv)
+
+        for i in range(min(self.ring, nb)):
+            convert(i)
+        for i in range(nb):
+            e0 = i * self.batch
+            e1 = min(E, e0 + self.batch)
+            main.wait_event(converted[i])
+            with self._timed("fp8_fc1"):
+                L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h, L.FMT_MXFP8,
+                               fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot, act_scale=b.x_perm_scale,
+                               expert_begin=e0, expert_end=e1, out_scale=b.h_scale, mode=self.mode,
+                               dev_err=b.dev_err)
+            with self._timed("fp8_fc2"):
+                L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                               fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot, act_scale=b.h_scale,
+                               expert_begin=e0, expert_end=e1, mode=self.mode, dev_err=b.dev_err)
+            consumed[i].record(main)
+            if i + self.ring < nb:
+                convert(i + self.ring)
+        main.wait_stream(conv)
+
+    def touched_weight_bytes(self, offsets: np.ndarray) -> int:
+        """Bytes of packed weights (codes/nibbles + scales) of the experts the
+        step touches: the decode roofline's algorithmic traffic."""
+        cnt = np.diff(np.asarray(offsets))
+        H, I = self.H, self.I
+        w2_bytes = 3 * H * I // 4 + 3 * H * I // 32 * 2
+        mx_bytes = 3 * H * I // 2 + 3 * H * I // 32
+        tot = 0
+        slot = None if self.expert_slot is None else self.expert_slot.cpu().numpy()
+        for e in np.nonzero(cnt)[0]:
+            if self.fmt == "w2" or (self.fmt == "mixed" and slot[e] < 0):
+                tot += w2_bytes
+            else:
+                tot += mx_bytes
+        return tot

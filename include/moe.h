@@ -1,0 +1,243 @@
+/*
+ * libmoe — low-bit routed-expert FFN for one GB300 (sm_103a).
+ *
+ * The layer (vLLM-Moet README, release v2026.11.03-r23 notes: "FC1 + SwiGLU +
+ * MXFP8 quant, FC2"; blog "这个项目我们能学到什么?": 2-bit codebook {-4,-1,1,4}
+ * experts and an FP4 delta cache of hot experts; "国产GPU完成MoE大模型Day-0适配"
+ * §四: MXFP4 weights converted online into a reused FP8 workspace):
+ *
+ *   moe_route      top-k softmax routing of router logits
+ *   moe_permute    stable grouping of the T*k assignments by expert (+ optional
+ *                  gather of activation rows, bf16 or MXFP8-quantised)
+ *   moe_w2_mm      expert FC1+SwiGLU or FC2 on 2-bit codebook weights
+ *   moe_mxfp4_mm   expert FC1+SwiGLU or FC2 on MXFP4 weights (delta cache) or
+ *                  on the FP8 workspace
+ *   mxfp4_to_fp8_ws  MXFP4 -> E4M3 conversion into the caller's workspace
+ *   moe_combine    out[t] = sum_j w[t,j] * y[inv[t*k+j]]
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Notation: T tokens, E experts, H hidden, I expert intermediate, k experts
+ *    per token, A = T*k assignments, a = t*k + j (j = slot in the top-k).
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless the
+ *    comment says "host".  The library never allocates, frees or keeps device
+ *    memory.  Buffers must not alias unless a comment allows it.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and never synchronises the host, except
+ *    moe_get_error.
+ *  - Every call returns MOE_OK or a status below.  On MOE_ERR_CUDA the CUDA
+ *    error text is available from moe_last_error_string() (per thread).
+ *  - Data errors found on the device never trap: kernels OR MOE_DEVERR_* bits
+ *    into the caller's `dev_err` word (a uint32 in device memory, which the
+ *    caller zeroes; may be NULL to ignore) and carry on.  Read with
+ *    moe_get_error.
+ *  - Thread-safe: the only global state is a per-device property cache.
+ *
+ * Canonical weight layout (what callers store; parity is stated against it)
+ * ---------------------------------------------------------------------------
+ *  - W1 of expert e: [2I][H] row-major, K = H contiguous; rows 0..I-1 are the
+ *    gate projection, rows I..2I-1 the up projection.
+ *  - W2 of expert e: [H][I] row-major, K = I contiguous.
+ *  - Experts are stacked on a leading dimension: W1 [E][2I][H], W2 [E][H][I].
+ *  - 2-bit codebook: code c in 0..3 is the c-th entry of {-4,-1,1,4}; 4 codes
+ *    per byte, element i of a row at bits 2*(i%4) of byte i/4; one fp16 scale
+ *    per 32 consecutive K elements, [rows][K/32].  The dequantised weight is
+ *    entry * RNE_bf16(scale) (exact in bf16).
+ *  - MXFP4 (OCP MX v1.0): E2M1 nibbles, element 2i in the LOW nibble of byte
+ *    i; one E8M0 byte per 32 consecutive K elements, [rows][K/32]; value =
+ *    E2M1 * 2^(E8M0-127); E8M0 = 255 is NaN.
+ *  - moe_w2_mm reads the 2-bit weights in the "w2k" kernel layout written once
+ *    by moe_w2_repack (same byte sizes; see there).
+ *
+ * Shape limits: 1 <= k <= E <= 1024, k <= 32; H and I multiples of 128;
+ * T*k < 2^31.
+ */
+#ifndef BIT_MOE_EXPERT_TOP_MOE_H
+#define BIT_MOE_EXPERT_TOP_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* status codes */
+#define MOE_OK 0
+#define MOE_ERR_ARG 1          /* NULL / misaligned pointer, bad shape or enum     */
+#define MOE_ERR_WS_SMALL 2     /* workspace smaller than the *_workspace_size query */
+#define MOE_ERR_UNSUPPORTED 3  /* device is not sm_103 / sm_100 family, or format combination not built */
+#define MOE_ERR_CUDA 4         /* a CUDA call failed; see moe_last_error_string()   */
+
+/* bits a kernel ORs into *dev_err */
+#define MOE_DEVERR_BAD_ID 0x1u       /* expert id outside [0, E)                        */
+#define MOE_DEVERR_NAN_LOGIT 0x2u    /* NaN router logit (ranked below every number)    */
+#define MOE_DEVERR_NAN_SCALE 0x4u    /* E8M0 scale byte 255 (NaN) in MXFP4 weights      */
+#define MOE_DEVERR_TIMEOUT 0x8u      /* a bounded on-chip wait gave up; outputs invalid */
+#define MOE_DEVERR_OVERFLOW 0x10u    /* an expert group exceeded a kernel's row limit   */
+
+/* activation / output formats */
+#define MOE_FMT_NONE 0
+#define MOE_FMT_BF16 1   /* uint16 bf16 bit patterns, [rows][cols]                       */
+#define MOE_FMT_F32 2    /* float, [rows][cols]                                          */
+#define MOE_FMT_MXFP8 3  /* E4M3 bytes [rows][cols] + E8M0 bytes [rows][cols/32] (OCP MX)  */
+
+/* expert matmul stage */
+#define MOE_STAGE_FC1_SWIGLU 1  /* h[p][n] = silu(g)*u, g/u = gate/up rows of W1, n < I */
+#define MOE_STAGE_FC2 2         /* y[p][n] = W2 row n . h[p],               n < H       */
+
+/* expert matmul mode */
+#define MOE_MODE_AUTO 0  /* GEMV for small groups, tensor-core GEMM for large ones */
+#define MOE_MODE_GEMV 1  /* CUDA-core grouped GEMV (any group size)               */
+#define MOE_MODE_GEMM 2  /* tcgen05 tensor-core grouped GEMM                      */
+
+/* Library version (MOE_ABI_VERSION). */
+MOE_API int moe_version(void);
+
+/* Text of the last MOE_ERR_* raised on the calling host thread ("" if none).
+ * The pointer stays valid until the next library call on this thread. */
+MOE_API const char* moe_last_error_string(void);
+
+/* Synchronises `stream`, then copies the device word *dev_err to the host
+ * word *bits (host pointer).  The device word is left unchanged. */
+MOE_API int moe_get_error(const uint32_t* dev_err, void* stream, uint32_t* bits);
+
+/* ------------------------------------------------------------------ routing
+ * Top-k softmax routing (vLLM-Moet README line table: 384 routed experts per
+ * layer; "top-8 softmax routing").
+ *   logits  float [T][E]
+ *   ids     int32 [T][k]  out: experts ordered by (logit desc, id asc); NaN
+ *                         logits rank below every number (sets NAN_LOGIT)
+ *   w       float [T][k]  out: w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0)
+ *                         (softmax renormalised over the k selected; sums to 1)
+ * T = 0 is a no-op. */
+MOE_API int moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+              uint32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------ grouping
+ * Stable counting sort of the A = T*k assignments by expert id.
+ *   ids      int32 [T][k]   expert of each assignment (ids outside [0,E) set
+ *                           BAD_ID; such an assignment gets inv = -1 and no row)
+ *   offsets  int32 [E+1]    out: group e occupies permuted rows
+ *                           offsets[e] .. offsets[e+1]-1; offsets[0] = 0
+ *   perm     int32 [A]      out: perm[p] = assignment a of permuted row p, rows of
+ *                           one group in increasing a
+ *   inv      int32 [A]      out: inv[perm[p]] = p
+ *   x        bf16 [T][H]    optional activations (NULL when act_fmt = NONE)
+ *   act_fmt  MOE_FMT_NONE: no gather; MOE_FMT_BF16: x_perm[p] = x[perm[p]/k]
+ *            (bf16 [A][H]); MOE_FMT_MXFP8: x_perm[p] = MXFP8(x[perm[p]/k]),
+ *            E4M3 [A][H] + E8M0 x_perm_scale [A][H/32] (OCP MX: per block of 32,
+ *            scale 2^(floor(log2 amax) - 8), elements RNE + saturate).
+ *   ws       unused (pass NULL, 0); kept so the signature stays stable.
+ * Deterministic and atomics-free in its outputs. */
+MOE_API size_t moe_permute_workspace_size(int T, int k, int E);
+MOE_API int moe_permute(const int32_t* ids, int T, int k, int E,
+                int32_t* offsets, int32_t* perm, int32_t* inv,
+                const uint16_t* x, int H, int act_fmt, void* x_perm, uint8_t* x_perm_scale,
+                void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
+
+/* rows[a] = rows_perm[inv[a]] for a < A (the inverse of the gather).  fmt is
+ * MOE_FMT_BF16 or MOE_FMT_F32; cols elements per row.  A test helper. */
+MOE_API int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols,
+                  void* rows, void* stream);
+
+/* ------------------------------------------------------------------ weights
+ * Rewrite canonical 2-bit weights into the w2k kernel layout (run once, at load).
+ *   codes   uint8 [rows][K/4] canonical;   scales fp16 [rows][K/32]
+ *   codes_k uint8 [rows][K/4] out;         scales_k bf16 [rows][K/32] out
+ * w2k: every 32-bit word still holds 16 consecutive K elements, with the two
+ * bits of element 2q+h (q < 8, h < 2) moved to bit (8+16h-2q) mod 32 (set when
+ * |entry| = 4) and bit (15+16h-2q) mod 32 (set when entry < 0), so rotating
+ * the word left by 2q puts the pair's bits where a bf16 pair's exponent bit 1
+ * and sign bits are.  Scales become RNE_bf16(scale).  `rows` counts all rows of
+ * all experts (e.g. E*2I). */
+MOE_API int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K,
+                  uint8_t* codes_k, uint16_t* scales_k, void* stream);
+
+/* Exact dequantised values (bf16 bit patterns [rows][K]) of w2k weights:
+ * entry * RNE_bf16(scale) — what the GEMM tiles hold. */
+MOE_API int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K,
+                   uint16_t* out_bf16, void* stream);
+
+/* Exact dequantised MXFP4 values as float [rows][K] (NaN where the scale is 255). */
+MOE_API int moe_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K,
+                      float* out_f32, void* stream);
+
+/* MXFP4 -> FP8 workspace ("国产GPU完成MoE大模型Day-0适配" §四: weights stay MXFP4,
+ * the needed expert blocks are converted online into a preallocated FP8
+ * workspace that is reused).
+ *   e2m1, e8m0  MXFP4 matrices stacked [n_src][rows][K/2], [n_src][rows][K/32]
+ *   experts     int32 [n_experts] (device): source matrix index of each converted expert
+ *   ws_slots    int32 [n_experts] (device): destination slot of each
+ *   ws          uint8 workspace; slot s is the E4M3 matrix at ws + s*rows*K
+ *               (scale folded in: byte = E4M3_RNE_satfinite(E2M1 * 2^(E8M0-127)),
+ *               0x7F where the scale is NaN, which also sets NAN_SCALE)
+ *   ws_bytes    capacity; every slot must fit (checked on the device: a slot
+ *               that does not fit sets OVERFLOW and is skipped)
+ * Exact for every code when E8M0-127 lies in [-8, 6]. */
+MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* experts, int n_experts,
+                    int rows, int K, uint8_t* ws, size_t ws_bytes, const int32_t* ws_slots,
+                    uint32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------ expert matmuls
+ * For every expert e whose group is non-empty and selected (see below), for
+ * every permuted row p of the group (offsets[e] <= p < offsets[e+1]):
+ *   activation row a_p = act row (act_row ? act_row[p] / act_row_div : p), K elements
+ *   FC1_SWIGLU: g_n = W1_e[n] . a_p, u_n = W1_e[N+n] . a_p (fp32);
+ *               out[p][n] = silu(g_n) * u_n, n < N (N = I); weights have 2N rows
+ *   FC2:        out[p][n] = W2_e[n] . a_p, n < N (N = H); weights have N rows
+ * Formats: act_fmt BF16 or MXFP8 (act_scale = E8M0 [rows][K/32]); out_fmt BF16
+ * or F32, and MXFP8 for FC1 (out_scale receives E8M0 [rows][N/32]).  Rounding:
+ * out = RNE of the fp32 result into out_fmt.  Rows of unselected experts are
+ * left untouched.
+ *   ws   unused (NULL, 0).
+ */
+MOE_API int moe_w2_mm(int stage, int mode,
+              const void* act, int act_fmt, const uint8_t* act_scale,
+              const int32_t* act_row, int act_row_div,
+              const uint8_t* codes_k, const uint16_t* scales_k,  /* w2k [E][rows][K/4], [E][rows][K/32] */
+              const int32_t* offsets, const int32_t* expert_slot, /* nullable: skip e with expert_slot[e] >= 0 */
+              int E, int N, int K,
+              void* out, int out_fmt, uint8_t* out_scale,
+              void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
+
+/* As moe_w2_mm for MXFP4 weights, or for FP8 workspace weights.
+ * Weight source, exactly one of:
+ *   e2m1/e8m0 non-NULL: MXFP4 slots [S][rows][K/2], [S][rows][K/32]; expert e
+ *       uses slot expert_slot[e] (experts with expert_slot[e] < 0 are skipped;
+ *       expert_slot NULL means slot = e).
+ *   fp8_ws non-NULL: E4M3 workspace, expert e uses slot ws_slot_of_expert[e]
+ *       (rows*K bytes per slot, as written by mxfp4_to_fp8_ws); experts with a
+ *       negative slot are skipped.
+ * Only experts e in [expert_begin, expert_end) are processed. */
+MOE_API int moe_mxfp4_mm(int stage, int mode,
+                 const void* act, int act_fmt, const uint8_t* act_scale,
+                 const int32_t* act_row, int act_row_div,
+                 const uint8_t* e2m1, const uint8_t* e8m0,
+                 const uint8_t* fp8_ws, const int32_t* ws_slot_of_expert,
+                 const int32_t* offsets, const int32_t* expert_slot,
+                 int expert_begin, int expert_end,
+                 int E, int N, int K,
+                 void* out, int out_fmt, uint8_t* out_scale,
+                 void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------ combine
+ * out[t][n] = sum_{j=0..k-1} w[t][j] * y[inv[t*k+j]][n], accumulated in fp32 in
+ * ascending j, then rounded to out_fmt (BF16 or F32).  One owner per output
+ * row: deterministic, no atomics.  Assignments with inv < 0 contribute nothing.
+ *   y    [A][H] in y_fmt (BF16 or F32), permuted row order */
+MOE_API int moe_combine(const void* y, int y_fmt, const float* w, const int32_t* inv,
+                int T, int k, int H, void* out, int out_fmt, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
