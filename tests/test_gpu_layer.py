@@ -33,7 +33,11 @@ def _check_full(w, seed=0, mode=L.MODE_GEMV):
     y = bf16_to_f64(b.y)[host(b.inv)].reshape(w.T, w.k, w.H)
     diff = np.abs(y - ref["y"])
     assert np.mean(diff > 0) < (0.05 if prof == "fp8" else 2e-3)
-    assert np.max(diff) <= (TOL_FP8 if prof == "fp8" else 1e-2) * np.sqrt(np.mean(ref["y"] ** 2))
+    rms_y = np.sqrt(np.mean(ref["y"] ** 2))
+    if prof == "fp8":
+        assert np.max(diff) <= TOL_FP8 * rms_y
+    else:   # one bf16 ulp of the element itself, plus a flipped h's share
+        assert np.all(diff <= 2.0 ** -7 * np.abs(ref["y"]) + 1e-2 * rms_y)
     return err
 
 
