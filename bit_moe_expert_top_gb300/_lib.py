@@ -26,7 +26,7 @@ MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
 # every entry point declared in include/moe.h
 EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
-           "mxfp4_to_fp8_ws", "moe_w2_mm", "moe_mxfp4_mm", "moe_combine"]
+           "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_mxfp4_mm", "moe_combine"]
 
 
 class MoEError(RuntimeError):
@@ -44,13 +44,14 @@ _SIGS = {
     "moe_permute_workspace_size": (_S, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _S, _P, _P]),
     "moe_unpermute": (_I, [_P, _I, _P, _I, _I, _P, _P]),
-    "moe_w2_repack": (_I, [_P, _P, _L, _I, _P, _P, _P]),
-    "moe_dequant_w2": (_I, [_P, _P, _L, _I, _P, _P]),
+    "moe_w2_repack": (_I, [_P, _P, _L, _I, _I, _P, _P, _P]),
+    "moe_dequant_w2": (_I, [_P, _P, _L, _I, _I, _P, _P]),
     "moe_dequant_mxfp4": (_I, [_P, _P, _L, _I, _P, _P]),
     "mxfp4_to_fp8_ws": (_I, [_P, _P, _P, _I, _I, _I, _P, _S, _P, _P, _P]),
-    "moe_w2_mm": (_I, [_I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _S, _P, _P]),
-    "moe_mxfp4_mm": (_I, [_I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P,
-                          _P, _S, _P, _P]),
+    "moe_w2_mm_workspace_size": (_S, [_I, _I, _I, _I]),
+    "moe_w2_mm": (_I, [_I, _I, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _S, _P, _P]),
+    "moe_mxfp4_mm": (_I, [_I, _I, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
+                          _P, _P, _S, _P, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _I, _P]),
 }
 
@@ -127,12 +128,13 @@ def moe_unpermute(rows_perm, fmt, inv, rows, stream=None):
     _check(lib().moe_unpermute(_ptr(rows_perm), fmt, _ptr(inv), A, cols, _ptr(rows), _stream(stream)))
 
 
-def moe_w2_repack(codes, scales, rows, K, codes_k, scales_k, stream=None):
-    _check(lib().moe_w2_repack(_ptr(codes), _ptr(scales), rows, K, _ptr(codes_k), _ptr(scales_k), _stream(stream)))
+def moe_w2_repack(codes, scales, mats, R, K, codes_k, scales_k, stream=None):
+    _check(lib().moe_w2_repack(_ptr(codes), _ptr(scales), mats, R, K, _ptr(codes_k), _ptr(scales_k),
+                               _stream(stream)))
 
 
-def moe_dequant_w2(codes_k, scales_k, rows, K, out_bf16, stream=None):
-    _check(lib().moe_dequant_w2(_ptr(codes_k), _ptr(scales_k), rows, K, _ptr(out_bf16), _stream(stream)))
+def moe_dequant_w2(codes_k, scales_k, mats, R, K, out_bf16, stream=None):
+    _check(lib().moe_dequant_w2(_ptr(codes_k), _ptr(scales_k), mats, R, K, _ptr(out_bf16), _stream(stream)))
 
 
 def moe_dequant_mxfp4(e2m1, e8m0, rows, K, out_f32, stream=None):
@@ -146,19 +148,26 @@ def mxfp4_to_fp8_ws(e2m1, e8m0, experts, rows, K, ws, ws_slots, dev_err=None, st
                                  _ptr(ws_slots), _ptr(dev_err), _stream(stream)))
 
 
+def moe_w2_mm_workspace_size(stage, rows, N, K) -> int:
+    return int(lib().moe_w2_mm_workspace_size(stage, rows, N, K))
+
+
 def moe_w2_mm(stage, act, act_fmt, codes_k, scales_k, offsets, E, N, K, out, out_fmt, act_scale=None,
-              act_row=None, act_row_div=1, expert_slot=None, out_scale=None, mode=MODE_AUTO, dev_err=None,
-              stream=None):
-    _check(lib().moe_w2_mm(stage, mode, _ptr(act), act_fmt, _ptr(act_scale), _ptr(act_row), act_row_div,
+              act_row=None, act_row_div=1, expert_slot=None, out_scale=None, mode=MODE_AUTO, ws=None,
+              dev_err=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().moe_w2_mm(stage, mode, _ptr(act), act_fmt, _ptr(act_scale), act.shape[0], _ptr(act_row),
+                           act_row_div,
                            _ptr(codes_k), _ptr(scales_k), _ptr(offsets), _ptr(expert_slot), E, N, K, _ptr(out),
-                           out_fmt, _ptr(out_scale), None, 0, _ptr(dev_err), _stream(stream)))
+                           out_fmt, _ptr(out_scale), _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))
 
 
 def moe_mxfp4_mm(stage, act, act_fmt, offsets, E, N, K, out, out_fmt, e2m1=None, e8m0=None, fp8_ws=None,
                  ws_slot_of_expert=None, act_scale=None, act_row=None, act_row_div=1, expert_slot=None,
                  expert_begin=0, expert_end=None, out_scale=None, mode=MODE_AUTO, dev_err=None, stream=None):
     expert_end = E if expert_end is None else expert_end
-    _check(lib().moe_mxfp4_mm(stage, mode, _ptr(act), act_fmt, _ptr(act_scale), _ptr(act_row), act_row_div,
+    _check(lib().moe_mxfp4_mm(stage, mode, _ptr(act), act_fmt, _ptr(act_scale), act.shape[0], _ptr(act_row),
+                              act_row_div,
                               _ptr(e2m1), _ptr(e8m0), _ptr(fp8_ws), _ptr(ws_slot_of_expert), _ptr(offsets),
                               _ptr(expert_slot), expert_begin, expert_end, E, N, K, _ptr(out), out_fmt,
                               _ptr(out_scale), None, 0, _ptr(dev_err), _stream(stream)))

@@ -128,25 +128,25 @@ int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int
                      "moe_unpermute");
 }
 
-int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
+int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t mats, int R, int K, uint8_t* codes_k,
                   uint16_t* scales_k, void* stream) {
-  if (rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "moe_w2_repack: bad shape");
-  if (rows == 0) return MOE_OK;
+  if (mats < 0 || R < 0 || R % 4 || K <= 0 || K % 128) return fail(MOE_ERR_ARG, "moe_w2_repack: bad shape");
+  if (mats == 0 || R == 0) return MOE_OK;
   if (!codes || !scales || !codes_k || !scales_k || !aligned(codes, 4) || !aligned(codes_k, 4) ||
       !aligned(scales, 2) || !aligned(scales_k, 2))
     return fail(MOE_ERR_ARG, "moe_w2_repack: NULL or misaligned pointer");
   if (int r = check_device()) return r;
-  return cuda_status(launch_w2_repack(codes, scales, rows, K, codes_k, scales_k, static_cast<cudaStream_t>(stream)),
+  return cuda_status(launch_w2_repack(codes, scales, mats, R, K, codes_k, scales_k, static_cast<cudaStream_t>(stream)),
                      "moe_w2_repack");
 }
 
-int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out_bf16,
+int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t mats, int R, int K, uint16_t* out_bf16,
                    void* stream) {
-  if (rows < 0 || K <= 0 || K % 32) return fail(MOE_ERR_ARG, "moe_dequant_w2: bad shape");
-  if (rows == 0) return MOE_OK;
+  if (mats < 0 || R < 0 || R % 4 || K <= 0 || K % 128) return fail(MOE_ERR_ARG, "moe_dequant_w2: bad shape");
+  if (mats == 0 || R == 0) return MOE_OK;
   if (!codes_k || !scales_k || !out_bf16 || !aligned(codes_k, 4)) return fail(MOE_ERR_ARG, "moe_dequant_w2: pointer");
   if (int r = check_device()) return r;
-  return cuda_status(launch_dequant_w2(codes_k, scales_k, rows, K, out_bf16, static_cast<cudaStream_t>(stream)),
+  return cuda_status(launch_dequant_w2(codes_k, scales_k, mats, R, K, out_bf16, static_cast<cudaStream_t>(stream)),
                      "moe_dequant_w2");
 }
 
@@ -189,27 +189,40 @@ static int check_mm(const char* who, int stage, int mode, const void* act, int a
   return check_device();
 }
 
-int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, const int32_t* act_row,
-              int act_row_div, const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
+size_t moe_w2_mm_workspace_size(int stage, int rows, int N, int K) {
+  if ((stage != MOE_STAGE_FC1_SWIGLU && stage != MOE_STAGE_FC2) || rows < 0 || N <= 0 || K <= 0 || N % 128 ||
+      K % 128)
+    return 0;
+  return lut_workspace_bytes(stage, rows, N, K);
+}
+
+int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
+              const int32_t* act_row, int act_row_div, const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
               const int32_t* expert_slot, int E, int N, int K, void* out, int out_fmt, uint8_t* out_scale, void* ws,
               size_t ws_bytes, uint32_t* dev_err, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (int r = check_mm("moe_w2_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
     return r;
   if (!codes_k || !scales_k || !aligned(codes_k, 16) || !aligned(scales_k, 16))
     return fail(MOE_ERR_ARG, "moe_w2_mm: weights NULL or not 16-byte aligned");
+  if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_w2_mm: act_rows < 0");
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm: act_row_div < 1");
   MMArgs a{};
   a.stage = stage;
   a.act = act;
   a.act_fmt = act_fmt;
   a.act_scale = act_scale;
+  a.act_rows = act_rows;
+  a.mode = mode;
   a.act_row = act_row;
   a.act_row_div = act_row ? act_row_div : 1;
   a.wkind = kW2;
   a.wq = codes_k;
   a.wscale = scales_k;
+  a.ws = (ws && ws_bytes) ? ws : nullptr;
+  a.ws_bytes = ws_bytes;
+  a.ws_rows = a.ws ? lut_workspace_rows(stage, ws_bytes, N, K) : 0;
+  if (a.ws && !aligned(ws, 256)) return fail(MOE_ERR_ARG, "moe_w2_mm: ws must be 256-byte aligned");
+  if (a.ws && a.ws_rows < 1) return fail(MOE_ERR_WS_SMALL, "moe_w2_mm: workspace below one row");
   a.wslot_of = nullptr;  // 2-bit weights are indexed by expert
   a.select_map = expert_slot;
   a.select = expert_slot ? 1 : 0;
@@ -227,8 +240,8 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
   return cuda_status(launch_gemv(a, s), "moe_w2_mm");
 }
 
-int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, const int32_t* act_row,
-                 int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
+int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
+                 const int32_t* act_row, int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
                  const int32_t* ws_slot_of_expert, const int32_t* offsets, const int32_t* expert_slot,
                  int expert_begin, int expert_end, int E, int N, int K, void* out, int out_fmt, uint8_t* out_scale,
                  void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
@@ -237,6 +250,7 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
   if (int r = check_mm("moe_mxfp4_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
     return r;
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_row_div < 1");
+  if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_rows < 0");
   if (expert_begin < 0 || expert_end > E || expert_begin > expert_end)
     return fail(MOE_ERR_ARG, "moe_mxfp4_mm: bad expert range");
   const bool use_fp8 = fp8_ws != nullptr;
@@ -246,6 +260,8 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
   a.act = act;
   a.act_fmt = act_fmt;
   a.act_scale = act_scale;
+  a.act_rows = act_rows;
+  a.mode = mode;
   a.act_row = act_row;
   a.act_row_div = act_row ? act_row_div : 1;
   if (use_fp8) {

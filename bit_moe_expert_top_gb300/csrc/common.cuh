@@ -159,4 +159,30 @@ MOE_D int mx_scale_exp(float amax) {
   return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
+// ---------------------------------------------------------------- w2l layout
+// The 2-bit kernel layout keeps the canonical code bytes (4 codes per byte,
+// element i at bits 2(i%4)) but moves whole 32-bit words: a row's K is cut
+// into slices of SW elements (w2l_sw); inside a slice, lane l (of SW/16)
+// owns the word of elements 16l..16l+15, and the words of 4 consecutive rows
+// of one lane sit together.  Word (row, slice s, lane l) lands at
+//   s*(R*SW/16) + (row/4)*(4*SW/16) + l*4 + row%4          (in words, per matrix)
+// and bf16 scale (row, slice s, group g of the slice) at
+//   s*(R*SW/32) + (row/4)*(4*SW/32) + g*4 + row%4.
+// A block of 4*n rows of one slice is contiguous (one bulk copy), and a lane
+// reads its 4 rows' words with one 16-byte load.
+// Slice width: K itself up to 512, else the largest of 512/256/128 dividing K.
+MOE_HD int w2l_sw(int K) { return K <= 512 ? K : (K % 512 == 0 ? 512 : (K % 256 == 0 ? 256 : 128)); }
+
+MOE_HD int64_t w2l_word(int64_t row, int64_t R, int K, int64_t kw) {
+  // kw = canonical word index within the row (16 elements per word)
+  const int SW = w2l_sw(K);
+  const int64_t s = (kw * 16) / SW, l = ((kw * 16) % SW) / 16;
+  return s * (R * SW / 16) + (row / 4) * (4 * (SW / 16)) + l * 4 + row % 4;
+}
+MOE_HD int64_t w2l_scale(int64_t row, int64_t R, int K, int64_t g) {
+  const int SW = w2l_sw(K);
+  const int64_t s = (g * 32) / SW, gs = ((g * 32) % SW) / 32;
+  return s * (R * SW / 32) + (row / 4) * (4 * (SW / 32)) + gs * 4 + row % 4;
+}
+
 }  // namespace moe

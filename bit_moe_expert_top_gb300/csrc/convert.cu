@@ -13,59 +13,42 @@ namespace moe {
 
 namespace {
 
-MOE_D uint32_t rotl(uint32_t w, int r) { return __funnelshift_l(w, w, r); }
-
-// Canonical word (16 codes, element i at bits 2i, 2i+1; code c is the c-th
-// entry of {-4,-1,1,4}) -> w2k word: element 2q+h gets its "|entry| = 4" bit
-// at (8+16h-2q) mod 32 and its "entry < 0" bit at (15+16h-2q) mod 32.
-MOE_D uint32_t w2_repack_word(uint32_t w) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t c = (w >> (2 * i)) & 3u;
-    const uint32_t big = (c == 0u || c == 3u) ? 1u : 0u;
-    const uint32_t neg = (c < 2u) ? 1u : 0u;
-    const int q = i >> 1, h = i & 1;
-    const int pm = (8 + 16 * h - 2 * q + 32) & 31;
-    const int ps = (15 + 16 * h - 2 * q + 32) & 31;
-    out |= (big << pm) | (neg << ps);
-  }
-  return out;
-}
-
 __global__ void w2_repack_kernel(const uint32_t* __restrict__ codes, const __half* __restrict__ scales,
-                                 int64_t nwords, int64_t nscales, uint32_t* __restrict__ codes_k,
+                                 int64_t mats, int64_t R, int K, uint32_t* __restrict__ codes_k,
                                  uint16_t* __restrict__ scales_k) {
+  const int64_t wpr = K / 16, gpr = K / 32;
+  const int64_t nwords = mats * R * wpr, nsc = mats * R * gpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nwords; i += stride)
-    codes_k[i] = w2_repack_word(codes[i]);
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nscales; i += stride)
-    scales_k[i] = f32_to_bf16_rne(__half2float(scales[i]));
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nwords; i += stride) {
+    const int64_t m = i / (R * wpr), rem = i % (R * wpr), row = rem / wpr, kw = rem % wpr;
+    codes_k[m * R * wpr + w2l_word(row, R, K, kw)] = codes[i];
+  }
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nsc; i += stride) {
+    const int64_t m = i / (R * gpr), rem = i % (R * gpr), row = rem / gpr, g = rem % gpr;
+    scales_k[m * R * gpr + w2l_scale(row, R, K, g)] = f32_to_bf16_rne(__half2float(scales[i]));
+  }
 }
 
-// Exact dequantised value of w2k element (word w, element 2q+h) with bf16
-// scale bits sb: entry * scale.
-MOE_D float w2k_value(uint32_t w, int q, int h, uint32_t sb) {
-  const uint32_t r = rotl(w, 2 * q);
-  const uint32_t bits = h ? (r & 0x81000000u) : ((r << 16) & 0x81000000u);
-  const float quarter = __uint_as_float(bits | 0x3E800000u);  // entry / 4
-  return quarter * 4.0f * bf16_bits_to_f32(sb);
+// Exact dequantised value entry * scale as bf16 bits, element j (0..15) of a
+// canonical code word.
+MOE_D uint16_t w2_value_bf16(uint32_t w, int j, uint32_t sb) {
+  const uint32_t c = (w >> (2 * j)) & 3u;
+  const float entry = (c == 0u) ? -4.f : (c == 1u) ? -1.f : (c == 2u) ? 1.f : 4.f;
+  return f32_to_bf16_rne(entry * bf16_bits_to_f32(sb));
 }
 
 __global__ void dequant_w2_kernel(const uint32_t* __restrict__ codes_k, const uint16_t* __restrict__ scales_k,
-                                  int64_t ngroups, uint16_t* __restrict__ out) {
+                                  int64_t mats, int64_t R, int K, uint16_t* __restrict__ out) {
+  const int64_t wpr = K / 16;
+  const int64_t nwords = mats * R * wpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < ngroups; gi += stride) {
-    const uint32_t sb = scales_k[gi];
-    uint16_t* o = out + gi * 32;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nwords; i += stride) {
+    const int64_t m = i / (R * wpr), rem = i % (R * wpr), row = rem / wpr, kw = rem % wpr;
+    const uint32_t w = codes_k[m * R * wpr + w2l_word(row, R, K, kw)];
+    const uint32_t sb = scales_k[m * R * (K / 32) + w2l_scale(row, R, K, kw / 2)];
+    uint16_t* o = out + i * 16;
 #pragma unroll
-    for (int wd = 0; wd < 2; ++wd) {
-      const uint32_t w = codes_k[gi * 2 + wd];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) o[wd * 16 + 2 * q + h] = f32_to_bf16_rne(w2k_value(w, q, h, sb));
-    }
+    for (int j = 0; j < 16; ++j) o[j] = w2_value_bf16(w, j, sb);
   }
 }
 
@@ -149,22 +132,22 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
-                             uint16_t* scales_k, cudaStream_t s) {
-  const int64_t nwords = rows * (K / 16), nsc = rows * (K / 32);
+cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t mats, int64_t R, int K,
+                             uint8_t* codes_k, uint16_t* scales_k, cudaStream_t s) {
+  const int64_t nwords = mats * R * (K / 16);
   if (nwords == 0) return cudaSuccess;
   w2_repack_kernel<<<grid_for(nwords, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes),
-                                                         reinterpret_cast<const __half*>(scales), nwords, nsc,
+                                                         reinterpret_cast<const __half*>(scales), mats, R, K,
                                                          reinterpret_cast<uint32_t*>(codes_k), scales_k);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out,
-                              cudaStream_t s) {
-  const int64_t ng = rows * (K / 32);
-  if (ng == 0) return cudaSuccess;
-  dequant_w2_kernel<<<grid_for(ng, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes_k), scales_k, ng,
-                                                      out);
+cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t mats, int64_t R, int K,
+                              uint16_t* out, cudaStream_t s) {
+  const int64_t nw = mats * R * (K / 16);
+  if (nw == 0) return cudaSuccess;
+  dequant_w2_kernel<<<grid_for(nw, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes_k), scales_k, mats,
+                                                      R, K, out);
   return cudaGetLastError();
 }
 

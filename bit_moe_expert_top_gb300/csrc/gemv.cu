@@ -76,17 +76,17 @@ MOE_HD SmemLayout smem_layout(int stages, int stage_bytes, int G, int V, int E) 
   return l;
 }
 
-MOE_D uint32_t rotl(uint32_t w, int r) { return __funnelshift_l(w, w, r); }
+// Codebook entry of a canonical 2-bit code (ascending {-4,-1,1,4}), built
+// from its bits: |entry| = 4 when both bits agree, entry < 0 when bit 1 is 0.
+MOE_D float w2_entry(uint32_t c) {
+  const uint32_t big = ((c ^ (c >> 1)) & 1u) ^ 1u;
+  const uint32_t neg = ((c >> 1) & 1u) ^ 1u;
+  return __uint_as_float(0x3F800000u + (big << 24) | (neg << 31));
+}
 
-// Decoded pair of w2k weights q (elements 2q, 2q+1 of the word), as v/4 in
-// {+-0.25, +-1}: the pair's magnitude bits land on fp32 exponent bit 1 and
-// its sign bits on the sign bit.
+// The two entries of elements 2q, 2q+1 of a canonical code word.
 MOE_D float2 w2_pair(uint32_t w, int q) {
-  const uint32_t r = rotl(w, 2 * q);
-  float2 v;
-  v.x = __uint_as_float(((r << 16) & 0x81000000u) | 0x3E800000u);
-  v.y = __uint_as_float((r & 0x81000000u) | 0x3E800000u);
-  return v;
+  return make_float2(w2_entry(w >> (4 * q)), w2_entry(w >> (4 * q + 2)));
 }
 
 // Activations of one 32-element group for one token, as 16 fp32 pairs.
@@ -132,8 +132,13 @@ MOE_D void row_group_dot(const uint8_t* sq, const uint8_t* ss, int rr, int g, in
   for (int t = 0; t < kNT; ++t) acc[t] = make_float2(0.f, 0.f);
   float sc;
   if (WK == kW2) {
-    const uint2 wv = *reinterpret_cast<const uint2*>(sq + static_cast<size_t>(rr) * P.qrow_bytes + g * 8);
-    sc = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ss + (static_cast<size_t>(rr) * G + g) * 2));
+    // w2l stage layout: [slice][row quad][lane][4 rows] words, [slice][row quad][group][4 rows] scales
+    const int SW = w2l_sw(P.a.K), NLn = SW / 16, Gs = SW / 32, nq = WTraits<kW2>::kRS / 4;
+    const int sl = g / Gs, gs = g % Gs, q = rr >> 2, r = rr & 3;
+    const uint8_t* wb = sq + ((static_cast<size_t>(sl) * nq + q) * NLn + 2 * gs) * 16 + r * 4;
+    const uint2 wv = make_uint2(*reinterpret_cast<const uint32_t*>(wb), *reinterpret_cast<const uint32_t*>(wb + 16));
+    sc = bf16_bits_to_f32(
+        *reinterpret_cast<const uint16_t*>(ss + ((static_cast<size_t>(sl) * nq + q) * Gs + gs) * 8 + r * 2));
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t w = h ? wv.y : wv.x;
@@ -277,8 +282,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams P) {
         uint8_t* dq = ring + static_cast<size_t>(s) * P.stage_bytes;
         const uint32_t qb = RS * P.qrow_bytes, sb = RS * P.srow_bytes;
         mbar_arrive_expect_tx(&full[s], qb + sb);
-        bulk_g2s(dq, a.wq + grow * P.qrow_bytes, qb, &full[s]);
-        if (sb) bulk_g2s(dq + P.sq_bytes, static_cast<const uint8_t*>(a.wscale) + grow * P.srow_bytes, sb, &full[s]);
+        if (WK == kW2) {
+          // one copy per K slice: RS rows of a slice are contiguous in the w2l layout
+          const int SW = w2l_sw(K), nsl = K / SW;
+          const uint32_t qs = RS * SW / 4, ssz = RS * (SW / 32) * 2;
+          const uint8_t* wq_e = a.wq + static_cast<size_t>(slot) * P.rows_total * P.qrow_bytes;
+          const uint8_t* ws_e = static_cast<const uint8_t*>(a.wscale) + static_cast<size_t>(slot) * P.rows_total * P.srow_bytes;
+          for (int sl = 0; sl < nsl; ++sl) {
+            bulk_g2s(dq + sl * qs, wq_e + (static_cast<size_t>(sl) * P.rows_total + row0) * (SW / 4), qs, &full[s]);
+            bulk_g2s(dq + P.sq_bytes + sl * ssz,
+                     ws_e + (static_cast<size_t>(sl) * P.rows_total + row0) * (SW / 32) * 2, ssz, &full[s]);
+          }
+        } else {
+          bulk_g2s(dq, a.wq + grow * P.qrow_bytes, qb, &full[s]);
+          if (sb) bulk_g2s(dq + P.sq_bytes, static_cast<const uint8_t*>(a.wscale) + grow * P.srow_bytes, sb, &full[s]);
+        }
       }
     }
     return;
@@ -348,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams P) {
         if (tid < V) {
           const int rr = tid / kNT, t = tid % kNT;
           float v = (red2[tid] + red2[V + tid]) + (red2[2 * V + tid] + red2[3 * V + tid]);
-          if (WK == kW2) v *= 4.0f;  // codebook entries were decoded as entry/4
           const int orow = st * RS + rr;  // row within the item's 2*kOutBlk (FC1) or kOutBlk
           if (c0 + t < ntok) res[orow * kResPitch + c0 + t] = v;
         }
@@ -420,6 +437,13 @@ cudaError_t launch_t(const GemvParams& P0, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s) {
+  const bool want_gemm = a.mode == MOE_MODE_GEMM || (a.mode == MOE_MODE_AUTO && a.act_row == nullptr);
+  if (want_gemm && gemm_supported(a)) return launch_gemm_tc(a, a.act_rows, s);
+  if (a.ws && a.ws_rows > 0 && lut_supported(a)) return launch_lut_gemv(a, a.ws, s);
+  return launch_gemv_generic(a, s);
+}
+
+cudaError_t launch_gemv_generic(const MMArgs& a, cudaStream_t s) {
   GemvParams P;
   P.a = a;
   const bool fc1 = a.stage == MOE_STAGE_FC1_SWIGLU;

@@ -29,10 +29,10 @@ cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32
                            void* out, int out_fmt, cudaStream_t s);
 
 // ---- weight formats (convert.cu)
-cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K, uint8_t* codes_k,
-                             uint16_t* scales_k, cudaStream_t s);
-cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K, uint16_t* out,
-                              cudaStream_t s);
+cudaError_t launch_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t mats, int64_t R, int K,
+                             uint8_t* codes_k, uint16_t* scales_k, cudaStream_t s);
+cudaError_t launch_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t mats, int64_t R, int K,
+                              uint16_t* out, cudaStream_t s);
 cudaError_t launch_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K, float* out,
                                  cudaStream_t s);
 cudaError_t launch_mxfp4_to_fp8(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* experts, int n_experts,
@@ -47,6 +47,11 @@ struct MMArgs {
   const void* act;
   int act_fmt;
   const uint8_t* act_scale;
+  int act_rows;               // rows of act (bounds of the gathered row index)
+  void* ws;                   // caller workspace (LUT GEMV scratch), may be NULL
+  size_t ws_bytes;
+  int ws_rows;                // permuted rows the workspace covers
+  int mode;                   // MOE_MODE_*
   const int32_t* act_row;
   int act_row_div;
   int wkind;                  // WeightKind
@@ -64,6 +69,15 @@ struct MMArgs {
   uint8_t* out_scale;
   uint32_t* dev_err;
 };
+// Dispatch: the shared-memory LUT GEMV for 2-bit weights when the shape allows,
+// else the generic CUDA-core kernel.
 cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_generic(const MMArgs& a, cudaStream_t s);
+bool lut_supported(const MMArgs& a);
+size_t lut_workspace_bytes(int stage, int rows, int N, int K);
+int lut_workspace_rows(int stage, size_t bytes, int N, int K);
+cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s);
+bool gemm_supported(const MMArgs& a);
+cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 
 }  // namespace moe

@@ -306,69 +306,89 @@ cudaError_t launch_unpermute(const void* rows_perm, int fmt, const int32_t* inv,
 }
 
 // ------------------------------------------------------------------ combine
-// One warp per output row (token); each lane owns 8 consecutive columns per
-// 256-column step and accumulates the k rows in ascending slot order.
-template <bool kYF32, bool kOutF32>
-__global__ void combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
-                               const int32_t* __restrict__ inv, int T, int k, int H, void* __restrict__ out) {
-  const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += gridDim.x * (blockDim.x >> 5)) {
-    for (int base = 0; base < H; base += 256) {
-      const int c0 = base + lane * 8;
-      if (c0 >= H) continue;
-      float acc[8];
+// Grid (column blocks of 2048, tokens): thread i of block (cb, t) owns
+// columns cb*2048 + 8i .. +7 of token t and accumulates the k rows of its
+// token in ascending slot order; loads of four slots are issued together.
+template <bool kYF32>
+MOE_D void load8(const void* y, size_t off, float (&v)[8]) {
+  if (kYF32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) + off);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) + off));
+    const uint32_t wv[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int p = inv[static_cast<size_t>(t) * k + j];
-        if (p < 0) continue;
-        const float wj = w[static_cast<size_t>(t) * k + j];
-        float v[8];
-        if (kYF32) {
-          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) +
-                                                              static_cast<size_t>(p) * H + c0);
-          float4 a = __ldg(src), b = __ldg(src + 1);
-          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-          v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
-          uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
-                                                         static_cast<size_t>(p) * H + c0));
-          const uint32_t wv[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(wv[i] << 16);
-            v[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
-      }
-      if (kOutF32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<size_t>(t) * H + c0);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      } else {
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          o[i] = static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i])) |
-                 (static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i + 1])) << 16);
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + static_cast<size_t>(t) * H + c0) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-      }
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(wv[i] << 16);
+      v[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
     }
+  }
+}
+
+template <bool kYF32, bool kOutF32>
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
+                                                      const int32_t* __restrict__ inv, int T, int k, int H,
+                                                      void* __restrict__ out) {
+  const int t = blockIdx.y;
+  const int c0 = blockIdx.x * 2048 + threadIdx.x * 8;
+  if (t >= T || c0 >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const int32_t* iv = inv + static_cast<size_t>(t) * k;
+  const float* wt = w + static_cast<size_t>(t) * k;
+  int j = 0;
+  for (; j + 4 <= k; j += 4) {
+    float v[4][8];
+    int p[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      p[u] = iv[j + u];
+      if (p[u] >= 0) load8<kYF32>(y, static_cast<size_t>(p[u]) * H + c0, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (p[u] < 0) continue;
+      const float wj = wt[j + u];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[u][i], acc[i]);
+    }
+  }
+  for (; j < k; ++j) {
+    const int p = iv[j];
+    if (p < 0) continue;
+    float v[8];
+    load8<kYF32>(y, static_cast<size_t>(p) * H + c0, v);
+    const float wj = wt[j];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+  }
+  if (kOutF32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<size_t>(t) * H + c0);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  } else {
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i])) |
+             (static_cast<uint32_t>(f32_to_bf16_rne(acc[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + static_cast<size_t>(t) * H + c0) =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H,
                            void* out, int out_fmt, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int blocks = min((T + 7) / 8, device_info().sms * 8);
+  const dim3 grid((H + 2047) / 2048, T);
   const bool yf = y_fmt == MOE_FMT_F32, of = out_fmt == MOE_FMT_F32;
-  if (yf && of) combine_kernel<true, true><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else if (yf) combine_kernel<true, false><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else if (of) combine_kernel<false, true><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else combine_kernel<false, false><<<blocks, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  if (yf && of) combine_kernel<true, true><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else if (yf) combine_kernel<true, false><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else if (of) combine_kernel<false, true><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
+  else combine_kernel<false, false><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
   return cudaGetLastError();
 }
 

@@ -47,12 +47,13 @@ class StepBuffers:
     x_perm: Optional[torch.Tensor]
     x_perm_scale: Optional[torch.Tensor]
     dev_err: torch.Tensor
+    ws: Optional[torch.Tensor] = None
 
 
 class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
-                 out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO):
+                 out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
@@ -60,6 +61,7 @@ class MoELayer:
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
+        self.gemm_min_rows = gemm_min_rows
         dev = self.device
         if fmt in ("w2", "mixed"):
             c1, s1, c2, s2 = w2
@@ -70,8 +72,7 @@ class MoELayer:
             for src_c, src_s, dc, ds, K in ((c1, s1, self.c1k, self.s1k, H), (c2, s2, self.c2k, self.s2k, I)):
                 tc = _dev(src_c, dev)
                 ts = _dev(src_s.view(np.int16), dev)
-                rows = src_c.shape[0] * src_c.shape[1]
-                L.moe_w2_repack(tc, ts, rows, K, dc, ds)
+                L.moe_w2_repack(tc, ts, src_c.shape[0], src_c.shape[1], K, dc, ds)
                 del tc, ts
         if fmt in ("mixed", "fp8"):
             q1, s1, q2, s2 = mx
@@ -96,10 +97,18 @@ class MoELayer:
         torch.cuda.synchronize(dev)
 
     # ------------------------------------------------------------ buffers
+    def use_gemm(self, T: int) -> bool:
+        """Prefill-sized 2-bit steps run FC1/FC2 on the tensor cores over
+        permuted (gathered) activation rows; decode-sized ones on the GEMV."""
+        if self.fmt != "w2" or self.mode == L.MODE_GEMV:
+            return False
+        return self.mode == L.MODE_GEMM or T * self.k >= self.gemm_min_rows
+
     def buffers(self, T: int) -> StepBuffers:
         dev, E, H, I, k = self.device, self.E, self.H, self.I, self.k
         A = T * k
         fp8 = self.fmt == "fp8"
+        gather = self.use_gemm(T)
         return StepBuffers(
             ids=torch.empty((T, k), dtype=torch.int32, device=dev),
             w=torch.empty((T, k), dtype=torch.float32, device=dev),
@@ -110,10 +119,22 @@ class MoELayer:
             h_scale=torch.empty((A, I // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             y=torch.empty((A, H), dtype=torch.int16, device=dev),
             out=torch.empty((T, H), dtype=torch.float32 if self.out_fmt == L.FMT_F32 else torch.int16, device=dev),
-            x_perm=torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else None,
+            x_perm=(torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else
+                    torch.empty((A, H), dtype=torch.int16, device=dev) if gather else None),
             x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
+            ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed") and not gather else None,
         )
+
+    def _gemv_ws(self, A: int, cap_bytes: int = 1 << 30) -> Optional[torch.Tensor]:
+        """Zero-filled scratch of the 2-bit decode GEMV (FC1 and FC2 share it:
+        the calls run one after the other on the stream).  Decode-sized steps
+        need a few MB; beyond `cap_bytes` the GEMV runs without scratch."""
+        n = max(L.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, A, self.I, self.H),
+                L.moe_w2_mm_workspace_size(L.STAGE_FC2, A, self.H, self.I))
+        if n > cap_bytes:
+            return None
+        return torch.zeros((n + 3) // 4, dtype=torch.int32, device=self.device)
 
     # ------------------------------------------------------------ one step
     def step(self, x: torch.Tensor, logits: torch.Tensor, b: StepBuffers, ev: Optional[list] = None) -> torch.Tensor:
@@ -129,12 +150,21 @@ class MoELayer:
             L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
                           x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
             self._fp8_experts(b)
+        elif self.use_gemm(T):
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
+                          dev_err=b.dev_err)
+            with self._timed("w2_fc1_gemm"):
+                L.moe_w2_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
+                            L.FMT_BF16, mode=L.MODE_GEMM, dev_err=b.dev_err)
+            with self._timed("w2_fc2_gemm"):
+                L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                            mode=L.MODE_GEMM, dev_err=b.dev_err)
         else:
             L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
             with self._timed("w2_fc1"):
                 L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
                             L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
-                            mode=self.mode, dev_err=b.dev_err)
+                            mode=self.mode, ws=b.ws, dev_err=b.dev_err)
             if self.fmt == "mixed":
                 with self._timed("mx_fc1"):
                     L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
@@ -142,7 +172,7 @@ class MoELayer:
                                    expert_slot=self.expert_slot, mode=self.mode, dev_err=b.dev_err)
             with self._timed("w2_fc2"):
                 L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
-                            expert_slot=self.expert_slot, mode=self.mode, dev_err=b.dev_err)
+                            expert_slot=self.expert_slot, mode=self.mode, ws=b.ws, dev_err=b.dev_err)
             if self.fmt == "mixed":
                 with self._timed("mx_fc2"):
                     L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
@@ -152,17 +182,27 @@ class MoELayer:
         return b.out
 
     class _Timer:
+        """Event pair around one library call; recorded as timing nodes when
+        the step is being captured into a CUDA graph (external events)."""
+
         def __init__(self, ev, label):
             self.ev, self.label = ev, label
 
+        @staticmethod
+        def _event():
+            try:
+                return torch.cuda.Event(enable_timing=True, external=True)
+            except TypeError:
+                return torch.cuda.Event(enable_timing=True)
+
         def __enter__(self):
             if self.ev is not None:
-                self.s = torch.cuda.Event(enable_timing=True)
+                self.s = self._event()
                 self.s.record()
 
         def __exit__(self, *exc):
             if self.ev is not None:
-                e = torch.cuda.Event(enable_timing=True)
+                e = self._event()
                 e.record()
                 self.ev.append((self.label, self.s, e))
 

@@ -46,7 +46,7 @@
  *  - MXFP4 (OCP MX v1.0): E2M1 nibbles, element 2i in the LOW nibble of byte
  *    i; one E8M0 byte per 32 consecutive K elements, [rows][K/32]; value =
  *    E2M1 * 2^(E8M0-127); E8M0 = 255 is NaN.
- *  - moe_w2_mm reads the 2-bit weights in the "w2k" kernel layout written once
+ *  - moe_w2_mm reads the 2-bit weights in the "w2l" kernel layout written once
  *    by moe_w2_repack (same byte sizes; see there).
  *
  * Shape limits: 1 <= k <= E <= 1024, k <= 32; H and I multiples of 128;
@@ -150,21 +150,25 @@ MOE_API int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, in
                   void* rows, void* stream);
 
 /* ------------------------------------------------------------------ weights
- * Rewrite canonical 2-bit weights into the w2k kernel layout (run once, at load).
- *   codes   uint8 [rows][K/4] canonical;   scales fp16 [rows][K/32]
- *   codes_k uint8 [rows][K/4] out;         scales_k bf16 [rows][K/32] out
- * w2k: every 32-bit word still holds 16 consecutive K elements, with the two
- * bits of element 2q+h (q < 8, h < 2) moved to bit (8+16h-2q) mod 32 (set when
- * |entry| = 4) and bit (15+16h-2q) mod 32 (set when entry < 0), so rotating
- * the word left by 2q puts the pair's bits where a bf16 pair's exponent bit 1
- * and sign bits are.  Scales become RNE_bf16(scale).  `rows` counts all rows of
- * all experts (e.g. E*2I). */
-MOE_API int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t rows, int K,
+ * Rewrite canonical 2-bit weights into the w2l kernel layout (run once, at load).
+ *   codes   uint8 [mats][R][K/4] canonical;   scales fp16 [mats][R][K/32]
+ *   codes_k uint8 [mats][R][K/4] out;         scales_k bf16 [mats][R][K/32] out
+ * w2l keeps the canonical code bytes but moves whole 32-bit words (16
+ * elements): K is cut into slices of SW elements (SW = K if K <= 512, else the
+ * largest of 512/256/128 dividing K); word (row, slice s, lane l) — elements
+ * s*SW + 16l .. +15 of the row — is stored at word index
+ *   s*(R*SW/16) + (row/4)*(4*SW/16) + 4l + row%4
+ * of its matrix, and scale (row, slice s, group g of the slice) at
+ *   s*(R*SW/32) + (row/4)*(4*SW/32) + 4g + row%4,
+ * converted to RNE_bf16(fp16 scale) (the scale the dequantised weights use).
+ * Any block of 4n rows of one slice is then contiguous.  `mats` counts the
+ * stacked matrices (E), R the rows of one (2I for W1, H for W2); R % 4 == 0. */
+MOE_API int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t mats, int R, int K,
                   uint8_t* codes_k, uint16_t* scales_k, void* stream);
 
-/* Exact dequantised values (bf16 bit patterns [rows][K]) of w2k weights:
- * entry * RNE_bf16(scale) — what the GEMM tiles hold. */
-MOE_API int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t rows, int K,
+/* Exact dequantised values (bf16 bit patterns [mats][R][K]) of w2l weights:
+ * entry * RNE_bf16(scale), the values the expert matmuls compute with. */
+MOE_API int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t mats, int R, int K,
                    uint16_t* out_bf16, void* stream);
 
 /* Exact dequantised MXFP4 values as float [rows][K] (NaN where the scale is 255). */
@@ -190,7 +194,9 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
 /* ------------------------------------------------------------------ expert matmuls
  * For every expert e whose group is non-empty and selected (see below), for
  * every permuted row p of the group (offsets[e] <= p < offsets[e+1]):
- *   activation row a_p = act row (act_row ? act_row[p] / act_row_div : p), K elements
+ *   activation row a_p = act row (act_row ? act_row[p] / act_row_div : p), K elements;
+ *   act holds act_rows rows (T for token rows read through act_row, A for
+ *   permuted rows); a row index outside [0, act_rows) sets BAD_ID
  *   FC1_SWIGLU: g_n = W1_e[n] . a_p, u_n = W1_e[N+n] . a_p (fp32);
  *               out[p][n] = silu(g_n) * u_n, n < N (N = I); weights have 2N rows
  *   FC2:        out[p][n] = W2_e[n] . a_p, n < N (N = H); weights have N rows
@@ -198,12 +204,26 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * or F32, and MXFP8 for FC1 (out_scale receives E8M0 [rows][N/32]).  Rounding:
  * out = RNE of the fp32 result into out_fmt.  Rows of unselected experts are
  * left untouched.
- *   ws   unused (NULL, 0).
+ * Modes: GEMV = CUDA-core kernels (2-bit: shared-memory partial-sum tables
+ * with the K dimension split over CTAs; MXFP4 / FP8: register decode); GEMM =
+ * tcgen05 tensor-core kernel (2-bit weights, bf16 activations already
+ * permuted: act_row must be NULL); AUTO = GEMM when act_row is NULL and the
+ * shape is supported, else GEMV.
+ *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
+ *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
+ *        256-byte aligned, ZERO-FILLED before its first use; every successful
+ *        call leaves it zero-filled again (after a MOE_DEVERR_TIMEOUT, zero it).
+ *        With ws == NULL the 2-bit GEMV uses the slower register-decode kernel.
+ *        A row beyond the workspace's capacity sets OVERFLOW and is skipped.
+ *        Calls that share one workspace must not overlap on the GPU.
+ *   ws (moe_mxfp4_mm): unused (NULL, 0).
  */
+MOE_API size_t moe_w2_mm_workspace_size(int stage, int rows, int N, int K);
+
 MOE_API int moe_w2_mm(int stage, int mode,
-              const void* act, int act_fmt, const uint8_t* act_scale,
+              const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
               const int32_t* act_row, int act_row_div,
-              const uint8_t* codes_k, const uint16_t* scales_k,  /* w2k [E][rows][K/4], [E][rows][K/32] */
+              const uint8_t* codes_k, const uint16_t* scales_k,  /* w2l [E][rows][K/4], [E][rows][K/32] */
               const int32_t* offsets, const int32_t* expert_slot, /* nullable: skip e with expert_slot[e] >= 0 */
               int E, int N, int K,
               void* out, int out_fmt, uint8_t* out_scale,
@@ -219,7 +239,7 @@ MOE_API int moe_w2_mm(int stage, int mode,
  *       negative slot are skipped.
  * Only experts e in [expert_begin, expert_end) are processed. */
 MOE_API int moe_mxfp4_mm(int stage, int mode,
-                 const void* act, int act_fmt, const uint8_t* act_scale,
+                 const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
                  const int32_t* act_row, int act_row_div,
                  const uint8_t* e2m1, const uint8_t* e8m0,
                  const uint8_t* fp8_ws, const int32_t* ws_slot_of_expert,

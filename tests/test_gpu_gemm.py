@@ -1,0 +1,81 @@
+"""Parity of the tcgen05 tensor-core expert matmuls (MODE_GEMM) against the
+oracle, through the C ABI (GPU).
+
+Two kinds of checks:
+  * the whole layer at the problem's output gate (max|err| <= 2e-2 * RMS) on
+    shapes with several 128-row tiles per group, partial tiles, BN = 128 and
+    256 output blocks and K slices of 128 / 384 / 512;
+  * FC1 and FC2 alone with fp32 outputs against the exact (fp64) sums of the
+    same bf16 operands, element by element at 1e-4 * RMS: this checks the
+    tensor-core arithmetic itself, free of the bf16 rounding flips that an
+    accumulation-order difference can cause in h and y.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_moe_expert_top_gb300 import _lib as L
+from bit_moe_expert_top_gb300 import synth
+from oracle import codecs as C
+from oracle import moe as M
+
+from tests._gpu import DEV, dev, host, make_layer
+from tests.test_gpu_layer import _check_full, _check_sampled
+
+pytestmark = pytest.mark.gpu
+
+
+def test_gemm_tiny_full_parity():
+    err = _check_full(synth.get_workload("tiny"), mode=L.MODE_GEMM)
+    assert err < 1e-3
+
+
+@pytest.mark.parametrize("E,H,I,k,T", [(16, 1024, 512, 4, 100), (4, 512, 256, 4, 301), (8, 256, 128, 8, 1),
+                                       (3, 384, 640, 3, 77), (4, 512, 384, 4, 250)])
+def test_gemm_tiles_and_ragged_tail(E, H, I, k, T):
+    w = synth.get_workload("tiny").replace(E=E, H=H, I=I, k=k, T=T, logits="uniform")
+    _check_full(w, mode=L.MODE_GEMM)
+
+
+@pytest.mark.parametrize("E,H,I,k,T", [(4, 512, 384, 2, 400), (8, 1024, 512, 4, 260), (3, 384, 640, 3, 77)])
+def test_gemm_stages_exact_sums(E, H, I, k, T):
+    w = synth.get_workload("tiny").replace(E=E, H=H, I=I, k=k, T=T, logits="uniform")
+    ml, acc, _ = make_layer(w, mode=L.MODE_GEMM)
+    x = synth.make_x(w)
+    logits = synth.make_logits(w, x_bits=x)
+    ids, _, _ = M.route(logits, k)
+    off, perm, inv = M.permute(ids, E)
+    A = T * k
+    xp = C.bf16_bits_to_f64(x)[perm // k]                       # permuted activation rows
+    xp_bits = C.f32_to_bf16_bits(xp.astype(np.float32))
+    d_off = dev(off)
+    # FC1 with fp32 output: h_f32 = silu(g) * u, g/u exact sums rounded once to fp32
+    h32 = torch.empty((A, I), dtype=torch.float32, device=DEV)
+    L.moe_w2_mm(L.STAGE_FC1_SWIGLU, dev(xp_bits.view(np.int16)), L.FMT_BF16, ml.c1k, ml.s1k, d_off, E, I, H, h32,
+                L.FMT_F32, mode=L.MODE_GEMM)
+    want_h = np.zeros((A, I))
+    for e in range(E):
+        rows = slice(off[e], off[e + 1])
+        W1, W2 = acc(e)
+        g = C.to_f32(xp[rows] @ W1[:I].T)
+        u = C.to_f32(xp[rows] @ W1[I:].T)
+        want_h[rows] = M.silu(g) * u
+    got_h = host(h32).astype(np.float64)
+    rms_h = np.sqrt(np.mean(want_h ** 2))
+    assert np.max(np.abs(got_h - want_h)) <= 1e-4 * rms_h
+    # FC2 with fp32 output on bf16 h (the oracle's h)
+    h_bits = C.f32_to_bf16_bits(want_h.astype(np.float32))
+    hval = C.bf16_bits_to_f64(h_bits)
+    y32 = torch.empty((A, H), dtype=torch.float32, device=DEV)
+    L.moe_w2_mm(L.STAGE_FC2, dev(h_bits.view(np.int16)), L.FMT_BF16, ml.c2k, ml.s2k, d_off, E, H, I, y32,
+                L.FMT_F32, mode=L.MODE_GEMM)
+    want_y = np.zeros((A, H))
+    for e in range(E):
+        rows = slice(off[e], off[e + 1])
+        want_y[rows] = hval[rows] @ acc(e)[1].T
+    rms_y = np.sqrt(np.mean(want_y ** 2))
+    assert np.max(np.abs(host(y32).astype(np.float64) - want_y)) <= 1e-4 * rms_y
+
+
+def test_gemm_prefill_bf16_full_size_sampled():
+    _check_sampled("prefill_bf16", [0, 4099, 8191], mode=L.MODE_GEMM)

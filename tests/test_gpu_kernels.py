@@ -34,9 +34,9 @@ def test_w2_repack_dequant_exhaustive():
     scales[0, :8] = np.array([6e-8, 1e-5, 1.0 + 2 ** -8, 0.0, 65504, 1e-7, 3.0, 1.0 + 3 * 2 ** -9], np.float16)
     ck = torch.empty((rows, K // 4), dtype=torch.uint8, device=DEV)
     sk = torch.empty((rows, K // 32), dtype=torch.int16, device=DEV)
-    L.moe_w2_repack(dev(codes), dev(scales.view(np.int16)), rows, K, ck, sk)
+    L.moe_w2_repack(dev(codes), dev(scales.view(np.int16)), 1, rows, K, ck, sk)
     out = torch.empty((rows, K), dtype=torch.int16, device=DEV)
-    L.moe_dequant_w2(ck, sk, rows, K, out)
+    L.moe_dequant_w2(ck, sk, 1, rows, K, out)
     got = C.bf16_bits_to_f64(host(out).view(np.uint16))
     want = C.decode_w2(codes, scales)
     assert np.array_equal(got, want)

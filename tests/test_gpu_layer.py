@@ -32,7 +32,8 @@ def _check_full(w, seed=0, mode=L.MODE_GEMV):
     # by about one bf16 ulp of h times a W2 row)
     y = bf16_to_f64(b.y)[host(b.inv)].reshape(w.T, w.k, w.H)
     diff = np.abs(y - ref["y"])
-    assert np.mean(diff > 0) < (0.05 if prof == "fp8" else 2e-3)
+    # tensor-core accumulation rounds differently from an fp32 FMA chain: more flips
+    assert np.mean(diff > 0) < (0.05 if prof == "fp8" else (3e-2 if mode == L.MODE_GEMM else 2e-3))
     rms_y = np.sqrt(np.mean(ref["y"] ** 2))
     if prof == "fp8":
         assert np.max(diff) <= TOL_FP8 * rms_y
@@ -71,9 +72,9 @@ def test_fp8_layer_nan_scale_flagged():
     assert L.moe_get_error(b.dev_err) & L.DEVERR_NAN_SCALE
 
 
-def _check_sampled(name, tokens, seed=0):
+def _check_sampled(name, tokens, seed=0, mode=L.MODE_GEMV):
     w = synth.get_workload(name)
-    ml, acc, prof = make_layer(w, seed)
+    ml, acc, prof = make_layer(w, seed, mode=mode)
     x = synth.make_x(w, seed)
     logits = synth.make_logits(w, seed, x_bits=x)
     out, b = run_layer(ml, x, logits)
