@@ -437,7 +437,10 @@ cudaError_t launch_t(const GemvParams& P0, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s) {
-  const bool want_gemm = a.mode == MOE_MODE_GEMM || (a.mode == MOE_MODE_AUTO && a.act_row == nullptr);
+  // AUTO: the tensor-core GEMM for prefill-sized calls over permuted rows; the
+  // GEMV for decode-sized ones (one 128-row tile per expert would be mostly idle)
+  const bool want_gemm =
+      a.mode == MOE_MODE_GEMM || (a.mode == MOE_MODE_AUTO && a.act_row == nullptr && a.act_rows >= 2048);
   if (want_gemm && gemm_supported(a)) return launch_gemm_tc(a, a.act_rows, s);
   if (a.ws && a.ws_rows > 0 && lut_supported(a)) return launch_lut_gemv(a, a.ws, s);
   return launch_gemv_generic(a, s);

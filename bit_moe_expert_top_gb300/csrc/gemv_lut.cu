@@ -187,49 +187,57 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&flags[0]) != 0; };
 
+  // stages are issued in groups of 4, one per producer lane: a multiple of 4 ring slots
+  const int S = stages & ~3;
+
   if (warp == kLutWarps) {
-    // ================= producer: ring of 32-row stages of the item's K slice =================
-    if (lane == 0 && i_beg < i_end) {
+    // ================= producer: lanes 0..3 each issue one 32-row stage of a group of 4 =================
+    if (lane < 4 && i_beg < i_end) {
       const int64_t mat_bytes = static_cast<int64_t>(P.R) * (P.K / 4);  // codes bytes per expert
       const int64_t mat_scales = static_cast<int64_t>(P.R) * (P.K / 32);
       const int64_t slice_codes = static_cast<int64_t>(P.R) * SW / 4;
       const int64_t slice_scales = static_cast<int64_t>(P.R) * G;
-      uint32_t L = 0;
-      int s = 0;
+      const int nstages = (i_end - i_beg) * NST;
+      int s0 = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int i = i_beg; i < i_end && ok; ++i) {
-        int e, t, sl, rb;
-        decode(i, e, t, sl, rb);
-        for (int st = 0; st < NST; ++st, ++L) {
+      int issued = 0;
+      for (int L0 = 0; L0 < nstages && ok; L0 += 4) {
+        const int L = L0 + lane;
+        if (L < nstages) {
+          const int i = i_beg + L / NST, st = L % NST;
+          int e, t, sl, rb;
+          decode(i, e, t, sl, rb);
           int row0;
           if (fc1) row0 = (st < NST / 2) ? rb * (RPI / 2) + st * kStageRows : P.N + rb * (RPI / 2) + (st - NST / 2) * kStageRows;
           else row0 = rb * RPI + st * kStageRows;
-          if (L >= static_cast<uint32_t>(stages) && !mbar_wait(&empty[s], ph ^ 1u)) {
+          const int slot = s0 + lane;
+          if (L >= S && !mbar_wait(&empty[slot], ph ^ 1u)) {
             abort_all();
             ok = false;
-            break;
-          }
-          if (aborted()) {
+          } else if (aborted()) {
             ok = false;
-            break;
-          }
-          const uint8_t* gc = P.codes + e * mat_bytes + sl * slice_codes + static_cast<int64_t>(row0 / 4) * SW;
-          const uint8_t* gs = reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + sl * slice_scales +
-                                                               static_cast<int64_t>(row0 / 4) * (G * 4));
-          uint8_t* d = ring + static_cast<size_t>(s) * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          bulk_g2s(d, gc, codes_stage, &full[s]);
-          bulk_g2s(d + codes_stage, gs, scales_stage, &full[s]);
-          if (++s == stages) {
-            s = 0;
-            ph ^= 1u;
+          } else {
+            const uint8_t* gc = P.codes + e * mat_bytes + sl * slice_codes + static_cast<int64_t>(row0 / 4) * SW;
+            const uint8_t* gs = reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + sl * slice_scales +
+                                                                 static_cast<int64_t>(row0 / 4) * (G * 4));
+            uint8_t* d = ring + static_cast<size_t>(slot) * stage_bytes;
+            mbar_arrive_expect_tx(&full[slot], stage_bytes);
+            bulk_g2s(d, gc, codes_stage, &full[slot]);
+            bulk_g2s(d + codes_stage, gs, scales_stage, &full[slot]);
+            issued = L + 1;
           }
         }
+        ok = __all_sync(0x0000000fu, ok);
+        s0 += 4;
+        if (s0 == S) {
+          s0 = 0;
+          ph ^= 1u;
+        }
       }
-      if (!ok) {  // copies already issued complete (bounded) before the CTA may leave
-        const uint32_t first = L > static_cast<uint32_t>(stages) ? L - stages : 0;
-        for (uint32_t l = first; l < L; ++l) (void)mbar_wait(&full[l % stages], (l / stages) & 1);
+      if (!ok) {  // this lane's copies already issued complete (bounded) before the CTA may leave
+        for (int l = lane; l < issued; l += 4)
+          if (l + S >= issued) (void)mbar_wait(&full[l % S], (l / S) & 1);
       }
     }
     return;
@@ -253,14 +261,15 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
       }
       int* cnt = P.counters + static_cast<size_t>(p) * NB + rb;
       if (lane == 0) {
-        __threadfence();  // this CTA's slice sums (published through pub_bar) before the count
-        const int old = atomicAdd(cnt, 1);
+        // release: this CTA's slice sums (published to this warp through pub_bar)
+        // precede the count; acquire: the other slices' sums precede reading them
+        int old;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
         s_last = (old == NSL - 1);
       }
       __syncwarp();
       const bool last = *reinterpret_cast<volatile int*>(&s_last) != 0;
       if (last) {
-        __threadfence();  // the other slices' sums, published before their counts
         const float* sc = P.scratch + (static_cast<size_t>(p) * NB + rb) * NSL * RPI;
         for (int o = lane; o < outs_item; o += 32) {
           float v = 0.f, u = 0.f;
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
       if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
       for (int r = 0; r < 4; ++r) tile[(st * 4 + r) * 33 + lane] = r4[r];
-      if (++s == stages) {
+      if (++s == S) {
         s = 0;
         ph ^= 1u;
       }

@@ -207,8 +207,8 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * Modes: GEMV = CUDA-core kernels (2-bit: shared-memory partial-sum tables
  * with the K dimension split over CTAs; MXFP4 / FP8: register decode); GEMM =
  * tcgen05 tensor-core kernel (2-bit weights, bf16 activations already
- * permuted: act_row must be NULL); AUTO = GEMM when act_row is NULL and the
- * shape is supported, else GEMV.
+ * permuted: act_row must be NULL); AUTO = GEMM when act_row is NULL,
+ * act_rows >= 2048 and the shape is supported, else GEMV.
  *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
  *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
  *        256-byte aligned, ZERO-FILLED before its first use; every successful
