@@ -26,7 +26,9 @@ MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
 # every entry point declared in include/moe.h
 EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
-           "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_mxfp4_mm", "moe_combine"]
+           "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
+           "moe_combine"]
+W2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class MoEError(RuntimeError):
@@ -50,6 +52,7 @@ _SIGS = {
     "mxfp4_to_fp8_ws": (_I, [_P, _P, _P, _I, _I, _I, _P, _S, _P, _P, _P]),
     "moe_w2_mm_workspace_size": (_S, [_I, _I, _I, _I]),
     "moe_w2_mm": (_I, [_I, _I, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _S, _P, _P]),
+    "moe_w2_mm_noalloc": (_I, [_I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P]),
     "moe_mxfp4_mm": (_I, [_I, _I, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
                           _P, _P, _S, _P, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _I, _P]),
@@ -160,6 +163,14 @@ def moe_w2_mm(stage, act, act_fmt, codes_k, scales_k, offsets, E, N, K, out, out
                            act_row_div,
                            _ptr(codes_k), _ptr(scales_k), _ptr(offsets), _ptr(expert_slot), E, N, K, _ptr(out),
                            out_fmt, _ptr(out_scale), _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))
+
+
+def moe_w2_mm_noalloc(stage, act, codes_k, scales_k, offsets, E, N, K, rows, out, out_fmt, act_row=None,
+                      act_row_div=1, expert_slot=None, dev_err=None, stream=None):
+    """moe_w2_mm's table GEMV on the library's own fixed scratch (bf16 act)."""
+    _check(lib().moe_w2_mm_noalloc(stage, _ptr(act), act.shape[0], _ptr(act_row), act_row_div, _ptr(codes_k),
+                                   _ptr(scales_k), _ptr(offsets), _ptr(expert_slot), E, N, K, rows, _ptr(out),
+                                   out_fmt, _ptr(dev_err), _stream(stream)))
 
 
 def moe_mxfp4_mm(stage, act, act_fmt, offsets, E, N, K, out, out_fmt, e2m1=None, e8m0=None, fp8_ws=None,

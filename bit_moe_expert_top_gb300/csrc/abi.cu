@@ -240,6 +240,54 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
   return cuda_status(launch_gemv(a, s), "moe_w2_mm");
 }
 
+int moe_w2_mm_noalloc(int stage, const void* act, int act_rows, const int32_t* act_row, int act_row_div,
+                      const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
+                      const int32_t* expert_slot, int E, int N, int K, int rows, void* out, int out_fmt,
+                      uint32_t* dev_err, void* stream) {
+  if (int r = check_mm("moe_w2_mm_noalloc", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, offsets, E, N, K, out,
+                       out_fmt, nullptr))
+    return r;
+  if (out_fmt == MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: out_fmt must be BF16 or F32");
+  if (!codes_k || !scales_k || !aligned(codes_k, 16) || !aligned(scales_k, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: weights NULL or not 16-byte aligned");
+  if (act_rows < 0 || rows < 0) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: act_rows or rows < 0");
+  if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: act_row_div < 1");
+  if (rows == 0) return MOE_OK;
+  const size_t need = lut_workspace_bytes(stage, rows, N, K);
+  if (need > MOE_W2_NOALLOC_SCRATCH_BYTES) {
+    std::snprintf(g_err, sizeof(g_err),
+                  "moe_w2_mm_noalloc: %d rows need %zu bytes of scratch, above the fixed %u bytes; use moe_w2_mm "
+                  "with a workspace",
+                  rows, need, MOE_W2_NOALLOC_SCRATCH_BYTES);
+    return MOE_ERR_WS_SMALL;
+  }
+  MMArgs a{};
+  a.stage = stage;
+  a.act = act;
+  a.act_fmt = MOE_FMT_BF16;
+  a.act_rows = act_rows;
+  a.mode = MOE_MODE_GEMV;
+  a.act_row = act_row;
+  a.act_row_div = act_row ? act_row_div : 1;
+  a.wkind = kW2;
+  a.wq = codes_k;
+  a.wscale = scales_k;
+  a.select_map = expert_slot;
+  a.select = expert_slot ? 1 : 0;
+  a.offsets = offsets;
+  a.expert_begin = 0;
+  a.expert_end = E;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.out_fmt = out_fmt;
+  a.dev_err = dev_err;
+  if (!lut_supported(a))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_w2_mm_noalloc: K is not a multiple of the table GEMV's slice width");
+  return cuda_status(launch_lut_gemv_noalloc(a, rows, static_cast<cudaStream_t>(stream)), "moe_w2_mm_noalloc");
+}
+
 int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
                  const int32_t* act_row, int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
                  const int32_t* ws_slot_of_expert, const int32_t* offsets, const int32_t* expert_slot,

@@ -420,6 +420,12 @@ size_t lut_workspace_bytes(int stage, int rows, int N, int K) {
   return cnt + static_cast<size_t>(rows) * nb * nsl * rpi * sizeof(float);
 }
 
+size_t lut_counter_bytes(int stage, int rows, int N, int K) {
+  int rpi, nb, nsl;
+  lut_geometry(stage, N, K, rpi, nb, nsl);
+  return (static_cast<size_t>(rows) * nb * sizeof(int) + 255) & ~size_t(255);
+}
+
 int lut_workspace_rows(int stage, size_t bytes, int N, int K) {
   int rpi, nb, nsl;
   lut_geometry(stage, N, K, rpi, nb, nsl);

@@ -20,8 +20,9 @@
  *  - Notation: T tokens, E experts, H hidden, I expert intermediate, k experts
  *    per token, A = T*k assignments, a = t*k + j (j = slot in the top-k).
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless the
- *    comment says "host".  The library never allocates, frees or keeps device
- *    memory.  Buffers must not alias unless a comment allows it.
+ *    comment says "host".  The library never allocates or frees device memory;
+ *    the one device memory it keeps is the fixed scratch array of
+ *    moe_w2_mm_noalloc, part of its module image.  Buffers must not alias unless a comment allows it.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream) and never synchronises the host, except
  *    moe_get_error.
@@ -31,7 +32,8 @@
  *    into the caller's `dev_err` word (a uint32 in device memory, which the
  *    caller zeroes; may be NULL to ignore) and carry on.  Read with
  *    moe_get_error.
- *  - Thread-safe: the only global state is a per-device property cache.
+ *  - Thread-safe: the only host-side global state is a per-device property
+ *    cache and the per-device address of moe_w2_mm_noalloc's scratch.
  *
  * Canonical weight layout (what callers store; parity is stated against it)
  * ---------------------------------------------------------------------------
@@ -228,6 +230,38 @@ MOE_API int moe_w2_mm(int stage, int mode,
               int E, int N, int K,
               void* out, int out_fmt, uint8_t* out_scale,
               void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
+
+/* moe_w2_mm_noalloc: the 2-bit table GEMV of moe_w2_mm (decode), run on a
+ * scratch array that the library holds itself.  None of the pages has a
+ * counterpart: it exists for callers that cannot pass a workspace, e.g. C host
+ * code with no device allocator of its own, or a serving engine that has given
+ * all spare device memory to its KV cache and may not allocate while decoding.
+ * The call allocates and frees nothing.
+ *
+ * Computes exactly what moe_w2_mm computes with mode GEMV and a workspace
+ * (same kernel, same summation order: the outputs are bit-identical), with
+ *   act     bf16 [act_rows][K] (act_fmt is BF16; act_row / act_row_div as in
+ *           moe_w2_mm); out_fmt BF16 or F32 (no MXFP8 output)
+ *   rows    the number of permuted rows the call covers (offsets[E], e.g. T*k);
+ *           a row p >= rows sets OVERFLOW and is skipped
+ * Limit: moe_w2_mm_workspace_size(stage, rows, N, K) must not exceed
+ * MOE_W2_NOALLOC_SCRATCH_BYTES (16 MiB: 127 rows of FC1 at H=4096, I=2048, or
+ * 255 rows of FC2), else MOE_ERR_WS_SMALL.  Shapes the table GEMV does not
+ * take (K not a multiple of its slice width) give MOE_ERR_UNSUPPORTED.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * scratch's device address (cudaGetSymbolAddress, which may load the module);
+ * make that first call before any stream capture.  Every call clears the
+ * scratch's counters with one cudaMemsetAsync on `stream`.
+ * One scratch per device: calls that overlap on the GPU (other streams or
+ * threads) race on it and give wrong results; serialise them. */
+#define MOE_W2_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+MOE_API int moe_w2_mm_noalloc(int stage,
+                      const void* act, int act_rows, const int32_t* act_row, int act_row_div,
+                      const uint8_t* codes_k, const uint16_t* scales_k,
+                      const int32_t* offsets, const int32_t* expert_slot,
+                      int E, int N, int K, int rows,
+                      void* out, int out_fmt, uint32_t* dev_err, void* stream);
 
 /* As moe_w2_mm for MXFP4 weights, or for FP8 workspace weights.
  * Weight source, exactly one of:

@@ -52,3 +52,18 @@ def test_host_only_calls(lib_path):
     b = lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 128, 2048, 4096)
     assert 0 < a < b
     assert lib.moe_w2_mm_workspace_size(7, 64, 2048, 4096) == 0
+
+
+def test_noalloc_limit_matches_header(lib_path):
+    """The binding's copy of MOE_W2_NOALLOC_SCRATCH_BYTES, and the row counts
+    the header states for it (decode shapes H=4096, I=2048)."""
+    from bit_moe_expert_top_gb300 import _lib as L
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    m = re.search(r"#define MOE_W2_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    assert m and int(m.group(1)) << int(m.group(2)) == L.W2_NOALLOC_SCRATCH_BYTES
+    lib = L.lib()
+    cap = L.W2_NOALLOC_SCRATCH_BYTES
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 127, 2048, 4096) <= cap
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 128, 2048, 4096) > cap
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 255, 4096, 2048) <= cap
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 256, 4096, 2048) > cap
