@@ -206,15 +206,17 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * or F32, and MXFP8 for FC1 (out_scale receives E8M0 [rows][N/32]).  Rounding:
  * out = RNE of the fp32 result into out_fmt.  Rows of unselected experts are
  * left untouched.
- * Modes: GEMV = CUDA-core kernels (2-bit: shared-memory partial-sum tables
- * with the K dimension split over CTAs; MXFP4 / FP8: register decode); GEMM =
+ * Modes: GEMV = CUDA-core kernels (2-bit with a workspace and K a multiple
+ * of 512: shared-memory partial-sum tables with K split in 512-element
+ * slices over CTAs; otherwise, and for MXFP4 / FP8: register decode); GEMM =
  * tcgen05 tensor-core kernel (2-bit weights, bf16 activations already
  * permuted: act_row must be NULL); AUTO = GEMM when act_row is NULL,
  * act_rows >= 2048 and the shape is supported, else GEMV.
  *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
  *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
  *        256-byte aligned, ZERO-FILLED before its first use; every successful
- *        call leaves it zero-filled again (after a MOE_DEVERR_TIMEOUT, zero it).
+ *        call leaves it zero-filled again, so FC1 and FC2 may share one (after a
+ *        call that returned an error, zero it).
  *        With ws == NULL the 2-bit GEMV uses the slower register-decode kernel.
  *        A row beyond the workspace's capacity sets OVERFLOW and is skipped.
  *        Calls that share one workspace must not overlap on the GPU.
@@ -246,7 +248,7 @@ MOE_API int moe_w2_mm(int stage, int mode,
  *           a row p >= rows sets OVERFLOW and is skipped
  * Limit: moe_w2_mm_workspace_size(stage, rows, N, K) must not exceed
  * MOE_W2_NOALLOC_SCRATCH_BYTES (16 MiB: 127 rows of FC1 at H=4096, I=2048, or
- * 255 rows of FC2), else MOE_ERR_WS_SMALL.  Shapes the table GEMV does not
+ * 254 rows of FC2), else MOE_ERR_WS_SMALL.  Shapes the table GEMV does not
  * take (K not a multiple of its slice width) give MOE_ERR_UNSUPPORTED.
  * Set-up: the first call on a device, with that device current, looks up the
  * scratch's device address (cudaGetSymbolAddress, which may load the module);
