@@ -204,6 +204,10 @@ def run_gpu(args):
     # from the event pairs of the last replay
     mm_ms = sum(a.elapsed_time(b) for _, a, b in graph_ev)
     n_mm = len(graph_ev)
+    per_label = {}
+    for label, a, b in graph_ev:
+        per_label.setdefault(label, []).append(a.elapsed_time(b) * 1e3)
+    kernels_us = {k: round(sum(v) / len(v), 2) for k, v in per_label.items()}
     graph_bytes = sum(work_bytes[i % batches] for i in range(S))
     tot_bytes = sum(work_bytes[i % batches] for i in range(args.steps))
     A = w.A
@@ -223,7 +227,7 @@ def run_gpu(args):
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                "kernel": "gemv_kernel (moe_w2_mm FC1+FC2)", "peak_src": peaks["src"],
+                "kernel": "expert matmuls (moe_w2_mm FC1+FC2)", "peak_src": peaks["src"],
                 "bytes_per_launch": round(graph_bytes / n_mm), "launch_us": round(mm_ms / n_mm * 1e3, 2)}
     else:
         achieved = S * A * flops_per_assignment(w) / (mm_ms / 1e3) / 1e12
@@ -245,6 +249,7 @@ def run_gpu(args):
         "weight_stream_gbs": round(tot_bytes / (t_max / 1e3) / 1e9 / world, 1) if decode else None,
         "tflops": round(tot_flops / (t_max / 1e3) / 1e12, 2),
         "roofline": roof,
+        "kernels_us": kernels_us,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clk,

@@ -218,8 +218,10 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
   a.wkind = kW2;
   a.wq = codes_k;
   a.wscale = scales_k;
-  a.ws = (ws && ws_bytes) ? ws : nullptr;
-  a.ws_bytes = ws_bytes;
+  // the workspace only serves the table GEMV; shapes it does not take need none
+  const bool table_shape = lut_workspace_bytes(stage, 1, N, K) > 0;  // K a multiple of 512
+  a.ws = (ws && ws_bytes && table_shape) ? ws : nullptr;
+  a.ws_bytes = a.ws ? ws_bytes : 0;
   a.ws_rows = a.ws ? lut_workspace_rows(stage, ws_bytes, N, K) : 0;
   if (a.ws && !aligned(ws, 256)) return fail(MOE_ERR_ARG, "moe_w2_mm: ws must be 256-byte aligned");
   if (a.ws && a.ws_rows < 1) return fail(MOE_ERR_WS_SMALL, "moe_w2_mm: workspace below one row");

@@ -72,6 +72,12 @@ MOE_D void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned address and
+// size); no completion to wait for and no scoreboard held.
+MOE_D void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 MOE_D void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

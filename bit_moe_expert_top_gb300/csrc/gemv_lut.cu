@@ -29,11 +29,11 @@
 // flight.  (Bulk copies of a few KB into a shared ring stream far slower on
 // this part, and would also spend shared-memory bandwidth twice.)  A shuffle
 // reduce-scatter turns the 32 lanes x 32 rows of partials into one slice sum
-// per row and lane; the warp stores them to a global scratch and counts the
-// slices of its batch with one atomic.  The warp that brings the count to the
-// number of slices sums them in slice order (deterministic), applies SwiGLU
-// for FC1, rounds and stores.  There is no spin-wait anywhere: no CTA waits
-// on another.
+// per row and lane, which the warp stores to a global scratch with plain
+// stores: no atomics and no fences, so nothing ever waits for the loads in
+// flight.  A second, small kernel (launched as a programmatic dependent of
+// the first) sums each row's slices in slice order (deterministic), applies
+// SwiGLU for FC1, rounds and stores.  Neither kernel waits on another CTA.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,6 +51,7 @@ constexpr int kPrologue = 8192;               // shared bytes below the table wi
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
+constexpr int kPrefetch = 2;                  // batches per warp prefetched to L2 ahead of the loads
 
 struct LutParams {
   const uint16_t* act;
@@ -66,7 +67,7 @@ struct LutParams {
   int NSL;                  // K slices
   int NB;                   // row batches per permuted row (FC1: N/16, FC2: N/32)
   int fc1;
-  int* counters;            // [A][NB] slice arrivals
+  int* rows_hdr;            // [0]: selected rows; then prow[A]: permuted row of selected row i, or -1
   float* scratch;           // [A][NB][NSL][32] per-slice row sums
   int A;                    // permuted rows the scratch covers
   void* out;
@@ -74,20 +75,47 @@ struct LutParams {
   uint32_t* dev_err;
 };
 
-// Sum of the four table lookups for one code word (lanebase = table window
-// address + 4 * lane, whose byte 1 is zero).
-MOE_D float word_sum(uint32_t w, uint32_t lanebase) {
+MOE_D float2 fadd2(float2 a, float2 b) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rd;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+MOE_D float2 fmul2(float2 a, float2 b) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rd;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+// The four table entries of one code word (lanebase = table window address +
+// 4 * lane, whose byte 1 is zero): byte k of the word indexes the table of
+// byte position 4*lane + k.
+MOE_D float4 word_lookup(uint32_t w, uint32_t lanebase) {
   uint32_t a0, a1, a2, a3;
   asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(a0) : "r"(w), "r"(lanebase));
   asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(a1) : "r"(w), "r"(lanebase));
   asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(a2) : "r"(w), "r"(lanebase));
   asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(a3) : "r"(w), "r"(lanebase));
-  float t0, t1, t2, t3;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(t0) : "r"(a0));
-  asm volatile("ld.shared.f32 %0, [%1+128];" : "=f"(t1) : "r"(a1));
-  asm volatile("ld.shared.f32 %0, [%1+65536];" : "=f"(t2) : "r"(a2));
-  asm volatile("ld.shared.f32 %0, [%1+65664];" : "=f"(t3) : "r"(a3));
-  return (t0 + t1) + (t2 + t3);
+  float4 t;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(t.x) : "r"(a0));
+  asm volatile("ld.shared.f32 %0, [%1+128];" : "=f"(t.y) : "r"(a1));
+  asm volatile("ld.shared.f32 %0, [%1+65536];" : "=f"(t.z) : "r"(a2));
+  asm volatile("ld.shared.f32 %0, [%1+65664];" : "=f"(t.w) : "r"(a3));
+  return t;
+}
+
+// Scaled word sums of two rows (words wa, wb; bf16 scales packed in sc as
+// lo = row a, hi = row b), with packed fp32x2 adds.
+MOE_D float2 word_pair(uint32_t wa, uint32_t wb, uint32_t sc, uint32_t lanebase) {
+  const float4 ta = word_lookup(wa, lanebase);
+  const float4 tb = word_lookup(wb, lanebase);
+  const float2 s01 = fadd2(make_float2(ta.x, tb.x), make_float2(ta.y, tb.y));
+  const float2 s23 = fadd2(make_float2(ta.z, tb.z), make_float2(ta.w, tb.w));
+  return fmul2(fadd2(s01, s23), make_float2(__uint_as_float(sc << 16), __uint_as_float(sc & 0xffff0000u)));
 }
 
 MOE_D uint4 ldg_stream(const void* p) {
@@ -104,16 +132,20 @@ MOE_D uint2 ldg_stream2(const void* p) {
   return v;
 }
 
-// One reduce-scatter level over v[0..2H): lanes with bit m set keep the upper
-// half and add the partner's upper half; the others keep the lower half.
+// One reduce-scatter level over the row pairs v[0..2H) (pair i = rows 2i,
+// 2i+1): lanes with bit m set keep the upper half and add the partner's upper
+// half; the others keep the lower half.
 template <int H>
-MOE_D void rs_level(float* v, int lane, int m) {
+MOE_D void rs_level2(float2* v, int lane, int m) {
   const bool up = (lane & m) != 0;
 #pragma unroll
   for (int i = 0; i < H; ++i) {
-    const float keep = up ? v[i + H] : v[i];
-    const float send = up ? v[i] : v[i + H];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    const float2 keep = up ? v[i + H] : v[i];
+    const float2 send = up ? v[i] : v[i + H];
+    float2 got;
+    got.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+    got.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+    v[i] = fadd2(keep, got);
   }
 }
 
@@ -153,6 +185,31 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     }
   }
   __syncthreads();
+  // the finishing kernel may be scheduled now; it waits for this grid's
+  // completion (and memory flush) before it reads the scratch
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- the permuted row of every selected row for the finishing kernel
+  // (-1 where the row is skipped: beyond the scratch, or a bad token index)
+  {
+    const int nsel = pref[P.E];
+    if (blockIdx.x == 0 && tid == 0) P.rows_hdr[0] = nsel;
+    const int lim = min(nsel, P.A);
+    for (int i = blockIdx.x * kLutThreads + tid; i < lim; i += gridDim.x * kLutThreads) {
+      int lo = 0, hi = P.E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref[mid] <= i) lo = mid; else hi = mid;
+      }
+      const int p = P.offsets[lo] + (i - pref[lo]);
+      bool ok = p < P.A;
+      if (ok) {
+        const int row = P.act_row ? P.act_row[p] / P.act_row_div : p;
+        ok = row >= 0 && row < P.act_rows;
+      }
+      P.rows_hdr[1 + i] = ok ? p : -1;
+    }
+  }
 
   // ---- this CTA's unit range; unit = (selected row, slice, batch), batch fastest
   const int64_t per_row = static_cast<int64_t>(NSL) * NB;
@@ -167,7 +224,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
 
   uint4 v[8];
   uint2 sc[8];
-  float acc[32];
+  float2 acc[16];  // row pairs (2i, 2i+1) of the batch
 
   for (int64_t u = u_beg; u < u_end;) {
     const int64_t seg = u / NB;
@@ -198,17 +255,36 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
         reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + s * slice_scales) + (lane >> 1) * 8;
     // quad index (rows 4Q..4Q+3 of the expert) of quad q of batch rb: FC1
     // batches are 16 gate rows then the 16 matching up rows
-    auto quad_of = [&](int rb, int q) -> int64_t {
-      if (fc1) return q < 4 ? rb * 4 + q : (P.N >> 2) + rb * 4 + (q - 4);
-      return rb * 8 + q;
+    auto quad_of = [&](int rb, int q) -> uint32_t {
+      if (fc1) return static_cast<uint32_t>(q < 4 ? rb * 4 + q : (P.N >> 2) + rb * 4 + (q - 4));
+      return static_cast<uint32_t>(rb * 8 + q);
     };
+    // one warp batch's codes and scales to L2 (lane 0; FC1: gate and up halves)
+    auto prefetch_batch = [&](int rb) {
+      const uint8_t* c0 = gcodes - lane * 16;
+      const uint8_t* s0 = gscales - (lane >> 1) * 8;
+      if (fc1) {
+        prefetch_l2(c0 + quad_of(rb, 0) * 512u, 2048);
+        prefetch_l2(c0 + quad_of(rb, 4) * 512u, 2048);
+        prefetch_l2(s0 + quad_of(rb, 0) * 128u, 512);
+        prefetch_l2(s0 + quad_of(rb, 4) * 128u, 512);
+      } else {
+        prefetch_l2(c0 + quad_of(rb, 0) * 512u, 4096);
+        prefetch_l2(s0 + quad_of(rb, 0) * 128u, 1024);
+      }
+    };
+    if (lane == 0) {
+#pragma unroll
+      for (int d = 1; d <= kPrefetch; ++d)
+        if (uw + d * kLutWarps < seg_end) prefetch_batch(static_cast<int>(uw + d * kLutWarps - seg0));
+    }
     if (uw < seg_end) {
       const int rb = static_cast<int>(uw - seg0);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const int64_t Q = quad_of(rb, q);
-        v[q] = ldg_stream(gcodes + Q * 512);
-        sc[q] = ldg_stream2(gscales + Q * 128);
+        const uint32_t Q = quad_of(rb, q);
+        v[q] = ldg_stream(gcodes + Q * 512u);
+        sc[q] = ldg_stream2(gscales + Q * 128u);
       }
     }
 
@@ -243,96 +319,100 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
       const int rb = static_cast<int>(uw - seg0);
       const int rbn = rb + kLutWarps;
       const bool more = uw + kLutWarps < seg_end;
+      if (lane == 0 && uw + (kPrefetch + 1) * kLutWarps < seg_end)
+        prefetch_batch(rb + (kPrefetch + 1) * kLutWarps);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint4 w4 = v[q];
         const uint2 s4 = sc[q];
-        acc[q * 4 + 0] = word_sum(w4.x, lanebase) * __uint_as_float(s4.x << 16);
-        acc[q * 4 + 1] = word_sum(w4.y, lanebase) * __uint_as_float(s4.x & 0xffff0000u);
-        acc[q * 4 + 2] = word_sum(w4.z, lanebase) * __uint_as_float(s4.y << 16);
-        acc[q * 4 + 3] = word_sum(w4.w, lanebase) * __uint_as_float(s4.y & 0xffff0000u);
+        acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
+        acc[2 * q + 1] = word_pair(w4.z, w4.w, s4.y, lanebase);
         if (more) {  // the next batch's loads go out while this one is consumed
-          const int64_t Q = quad_of(rbn, q);
-          v[q] = ldg_stream(gcodes + Q * 512);
-          sc[q] = ldg_stream2(gscales + Q * 128);
+          const uint32_t Q = quad_of(rbn, q);
+          v[q] = ldg_stream(gcodes + Q * 512u);
+          sc[q] = ldg_stream2(gscales + Q * 128u);
         }
       }
       // ---- reduce-scatter: afterwards lane l holds the slice sum of batch row l
-      rs_level<16>(acc, lane, 16);
-      rs_level<8>(acc, lane, 8);
-      rs_level<4>(acc, lane, 4);
-      rs_level<2>(acc, lane, 2);
-      rs_level<1>(acc, lane, 1);
+      rs_level2<8>(acc, lane, 16);
+      rs_level2<4>(acc, lane, 8);
+      rs_level2<2>(acc, lane, 4);
+      rs_level2<1>(acc, lane, 2);
+      const bool odd = (lane & 1) != 0;
+      const float keep = odd ? acc[0].y : acc[0].x;
+      const float send = odd ? acc[0].x : acc[0].y;
+      const float sum = keep + __shfl_xor_sync(0xffffffffu, send, 1);
       const size_t cell = static_cast<size_t>(p) * NB + rb;
-      P.scratch[(cell * NSL + s) * 32 + lane] = acc[0];
-      __syncwarp();
-      int old = 0;
-      if (lane == 0) {
-        // release: the warp's slice sums (ordered before by the warp barrier)
-        // precede the count; acquire: the other slices' sums precede reading them
-        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(P.counters + cell) : "memory");
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      __syncwarp();
-      if (old == NSL - 1) {
-        float* sp = P.scratch + cell * NSL * 32 + lane;
-        float t = 0.f;
-        for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * 32);
-        // leave the whole workspace zero: FC1 and FC2 may share it with
-        // counter regions of different sizes
-        for (int q = 0; q < NSL; ++q) __stcg(sp + q * 32, 0.f);
-        int n;
-        bool store = true;
-        if (fc1) {  // lanes 0..15 gate rows, 16..31 the matching up rows
-          const float up = __shfl_down_sync(0xffffffffu, t, 16);
-          t = silu_f32(t) * up;
-          n = rb * 16 + lane;
-          store = lane < 16;
-        } else {
-          n = rb * 32 + lane;
-        }
-        if (store) {
-          const size_t o = static_cast<size_t>(p) * P.N + n;
-          if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
-          else static_cast<uint16_t*>(P.out)[o] = f32_to_bf16_rne(t);
-        }
-        if (lane == 0) P.counters[cell] = 0;  // leave the counters zero for the next call
-      }
+      __stcg(P.scratch + (cell * NSL + s) * 32 + lane, sum);
     }
+  }
+}
+
+// Sums the NSL slice sums of every output in slice order, applies SwiGLU for
+// FC1, rounds and stores.  Block (i, j) takes selected rows i, i + gridDim.x,
+// ... and outputs [256 j, 256 j + 256); one thread per output.
+__global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
+  // everything read here is written by the preceding (primary) grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int NSL = P.NSL, NB = P.NB;
+  const int n = blockIdx.y * 256 + threadIdx.x;
+  if (n >= P.N) return;
+  const int lim = min(__ldcg(P.rows_hdr), P.A);
+  for (int i = blockIdx.x; i < lim; i += gridDim.x) {
+    const int p = __ldcg(P.rows_hdr + 1 + i);
+    if (p < 0) continue;
+    float t;
+    if (P.fc1) {  // batch n/16: lanes 0..15 gate rows, 16..31 the matching up rows
+      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * 32 + (n & 15);
+      float g = 0.f, u = 0.f;
+#pragma unroll 4
+      for (int q = 0; q < NSL; ++q) {
+        g += __ldcg(sp + q * 32);
+        u += __ldcg(sp + q * 32 + 16);
+      }
+      t = silu_f32(g) * u;
+    } else {
+      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 5)) * NSL * 32 + (n & 31);
+      t = 0.f;
+#pragma unroll 4
+      for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * 32);
+    }
+    const size_t o = static_cast<size_t>(p) * P.N + n;
+    if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
+    else static_cast<uint16_t*>(P.out)[o] = f32_to_bf16_rne(t);
   }
 }
 
 }  // namespace
 
-// Scratch of the table GEMV: slice-arrival counters [rows][NB] (ints,
-// padded to 256 bytes) then per-slice row sums [rows][NB][NSL][32] (fp32);
-// all zero before a call, and left zero by a call that completes.  NB = N/16 batches for FC1 (16 gate + 16 up
+// Scratch of the table GEMV: a row header (the selected-row count, then the
+// permuted row of each selected row; 256-byte padded) and the per-slice row
+// sums [rows][NB][NSL][32] (fp32).  Everything is written before it is read;
+// no initial contents needed.  NB = N/16 batches for FC1 (16 gate + 16 up
 // rows each), N/32 for FC2.
 static void lut_geometry(int stage, int N, int K, int& nb, int& nsl) {
   nb = stage == MOE_STAGE_FC1_SWIGLU ? N / 16 : N / 32;
   nsl = K / kSW;
 }
 
-size_t lut_counter_bytes(int stage, int rows, int N, int K) {
-  int nb, nsl;
-  lut_geometry(stage, N, K, nb, nsl);
-  return (static_cast<size_t>(rows) * nb * sizeof(int) + 255) & ~size_t(255);
-}
+static size_t lut_header_bytes(int rows) { return (static_cast<size_t>(rows + 1) * sizeof(int) + 255) & ~size_t(255); }
 
 size_t lut_workspace_bytes(int stage, int rows, int N, int K) {
   int nb, nsl;
   lut_geometry(stage, N, K, nb, nsl);
-  return lut_counter_bytes(stage, rows, N, K) + static_cast<size_t>(rows) * nb * nsl * 32 * sizeof(float);
+  if (nsl == 0 || rows <= 0) return 0;
+  return lut_header_bytes(rows) + static_cast<size_t>(rows) * nb * nsl * 32 * sizeof(float);
 }
 
 int lut_workspace_rows(int stage, size_t bytes, int N, int K) {
   int nb, nsl;
   lut_geometry(stage, N, K, nb, nsl);
-  const size_t per = static_cast<size_t>(nb) * sizeof(int) + static_cast<size_t>(nb) * nsl * 32 * sizeof(float);
-  if (per == 0) return 0;
+  if (nsl == 0) return 0;
+  const size_t per = static_cast<size_t>(nb) * nsl * 32 * sizeof(float) + sizeof(int);
   int64_t rows = static_cast<int64_t>(bytes / per);
+  if (rows > 0x7ffffffe) rows = 0x7ffffffe;
   while (rows > 0 && lut_workspace_bytes(stage, static_cast<int>(rows), N, K) > bytes) --rows;
-  return rows > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows);
+  return static_cast<int>(rows);
 }
 
 bool lut_supported(const MMArgs& a) {
@@ -359,8 +439,8 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   P.R = P.fc1 ? 2 * a.N : a.N;
   lut_geometry(a.stage, a.N, a.K, P.NB, P.NSL);
   P.A = a.ws_rows;
-  P.counters = static_cast<int*>(ws);
-  P.scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lut_counter_bytes(a.stage, a.ws_rows, a.N, a.K));
+  P.rows_hdr = static_cast<int*>(ws);
+  P.scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lut_header_bytes(a.ws_rows));
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
@@ -370,8 +450,23 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  w2_lut_kernel<<<device_info().sms, kLutThreads, kLutSmem, s>>>(P);
-  return cudaGetLastError();
+  const int sms = device_info().sms;
+  w2_lut_kernel<<<sms, kLutThreads, kLutSmem, s>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the finishing kernel as a programmatic dependent: its launch overlaps the
+  // main kernel's tail; griddepcontrol.wait orders its scratch reads
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.ws_rows < 4096 ? a.ws_rows : 4096), static_cast<unsigned>((a.N + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w2_lut_finish_kernel, P);
 }
 
 }  // namespace moe

@@ -76,7 +76,6 @@ cudaError_t launch_gemv_generic(const MMArgs& a, cudaStream_t s);
 bool lut_supported(const MMArgs& a);
 size_t lut_workspace_bytes(int stage, int rows, int N, int K);
 int lut_workspace_rows(int stage, size_t bytes, int N, int K);
-size_t lut_counter_bytes(int stage, int rows, int N, int K);  // leading counter region of the scratch
 cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s);
 bool gemm_supported(const MMArgs& a);
 cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
@@ -85,8 +84,8 @@ cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 // Device address of the scratch array on the current device (looked up on the
 // first call per device).
 cudaError_t noalloc_scratch(void** ptr);
-// Clears the counters and runs launch_lut_gemv on that scratch for `rows`
-// permuted rows; the caller has checked that the rows fit.
+// Runs launch_lut_gemv on that scratch for `rows` permuted rows; the caller
+// has checked that the rows fit.
 cudaError_t launch_lut_gemv_noalloc(MMArgs a, int rows, cudaStream_t s);
 
 }  // namespace moe

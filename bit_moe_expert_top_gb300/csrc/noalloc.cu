@@ -1,8 +1,8 @@
 // Scratch of the 2-bit decode GEMV held by the library itself, for callers
 // that cannot hand it a workspace.
 //
-// The table GEMV needs a few MB of device scratch per call (slice sums and
-// slice-arrival counters).  moe_w2_mm takes it from the caller.  Some callers
+// The table GEMV needs a few MB of device scratch per call (the per-slice
+// row sums that its second kernel adds up).  moe_w2_mm takes it from the caller.  Some callers
 // cannot provide it: plain C host code that drives the library with nothing
 // but the model's own buffers and has no device allocator of its own, or a
 // serving engine that has already handed all of its spare device memory to
@@ -58,10 +58,8 @@ cudaError_t launch_lut_gemv_noalloc(MMArgs a, int rows, cudaStream_t s) {
   a.ws = ws;
   a.ws_rows = rows;
   a.ws_bytes = lut_workspace_bytes(a.stage, rows, a.N, a.K);
-  // The slice-arrival counters must start at zero.  A completed call leaves
-  // them zero, but a call cut short by a wait timeout may not: clear them.
-  e = cudaMemsetAsync(ws, 0, lut_counter_bytes(a.stage, rows, a.N, a.K), s);
-  if (e != cudaSuccess) return e;
+  // nothing in the scratch needs to start at zero: every slice sum is
+  // written before it is read
   return launch_lut_gemv(a, ws, s);
 }
 

@@ -11,92 +11,96 @@ namespace moe {
 
 // ------------------------------------------------------------------ routing
 // Order used by the top-k: larger logit first, equal logits -> lower expert id
-// first, NaN after every number (NaNs among themselves by id).
-MOE_D bool route_better(float v1, int i1, float v2, int i2) {
-  const bool n1 = v1 != v1, n2 = v2 != v2;
-  if (n1 != n2) return n2;
-  if (!n1 && v1 != v2) return v1 > v2;
-  return i1 < i2;
+// first, NaN after every number (NaNs among themselves by id).  Each logit
+// becomes one 64-bit key whose unsigned order is exactly that order: the high
+// word is the value mapped to an order-preserving integer (-0 taken as +0,
+// NaN -> 1, below -inf), the low word is ~id; 0 marks "taken / absent".
+MOE_D uint64_t route_key(float v, int e) {
+  uint32_t ord;
+  if (v != v) {
+    ord = 1u;
+  } else {
+    const uint32_t u = __float_as_uint(v + 0.0f);  // -0 -> +0
+    ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  return (static_cast<uint64_t>(ord) << 32) | (0xffffffffu - static_cast<uint32_t>(e));
 }
 
-// One warp per token; the token's logits are staged in shared memory and the
-// top-k is taken by k rounds of a warp-wide arg-best.
+MOE_D float route_key_value(uint64_t key) {
+  const uint32_t ord = static_cast<uint32_t>(key >> 32);
+  if (ord == 1u) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
+
+// One warp per token.  Lane l holds the keys of experts l, l+32, ... in
+// registers (NPL per lane, NPL*32 >= E) and its own best; every round takes
+// the warp-wide maximum key (5 shuffle levels), and the owning lane retires
+// that key and recomputes its best.
+template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                     int32_t* __restrict__ ids, float* __restrict__ w,
                                                     uint32_t* dev_err) {
-  extern __shared__ float s_route[];  // [8 warps][E] values, then [8][E] taken flags (as float bits)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  float* vals = s_route + warp * E;
-  unsigned char* taken = reinterpret_cast<unsigned char*>(s_route + 8 * E) + warp * E;
   const float* row = logits + static_cast<size_t>(t) * E;
+  uint64_t key[NPL];
   bool any_nan = false;
-  for (int e = lane; e < E; e += 32) {
-    float v = row[e];
-    any_nan |= (v != v);
-    vals[e] = v;
-    taken[e] = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = 0;
+    if (e < E) {
+      const float v = __ldg(row + e);
+      any_nan |= (v != v);
+      key[i] = route_key(v, e);
+    }
   }
   if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_err(dev_err, MOE_DEVERR_NAN_LOGIT);
-  __syncwarp();
-  float my_sel = 0.f;
-  int my_id = 0;
+  uint64_t best = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) best = key[i] > best ? key[i] : best;
+  uint64_t mine = 0;  // lane j keeps the key of slot j
   for (int j = 0; j < k; ++j) {
-    float bv = 0.f;
-    int bi = 0x7fffffff;
-    bool have = false;
-    for (int e = lane; e < E; e += 32) {
-      if (taken[e]) continue;
-      float v = vals[e];
-      if (!have || route_better(v, e, bv, bi)) {
-        bv = v;
-        bi = e;
-        have = true;
-      }
-    }
-    // warp arg-best; lanes without a candidate carry id = INT_MAX and lose
+    uint64_t m = best;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      bool oh = __shfl_xor_sync(0xffffffffu, have, o);
-      if (oh && (!have || route_better(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-        have = true;
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, m, o);
+      m = other > m ? other : m;
+    }
+    if (lane == j) mine = m;
+    const int id = static_cast<int>(0xffffffffu - static_cast<uint32_t>(m));
+    if ((id & 31) == lane) {  // retire the winner, recompute this lane's best
+      const int slot = id >> 5;
+      best = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        if (i == slot) key[i] = 0;
+        best = key[i] > best ? key[i] : best;
       }
     }
-    if (lane == (bi & 31)) taken[bi] = 1;
-    if (lane == j) {
-      my_sel = bv;
-      my_id = bi;
-    }
-    __syncwarp();
   }
   // softmax over the selected logits, relative to the largest (slot 0)
-  float l = (my_sel != my_sel) ? -INFINITY : my_sel;
+  float l = route_key_value(mine);
+  l = (l != l) ? -INFINITY : l;
   const float l0 = __shfl_sync(0xffffffffu, l, 0);
-  float z = (lane < k) ? expf(l - l0) : 0.f;
-  float s = 0.f;
-  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, z, j);
+  const float z = (lane < k) ? expf(l - l0) : 0.f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, z, j);
   if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    w[static_cast<size_t>(t) * k + lane] = z / s;
+    ids[static_cast<size_t>(t) * k + lane] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(mine));
+    w[static_cast<size_t>(t) * k + lane] = z / sum;
   }
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
                          cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(8) * E * 4 + static_cast<size_t>(8) * E;
-  static bool attr_set = false;  // benign race: idempotent attribute write
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  route_kernel<<<(T + 7) / 8, 256, smem, s>>>(logits, T, E, k, ids, w, dev_err);
+  const dim3 grid((T + 7) / 8), block(256);
+  if (E <= 128) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
+  else if (E <= 256) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
+  else if (E <= 512) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
+  else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
   return cudaGetLastError();
 }
 
@@ -120,10 +124,11 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   const unsigned lt_mask = (1u << lane) - 1u;
   int chunk = (A + kPermWarps - 1) / kPermWarps;
   chunk = (chunk + 31) & ~31;
+  const int nw = chunk > 0 ? (A + chunk - 1) / chunk : 0;  // warps with a non-empty chunk
   const int beg = warp * chunk;
   const int end = min(A, beg + chunk);
 
-  for (int i = tid; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
 
   bool bad = false;
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   // per-expert exclusive scan over warps; totals
   for (int e = tid; e < E; e += blockDim.x) {
     int run = 0;
-    for (int w = 0; w < kPermWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       const int c = hist[w * E + e];
       hist[w * E + e] = run;
       run += c;
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     if (tid == E - 1) offsets[E] = excl + v;
   }
   __syncthreads();
-  for (int i = tid; i < kPermWarps * E; i += blockDim.x) hist[i] += tot[i % E];
+  for (int i = tid; i < nw * E; i += blockDim.x) hist[i] += tot[i % E];
   __syncthreads();
 
   for (int base = beg; base < end; base += 32) {

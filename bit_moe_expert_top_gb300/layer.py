@@ -127,14 +127,14 @@ class MoELayer:
         )
 
     def _gemv_ws(self, A: int, cap_bytes: int = 1 << 30) -> Optional[torch.Tensor]:
-        """Zero-filled scratch of the 2-bit decode GEMV (FC1 and FC2 share it:
-        the calls run one after the other on the stream).  Decode-sized steps
+        """Scratch of the 2-bit decode GEMV (FC1 and FC2 share it: the calls
+        run one after the other on the stream; no initial contents needed).  Decode-sized steps
         need a few MB; beyond `cap_bytes` the GEMV runs without scratch."""
         n = max(L.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, A, self.I, self.H),
                 L.moe_w2_mm_workspace_size(L.STAGE_FC2, A, self.H, self.I))
         if n > cap_bytes:
             return None
-        return torch.zeros((n + 3) // 4, dtype=torch.int32, device=self.device)
+        return torch.empty((n + 3) // 4, dtype=torch.int32, device=self.device)
 
     # ------------------------------------------------------------ one step
     def step(self, x: torch.Tensor, logits: torch.Tensor, b: StepBuffers, ev: Optional[list] = None) -> torch.Tensor:

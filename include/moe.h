@@ -214,9 +214,10 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * act_rows >= 2048 and the shape is supported, else GEMV.
  *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
  *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
- *        256-byte aligned, ZERO-FILLED before its first use; every successful
- *        call leaves it zero-filled again, so FC1 and FC2 may share one (after a
- *        call that returned an error, zero it).
+ *        256-byte aligned.  Its contents on entry do not matter (every value
+ *        is written before it is read), so FC1 and FC2 may share one.  The
+ *        size query returns 0 for shapes the table GEMV does not take (K not
+ *        a multiple of 512): a workspace passed with those is ignored.
  *        With ws == NULL the 2-bit GEMV uses the slower register-decode kernel.
  *        A row beyond the workspace's capacity sets OVERFLOW and is skipped.
  *        Calls that share one workspace must not overlap on the GPU.
@@ -248,12 +249,12 @@ MOE_API int moe_w2_mm(int stage, int mode,
  *           a row p >= rows sets OVERFLOW and is skipped
  * Limit: moe_w2_mm_workspace_size(stage, rows, N, K) must not exceed
  * MOE_W2_NOALLOC_SCRATCH_BYTES (16 MiB: 127 rows of FC1 at H=4096, I=2048, or
- * 254 rows of FC2), else MOE_ERR_WS_SMALL.  Shapes the table GEMV does not
+ * 255 rows of FC2), else MOE_ERR_WS_SMALL.  Shapes the table GEMV does not
  * take (K not a multiple of its slice width) give MOE_ERR_UNSUPPORTED.
  * Set-up: the first call on a device, with that device current, looks up the
  * scratch's device address (cudaGetSymbolAddress, which may load the module);
- * make that first call before any stream capture.  Every call clears the
- * scratch's counters with one cudaMemsetAsync on `stream`.
+ * make that first call before any stream capture.  Nothing in the scratch
+ * needs to start at zero, so a call issues no copy or memset.
  * One scratch per device: calls that overlap on the GPU (other streams or
  * threads) race on it and give wrong results; serialise them. */
 #define MOE_W2_NOALLOC_SCRATCH_BYTES (16u << 20)

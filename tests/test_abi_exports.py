@@ -65,5 +65,5 @@ def test_noalloc_limit_matches_header(lib_path):
     cap = L.W2_NOALLOC_SCRATCH_BYTES
     assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 127, 2048, 4096) <= cap
     assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 128, 2048, 4096) > cap
-    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 254, 4096, 2048) <= cap
-    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 255, 4096, 2048) > cap
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 255, 4096, 2048) <= cap
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 256, 4096, 2048) > cap

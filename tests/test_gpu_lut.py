@@ -58,9 +58,10 @@ def _want(acc, x, off, perm, k, E, H, I):
 
 
 def _ws(rows, N_fc1, K_fc1, N_fc2, K_fc2):
+    """A workspace full of garbage (NaN patterns): its contents must not matter."""
     n = max(L.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, rows, N_fc1, K_fc1),
             L.moe_w2_mm_workspace_size(L.STAGE_FC2, rows, N_fc2, K_fc2))
-    return torch.zeros((n + 3) // 4, dtype=torch.int32, device=DEV)
+    return torch.full(((n + 3) // 4,), 0x7FC01234, dtype=torch.int32, device=DEV)
 
 
 @pytest.mark.parametrize("E,H,I,k,T", SHAPES)
@@ -83,8 +84,6 @@ def test_lut_stages_exact_sums(E, H, I, k, T):
         assert np.max(np.abs(host(h32).astype(np.float64) - want_h)) <= 1e-4 * rms_h
         rms_y = np.sqrt(np.mean(want_y ** 2))
         assert np.max(np.abs(host(y32).astype(np.float64) - want_y)) <= 1e-4 * rms_y
-        if use_ws is not None:   # counters and slice sums all back to zero
-            assert int(torch.count_nonzero(ws)) == 0
     assert L.moe_get_error(err) == 0
 
 
@@ -99,7 +98,7 @@ def test_lut_small_workspace_flags_overflow():
     L.moe_w2_mm(L.STAGE_FC1_SWIGLU, d_x, L.FMT_BF16, ml.c1k, ml.s1k, d_off, E, I, H, ref, L.FMT_BF16,
                 act_row=d_perm, act_row_div=k, mode=L.MODE_GEMV, ws=full)
     n = L.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, cap, I, H)
-    small = torch.zeros((n + 3) // 4, dtype=torch.int32, device=DEV)
+    small = torch.full(((n + 3) // 4,), -1, dtype=torch.int32, device=DEV)
     got = torch.full((A, I), 0x7FC0, dtype=torch.int16, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     L.moe_w2_mm(L.STAGE_FC1_SWIGLU, d_x, L.FMT_BF16, ml.c1k, ml.s1k, d_off, E, I, H, got, L.FMT_BF16,
@@ -107,7 +106,6 @@ def test_lut_small_workspace_flags_overflow():
     assert L.moe_get_error(err) & L.DEVERR_OVERFLOW
     assert torch.equal(got[:cap], ref[:cap])
     assert bool((got[cap:] == 0x7FC0).all())
-    assert int(torch.count_nonzero(small)) == 0
 
 
 def test_lut_skips_delta_cached_experts():
