@@ -51,7 +51,6 @@ constexpr int kPrologue = 8192;               // shared bytes below the table wi
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
-constexpr int kPrefetch = 2;                  // batches per warp prefetched to L2 ahead of the loads
 
 struct LutParams {
   const uint16_t* act;
@@ -161,28 +160,37 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   const int NSL = P.NSL, NB = P.NB;
   const bool fc1 = P.fc1 != 0;
 
-  // ---- selected rows per expert, exclusive prefix (warp 0)
-  if (warp == 0) {
-    int run = 0;
-    for (int b0 = 0; b0 <= P.E; b0 += 32) {
-      const int e = b0 + lane;
-      int n = 0;
+  // ---- selected rows per expert, exclusive prefix: every thread loads the
+  // counts of experts 2t and 2t+1 at once (one round trip), then a block scan
+  {
+    __shared__ int warp_tot[kLutWarps];
+    int n[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * tid + h;
       if (e < P.E) {
         const int c = P.offsets[e + 1] - P.offsets[e];
         bool sel = c > 0;
         if (sel && P.select == 1) sel = P.select_map[e] < 0;
         if (sel && P.select == 2) sel = P.select_map[e] >= 0;
-        if (sel) n = c;
+        if (sel) n[h] = c;
       }
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (e <= P.E) pref[e] = run + incl - n;
-      run += __shfl_sync(0xffffffffu, incl, 31);
     }
+    const int local = n[0] + n[1];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
+    const int excl = before + incl - local;
+    if (2 * tid <= P.E) pref[2 * tid] = excl;
+    if (2 * tid + 1 <= P.E) pref[2 * tid + 1] = excl + n[0];
+    if (tid == kLutThreads - 1) pref[P.E] = excl + local;  // the total (also for E = 1024)
   }
   __syncthreads();
   // the finishing kernel may be scheduled now; it waits for this grid's
@@ -226,72 +234,78 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   uint2 sc[8];
   float2 acc[16];  // row pairs (2i, 2i+1) of the batch
 
-  for (int64_t u = u_beg; u < u_end;) {
-    const int64_t seg = u / NB;
-    const int64_t seg0 = seg * NB;  // unit of batch 0 of this segment
-    const int64_t seg_end = min(u_end, seg0 + NB);
-    const int psel = static_cast<int>(seg / NSL);
-    const int s = static_cast<int>(seg - static_cast<int64_t>(psel) * NSL);
-    int lo = 0, hi = P.E;  // largest e with pref[e] <= psel
+  auto expert_of = [&](int psel) {  // largest e with pref[e] <= psel
+    int lo = 0, hi = P.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (pref[mid] <= psel) lo = mid; else hi = mid;
     }
-    const int e = lo;
+    return lo;
+  };
+  // quad index (rows 4Q..4Q+3 of the expert) of quad q of batch rb: FC1
+  // batches are 16 gate rows then the 16 matching up rows
+  auto quad_of = [&](int rb, int q) -> uint32_t {
+    if (fc1) return static_cast<uint32_t>(q < 4 ? rb * 4 + q : (P.N >> 2) + rb * 4 + (q - 4));
+    return static_cast<uint32_t>(rb * 8 + q);
+  };
+  // this lane's code / scale addresses in slice s of expert e
+  auto codes_at = [&](int e, int sl) { return P.codes + e * mat_codes + sl * slice_codes + lane * 16; };
+  auto scales_at = [&](int e, int sl) {
+    return reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + sl * slice_scales) + (lane >> 1) * 8;
+  };
+  auto issue = [&](const uint8_t* gc, const uint8_t* gs, int rb) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t Q = quad_of(rb, q);
+      v[q] = ldg_stream(gc + Q * 512u);
+      sc[q] = ldg_stream2(gs + Q * 128u);
+    }
+  };
+
+  if (u_beg >= u_end) return;
+  // A warp's units: batches warp, warp + 16, ... of each segment (one segment
+  // = one (row, slice) table) of the CTA's range.  The loads of a warp's next
+  // unit go out while the current one is consumed, also across a segment
+  // boundary; the row checks (which need global loads) only gate the table
+  // build and the stores, never the weight loads.
+  int64_t seg = u_beg / NB;
+  int psel = static_cast<int>(seg / NSL);
+  int s = static_cast<int>(seg - static_cast<int64_t>(psel) * NSL);
+  int e = expert_of(psel);
+  const uint8_t* gcodes = codes_at(e, s);
+  const uint8_t* gscales = scales_at(e, s);
+  int64_t seg_end = min(u_end, (seg + 1) * NB);
+  int64_t uw = u_beg + warp;
+  bool pending = false;
+  if (uw < seg_end) {
+    issue(gcodes, gscales, static_cast<int>(uw - seg * NB));
+    pending = true;
+  }
+  while (true) {
+    const int64_t seg0 = seg * NB;
+    const bool has_next = seg_end < u_end;
+    const int64_t nseg_end = min(u_end, seg_end + NB);
     const int p = P.offsets[e] + (psel - pref[e]);
-    int64_t uw = u + warp;
-    u = seg_end;
-    if (p >= P.A) {  // the scratch does not cover this row: report and skip
+    int row = 0;
+    bool valid = p < P.A;
+    if (!valid) {  // the scratch does not cover this row: report and skip
       if (tid == 0) set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
-      continue;
-    }
-    const int row = P.act_row ? P.act_row[p] / P.act_row_div : p;
-    if (row < 0 || row >= P.act_rows) {
-      if (tid == 0) set_err(P.dev_err, MOE_DEVERR_BAD_ID);
-      continue;
-    }
-    const uint8_t* gcodes = P.codes + e * mat_codes + s * slice_codes + lane * 16;
-    const uint8_t* gscales =
-        reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + s * slice_scales) + (lane >> 1) * 8;
-    // quad index (rows 4Q..4Q+3 of the expert) of quad q of batch rb: FC1
-    // batches are 16 gate rows then the 16 matching up rows
-    auto quad_of = [&](int rb, int q) -> uint32_t {
-      if (fc1) return static_cast<uint32_t>(q < 4 ? rb * 4 + q : (P.N >> 2) + rb * 4 + (q - 4));
-      return static_cast<uint32_t>(rb * 8 + q);
-    };
-    // one warp batch's codes and scales to L2 (lane 0; FC1: gate and up halves)
-    auto prefetch_batch = [&](int rb) {
-      const uint8_t* c0 = gcodes - lane * 16;
-      const uint8_t* s0 = gscales - (lane >> 1) * 8;
-      if (fc1) {
-        prefetch_l2(c0 + quad_of(rb, 0) * 512u, 2048);
-        prefetch_l2(c0 + quad_of(rb, 4) * 512u, 2048);
-        prefetch_l2(s0 + quad_of(rb, 0) * 128u, 512);
-        prefetch_l2(s0 + quad_of(rb, 4) * 128u, 512);
-      } else {
-        prefetch_l2(c0 + quad_of(rb, 0) * 512u, 4096);
-        prefetch_l2(s0 + quad_of(rb, 0) * 128u, 1024);
+    } else {
+      row = P.act_row ? P.act_row[p] / P.act_row_div : p;
+      if (row < 0 || row >= P.act_rows) {
+        valid = false;
+        if (tid == 0) set_err(P.dev_err, MOE_DEVERR_BAD_ID);
       }
-    };
-    if (lane == 0) {
-#pragma unroll
-      for (int d = 1; d <= kPrefetch; ++d)
-        if (uw + d * kLutWarps < seg_end) prefetch_batch(static_cast<int>(uw + d * kLutWarps - seg0));
     }
-    if (uw < seg_end) {
-      const int rb = static_cast<int>(uw - seg0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t Q = quad_of(rb, q);
-        v[q] = ldg_stream(gcodes + Q * 512u);
-        sc[q] = ldg_stream2(gscales + Q * 128u);
-      }
+    if (!pending && uw < seg_end) {
+      issue(gcodes, gscales, static_cast<int>(uw - seg0));
+      pending = true;
     }
 
     // ---- (re)build the tables for (row, s): warp w writes byte-in-word j = w & 3
     // and code bytes b in [64*(w>>2), +64); lane l is byte position 4l + j
     __syncthreads();  // nobody still reads the previous segment's tables
-    {
+    if (valid) {
       const int j = warp & 3, bq = warp >> 2;
       const uint2 xv = *reinterpret_cast<const uint2*>(P.act + static_cast<size_t>(row) * P.K + s * kSW + 16 * lane +
                                                        4 * j);
@@ -315,36 +329,67 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     }
     __syncthreads();
 
-    for (; uw < seg_end; uw += kLutWarps) {
+    while (uw < seg_end) {
       const int rb = static_cast<int>(uw - seg0);
-      const int rbn = rb + kLutWarps;
-      const bool more = uw + kLutWarps < seg_end;
-      if (lane == 0 && uw + (kPrefetch + 1) * kLutWarps < seg_end)
-        prefetch_batch(rb + (kPrefetch + 1) * kLutWarps);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 w4 = v[q];
-        const uint2 s4 = sc[q];
-        acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
-        acc[2 * q + 1] = word_pair(w4.z, w4.w, s4.y, lanebase);
-        if (more) {  // the next batch's loads go out while this one is consumed
-          const uint32_t Q = quad_of(rbn, q);
-          v[q] = ldg_stream(gcodes + Q * 512u);
-          sc[q] = ldg_stream2(gscales + Q * 128u);
+      // the warp's next unit: the same segment, or its first batch of the next
+      int64_t un = uw + kLutWarps;
+      const uint8_t* nc = gcodes;
+      const uint8_t* ns = gscales;
+      int rbn = rb + kLutWarps;
+      bool more = un < seg_end;
+      if (!more) {
+        un = seg_end + warp;
+        more = has_next && un < nseg_end;
+        if (more) {
+          const int64_t nseg = seg + 1;
+          const int np = static_cast<int>(nseg / NSL);
+          const int nsl = static_cast<int>(nseg - static_cast<int64_t>(np) * NSL);
+          const int ne = expert_of(np);
+          nc = codes_at(ne, nsl);
+          ns = scales_at(ne, nsl);
+          rbn = warp;
         }
       }
-      // ---- reduce-scatter: afterwards lane l holds the slice sum of batch row l
-      rs_level2<8>(acc, lane, 16);
-      rs_level2<4>(acc, lane, 8);
-      rs_level2<2>(acc, lane, 4);
-      rs_level2<1>(acc, lane, 2);
-      const bool odd = (lane & 1) != 0;
-      const float keep = odd ? acc[0].y : acc[0].x;
-      const float send = odd ? acc[0].x : acc[0].y;
-      const float sum = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-      const size_t cell = static_cast<size_t>(p) * NB + rb;
-      __stcg(P.scratch + (cell * NSL + s) * 32 + lane, sum);
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w4 = v[q];
+          const uint2 s4 = sc[q];
+          acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
+          acc[2 * q + 1] = word_pair(w4.z, w4.w, s4.y, lanebase);
+          if (more) {  // the next unit's loads go out while this one is consumed
+            const uint32_t Q = quad_of(rbn, q);
+            v[q] = ldg_stream(nc + Q * 512u);
+            sc[q] = ldg_stream2(ns + Q * 128u);
+          }
+        }
+        // ---- reduce-scatter: afterwards lane l holds the slice sum of batch row l
+        rs_level2<8>(acc, lane, 16);
+        rs_level2<4>(acc, lane, 8);
+        rs_level2<2>(acc, lane, 4);
+        rs_level2<1>(acc, lane, 2);
+        const bool odd = (lane & 1) != 0;
+        const float keep = odd ? acc[0].y : acc[0].x;
+        const float send = odd ? acc[0].x : acc[0].y;
+        const float sum = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        const size_t cell = static_cast<size_t>(p) * NB + rb;
+        __stcg(P.scratch + (cell * NSL + s) * 32 + lane, sum);
+      } else if (more) {
+        issue(nc, ns, rbn);
+      }
+      uw = un;
+      pending = more;
     }
+    if (!has_next) break;
+    // ---- advance to the next segment
+    uw = seg_end + warp;
+    ++seg;
+    psel = static_cast<int>(seg / NSL);
+    s = static_cast<int>(seg - static_cast<int64_t>(psel) * NSL);
+    e = expert_of(psel);
+    gcodes = codes_at(e, s);
+    gscales = scales_at(e, s);
+    seg_end = nseg_end;
   }
 }
 
