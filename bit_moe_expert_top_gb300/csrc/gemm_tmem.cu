@@ -1,0 +1,605 @@
+// Grouped expert matmul on the tensor cores with the dequantised WEIGHTS as
+// the A operand in tensor memory (tcgen05 "A from TMEM" form).
+//
+// For each expert group (permuted rows offsets[e]..offsets[e+1]) the CTA
+// computes, per tile of NT tokens and a pair of 128-row weight blocks,
+//     D0[128 x NT] = W_block0 . X^T,   D1[128 x NT] = W_block1 . X^T
+// (FC1: block 0 = 128 gate rows, block 1 = the matching 128 up rows, so a
+// thread of the epilogue holds g and u of the same output; FC2: two
+// consecutive 128-row blocks).  TMEM lane = weight row, column = token.
+//
+//   warp 0      TMA: token tiles [NT rows x 64 K] bf16 (128-byte swizzle)
+//   warp 1      TMEM allocation; one thread issues tcgen05.mma kind::f16
+//               (A from TMEM, B = token tile in shared memory, M=128, N=NT,
+//               K=16) for both blocks, tcgen05.commit frees the stage
+//   warps 2-9   weight decode: each thread owns one weight row of one block
+//               (its TMEM lane) and per 64-K stage turns the row's codes into
+//               64 bf16 values in registers and writes them to its lane of
+//               the stage's A columns with tcgen05.st.  The decoded weights
+//               never touch shared memory, so the tensor core keeps the
+//               shared-memory bandwidth for the token tiles.
+//   warps 10-13 epilogue: tcgen05.ld of D0/D1 (a warp reads its 32 lanes),
+//               SwiGLU for FC1, rounding, stores (32 lanes = 32 consecutive
+//               outputs of one token row: coalesced)
+//
+// 2-bit decode: a per-lane copy of the 256-entry byte -> 4 bf16 codebook
+// table (64 KB at a 64 KB-aligned shared address, lane l's copy in banks
+// 2l, 2l+1) is read with one PRMT-formed address per code byte, then scaled
+// by the group's bf16 scale (exact: the entries are powers of two).
+//
+// Tiles (expert, weight-block pair, token tile) with the token tiles of one
+// weight block adjacent (the blocks' weights are read from HBM once and then
+// from L2); a persistent grid walks them round-robin.  Tokens of a tile past
+// the group end are computed but not stored.  Every mbarrier wait is bounded
+// (MOE_DEVERR_TIMEOUT).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTmWarps = 14;
+constexpr int kTmThreads = kTmWarps * 32;
+constexpr int kKB = 64;    // K per stage (one 128-byte swizzle row of bf16)
+constexpr int kTS = 3;     // pipeline stages
+constexpr int kPre = 16384;  // shared bytes for barriers and the tile tables (before the LUT window)
+
+enum { kFmtW2 = 0, kFmtE4M3 = 1 };
+
+struct TmParams {
+  const uint8_t* wq;        // W2: w2l codes; E4M3: workspace bytes [slots][R][K]
+  const uint16_t* wscale;   // W2: w2l bf16 scales
+  const int32_t* wslot_of;  // E4M3: expert -> workspace slot (< 0: skipped)
+  const int32_t* select_map;
+  int select;
+  const int32_t* offsets;
+  int E, N, K, R;
+  int fc1;
+  void* out;
+  int out_fmt;
+  uint32_t* dev_err;
+};
+
+// ------------------------------------------------------------------ PTX
+MOE_D void tm_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+MOE_D void tm_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
+MOE_D void tm_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+MOE_D void tm_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MOE_D void tm_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16 (bf16 x bf16 -> fp32)
+MOE_D void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+MOE_D void umma_commit_to(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+MOE_D void tm_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+MOE_D void tm_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 consecutive TMEM columns of this thread's lane (warp-collective).
+MOE_D void tm_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+MOE_D void tm_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+MOE_D void tma_load_tile(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzle
+// layout (8-row atoms of 1024 bytes stacked along N).
+MOE_D uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor: BF16 x BF16 -> FP32, both K-major, M x N.
+MOE_HD uint32_t idesc_bf16_mn(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+MOE_D uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  const __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  x = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&x);
+}
+
+// One code word's four LUT entries (4 bf16 each) for this lane, scaled.
+MOE_D void w2_decode_word(uint32_t w, uint32_t lanebase, uint32_t sc2, uint32_t* o) {
+  uint32_t a0, a1, a2, a3;
+  asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(a0) : "r"(w), "r"(lanebase));
+  asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(a1) : "r"(w), "r"(lanebase));
+  asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(a2) : "r"(w), "r"(lanebase));
+  asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(a3) : "r"(w), "r"(lanebase));
+  uint2 e0, e1, e2, e3;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(e0.x), "=r"(e0.y) : "r"(a0));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(e1.x), "=r"(e1.y) : "r"(a1));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(e2.x), "=r"(e2.y) : "r"(a2));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(e3.x), "=r"(e3.y) : "r"(a3));
+  o[0] = bf16x2_mul(e0.x, sc2);
+  o[1] = bf16x2_mul(e0.y, sc2);
+  o[2] = bf16x2_mul(e1.x, sc2);
+  o[3] = bf16x2_mul(e1.y, sc2);
+  o[4] = bf16x2_mul(e2.x, sc2);
+  o[5] = bf16x2_mul(e2.y, sc2);
+  o[6] = bf16x2_mul(e3.x, sc2);
+  o[7] = bf16x2_mul(e3.y, sc2);
+}
+
+// Two E4M3 bytes -> bf16x2 (exact: every E4M3 value is a bf16 value).
+MOE_D uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  const float2 f = e4m3x2_to_f32x2(static_cast<uint16_t>(two));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
+  return r;
+}
+
+template <int WF, int NT>
+__global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_constant__ CUtensorMap tmap_b,
+                                                                const TmParams P) {
+  constexpr int kBTile = NT * kKB * 2;  // token tile bytes per stage
+  constexpr uint32_t kColA = 2 * NT;   // first A column (after D0, D1)
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = smem_u32(smem);
+  // [barriers, tile table][LUT window (W2), 64 KB aligned][token tiles, 1024 aligned]
+  const uint32_t win = (base + kPre + 65535u) & ~65535u;
+  const uint32_t tiles_off =
+      (WF == kFmtW2) ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
+  uint8_t* tiles = smem + tiles_off;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* full_b = full_a + kTS;
+  uint64_t* empty = full_b + kTS;
+  uint64_t* acc_full = empty + kTS;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  int* flags = reinterpret_cast<int*>(tmem_base_s + 2);
+  int* tile_start = flags + 8;  // [E+1]
+  int* wslot = tile_start + (P.E + 1);  // [E] weight slot of each expert (-1: skipped)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool fc1 = P.fc1 != 0;
+  const int NBLK = fc1 ? P.N / 128 : P.N / 256;  // weight-block pairs
+  const int KB = P.K / kKB;
+
+  // ---- setup
+  for (int e = tid; e < P.E; e += kTmThreads) {
+    int sl = -1;
+    if (P.offsets[e + 1] > P.offsets[e]) {
+      if (WF == kFmtW2) {
+        sl = e;
+        if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
+      } else {
+        sl = P.wslot_of ? P.wslot_of[e] : e;
+      }
+    }
+    wslot[e] = sl;
+  }
+  if (WF == kFmtW2) {  // per-lane codebook LUT: entry b of lane l at win + 256 b + 8 l
+    const uint32_t ent[4] = {0xC080u, 0xBF80u, 0x3F80u, 0x4080u};  // -4, -1, 1, 4 as bf16
+    for (int i = tid; i < 256 * 32; i += kTmThreads) {
+      const uint32_t b = static_cast<uint32_t>(i >> 5);
+      const uint2 v =
+          make_uint2(ent[b & 3] | (ent[(b >> 2) & 3] << 16), ent[(b >> 4) & 3] | (ent[b >> 6] << 16));
+      *reinterpret_cast<uint2*>(smem + (win - base) + b * 256u + (i & 31) * 8u) = v;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int b0 = 0; b0 <= P.E; b0 += 32) {
+      const int e = b0 + lane;
+      int n = 0;
+      if (e < P.E && wslot[e] >= 0) n = ((P.offsets[e + 1] - P.offsets[e] + NT - 1) / NT) * NBLK;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e <= P.E) tile_start[e] = run + incl - n;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kTS; ++s) {
+      mbar_init(&full_a[s], 8);
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    flags[0] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tm_alloc(tmem_base_s, 512);
+    tm_relinquish();
+  }
+  tm_fence_before();
+  __syncthreads();
+  tm_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  const int total = tile_start[P.E];
+
+  auto decode_tile = [&](int i, int& e, int& blk, int& mt) {
+    int lo = 0, hi = P.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_start[mid] <= i) lo = mid; else hi = mid;
+    }
+    e = lo;
+    const int loc = i - tile_start[e];
+    const int nm = (P.offsets[e + 1] - P.offsets[e] + NT - 1) / NT;
+    blk = loc / nm;
+    mt = loc - blk * nm;
+  };
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&flags[0]) != 0; };
+  auto abort_all = [&]() {
+    flags[0] = 1;
+    set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ================= token tiles by TMA =================
+    if (lane == 0) {
+      uint32_t L = 0;
+      for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
+        int e, blk, mt;
+        decode_tile(i, e, blk, mt);
+        const int row0 = P.offsets[e] + mt * NT;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          const int s = L % kTS;
+          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_b[s], kBTile);
+          tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+        }
+        if (!ok) {
+          abort_all();
+          break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issue =================
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_mn(128, NT);
+      uint32_t L = 0;
+      int t = 0;
+      for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
+        if (t >= 1 && !mbar_wait(acc_empty, (t - 1) & 1)) {
+          abort_all();
+          break;
+        }
+        tm_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          const int s = L % kTS;
+          const uint32_t par = (L / kTS) & 1;
+          if (!mbar_wait(&full_b[s], par) || !mbar_wait(&full_a[s], par)) {
+            ok = false;
+            break;
+          }
+          tm_fence_after();
+          const uint32_t sb = smem_u32(tiles + s * kBTile);
+          const uint32_t a0 = tmem + kColA + static_cast<uint32_t>(s * 64);
+#pragma unroll
+          for (int ks = 0; ks < kKB / 16; ++ks) {
+            const uint64_t bd = desc_sw128(sb + ks * 32);
+            const uint32_t acc = (kb | ks) != 0;
+            umma_ts(tmem, a0 + ks * 8, bd, idesc, acc);
+            umma_ts(tmem + NT, a0 + 32 + ks * 8, bd, idesc, acc);
+          }
+          umma_commit_to(&empty[s]);
+        }
+        if (!ok) {
+          abort_all();
+          break;
+        }
+        umma_commit_to(acc_full);
+      }
+    }
+  } else if (warp < 10) {
+    // ================= weight decode: one weight row per thread =================
+    const int d = warp - 2;
+    const int bsel = d >> 2;       // weight block 0 / 1
+    const int q = warp & 3;        // TMEM lane quarter this warp may access
+    const int m = 32 * q + lane;   // row within the 128-row block
+    const uint32_t lanebase = win + 8u * static_cast<uint32_t>(lane);
+    const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
+    // weight row (within the expert) of block bsel of pair blk
+    auto wrow = [&](int blk) {
+      return fc1 ? (bsel ? P.N : 0) + blk * 128 + m : blk * 256 + bsel * 128 + m;
+    };
+    uint32_t L = 0;
+    bool ok = true;
+    if (WF == kFmtW2) {
+      const int SW = w2l_sw(P.K), NLn = SW / 16, Gs = SW / 32;
+      const int64_t mat_words = static_cast<int64_t>(P.R) * (P.K / 16);
+      const int64_t mat_sc = static_cast<int64_t>(P.R) * (P.K / 32);
+      const uint32_t* codes32 = reinterpret_cast<const uint32_t*>(P.wq);
+      // codes (4 words) and the two group scales of (tile i, k-block kb)
+      auto load = [&](int e, int r, int kb, uint32_t (&w)[4], uint32_t& sc) {
+        const int k0 = kb * kKB;
+        const int sl = k0 / SW, lb = (k0 % SW) / 16;
+        const uint32_t* wp = codes32 + e * mat_words + static_cast<int64_t>(sl) * (P.R * NLn) +
+                             static_cast<int64_t>(r / 4) * (4 * NLn) + lb * 4 + (r & 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = __ldg(wp + 4 * j);
+        const int g = (k0 % SW) / 32;
+        const uint16_t* sp = P.wscale + e * mat_sc + static_cast<int64_t>(sl) * (P.R * Gs) +
+                             static_cast<int64_t>(r / 4) * (4 * Gs) + g * 4 + (r & 3);
+        sc = static_cast<uint32_t>(__ldg(sp)) | (static_cast<uint32_t>(__ldg(sp + 4)) << 16);
+      };
+      uint32_t w[4], sc = 0;
+      int i = blockIdx.x;
+      int e = 0, blk = 0, mt = 0;
+      if (i < total) {
+        decode_tile(i, e, blk, mt);
+        load(e, wrow(blk), 0, w, sc);
+      }
+      for (; i < total && ok && !aborted(); i += gridDim.x) {
+        int ni = i + gridDim.x, ne = 0, nblk = 0, nmt = 0;
+        if (ni < total) decode_tile(ni, ne, nblk, nmt);
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          // the next stage's codes go out before this one is decoded
+          uint32_t wn[4] = {0, 0, 0, 0}, scn = 0;
+          if (kb + 1 < KB) load(e, wrow(blk), kb + 1, wn, scn);
+          else if (ni < total) load(ne, wrow(nblk), 0, wn, scn);
+          const int s = L % kTS;
+          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tm_fence_after();  // the MMAs that read this A stage are complete
+          uint32_t o[32];
+          const uint32_t s_lo = (sc & 0xffffu) | (sc << 16), s_hi = (sc >> 16) | (sc & 0xffff0000u);
+          w2_decode_word(w[0], lanebase, s_lo, o);
+          w2_decode_word(w[1], lanebase, s_lo, o + 8);
+          w2_decode_word(w[2], lanebase, s_hi, o + 16);
+          w2_decode_word(w[3], lanebase, s_hi, o + 24);
+          tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+          tm_st_wait();
+          tm_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_a[s]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w[j] = wn[j];
+          sc = scn;
+        }
+        e = ne;
+        blk = nblk;
+        mt = nmt;
+      }
+    } else {  // E4M3 workspace: [slot][R][K] bytes, scale folded in
+      const int64_t mat = static_cast<int64_t>(P.R) * P.K;
+      uint4 v[4];
+      auto load = [&](int e, int r, int kb, uint4 (&x)[4]) {
+        const uint4* p = reinterpret_cast<const uint4*>(P.wq + wslot[e] * mat + static_cast<int64_t>(r) * P.K + kb * kKB);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = __ldg(p + j);
+      };
+      int i = blockIdx.x;
+      int e = 0, blk = 0, mt = 0;
+      if (i < total) {
+        decode_tile(i, e, blk, mt);
+        load(e, wrow(blk), 0, v);
+      }
+      for (; i < total && ok && !aborted(); i += gridDim.x) {
+        int ni = i + gridDim.x, ne = 0, nblk = 0, nmt = 0;
+        if (ni < total) decode_tile(ni, ne, nblk, nmt);
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          uint4 vn[4];
+          if (kb + 1 < KB) load(e, wrow(blk), kb + 1, vn);
+          else if (ni < total) load(ne, wrow(nblk), 0, vn);
+          const int s = L % kTS;
+          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tm_fence_after();  // the MMAs that read this A stage are complete
+          uint32_t o[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t ww[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              o[8 * j + 2 * h] = e4m3x2_to_bf16x2(ww[h] & 0xffffu);
+              o[8 * j + 2 * h + 1] = e4m3x2_to_bf16x2(ww[h] >> 16);
+            }
+          }
+          tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+          tm_st_wait();
+          tm_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_a[s]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = vn[j];
+        }
+        e = ne;
+        blk = nblk;
+        mt = nmt;
+      }
+    }
+    if (!ok) abort_all();
+  } else {
+    // ================= epilogue =================
+    const int q = warp & 3;
+    const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
+    int t = 0;
+    for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
+      int e, blk, mt;
+      decode_tile(i, e, blk, mt);
+      if (!mbar_wait(acc_full, t & 1)) {
+        abort_all();
+        break;
+      }
+      tm_fence_after();
+      const int p0 = P.offsets[e] + mt * NT;
+      const int nvalid = min(NT, P.offsets[e + 1] - p0);
+      const int n0 = fc1 ? blk * 128 + 32 * q + lane : blk * 256 + 32 * q + lane;
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 32) {
+        uint32_t r0[32], r1[32];
+        tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
+        tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
+        tm_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c + j < nvalid) {
+            const size_t prow = static_cast<size_t>(p0 + c + j) * P.N;
+            if (fc1) {
+              const float h = silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+              if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[prow + n0] = h;
+              else static_cast<uint16_t*>(P.out)[prow + n0] = f32_to_bf16_rne(h);
+            } else {
+              if (P.out_fmt == MOE_FMT_F32) {
+                static_cast<float*>(P.out)[prow + n0] = __uint_as_float(r0[j]);
+                static_cast<float*>(P.out)[prow + n0 + 128] = __uint_as_float(r1[j]);
+              } else {
+                static_cast<uint16_t*>(P.out)[prow + n0] = f32_to_bf16_rne(__uint_as_float(r0[j]));
+                static_cast<uint16_t*>(P.out)[prow + n0 + 128] = f32_to_bf16_rne(__uint_as_float(r1[j]));
+              }
+            }
+          }
+        }
+      }
+      tm_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+
+  // ---- teardown: every role is done (or gave up); free TMEM
+  tm_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tm_fence_after();
+    tm_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+template <int WF, int NT>
+cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const TmParams& P, cudaStream_t s) {
+  const size_t smem = (WF == kFmtW2 ? static_cast<size_t>(kPre) + 65536 + 65536 : static_cast<size_t>(kPre)) +
+                      static_cast<size_t>(kTS) * NT * kKB * 2 + 1024;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  tmem_mm_kernel<WF, NT><<<device_info().sms, kTmThreads, smem, s>>>(map, P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tmem_mm_supported(const MMArgs& a) {
+  if (a.act_fmt != MOE_FMT_BF16 || a.act_row != nullptr) return false;
+  if (a.out_fmt != MOE_FMT_BF16 && a.out_fmt != MOE_FMT_F32) return false;
+  if (a.expert_begin != 0 || a.expert_end != a.E || a.E > 1024) return false;
+  if (a.K % kKB) return false;
+  if (a.stage == MOE_STAGE_FC1_SWIGLU ? a.N % 128 : a.N % 256) return false;
+  if (a.wkind == kW2) return a.K % w2l_sw(a.K) == 0;
+  if (a.wkind == kFP8) return a.select == 0;  // the workspace slot map does the selection
+  return false;
+}
+
+cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  TmParams P;
+  P.wq = a.wq;
+  P.wscale = static_cast<const uint16_t*>(a.wscale);
+  P.wslot_of = a.wslot_of;
+  P.select_map = a.select_map;
+  P.select = a.select;
+  P.offsets = a.offsets;
+  P.E = a.E;
+  P.N = a.N;
+  P.K = a.K;
+  P.fc1 = a.stage == MOE_STAGE_FC1_SWIGLU;
+  P.R = P.fc1 ? 2 * a.N : a.N;
+  P.out = a.out;
+  P.out_fmt = a.out_fmt;
+  P.dev_err = a.dev_err;
+  constexpr int NT = 128;
+  // tokens: [rows_total][K] bf16, box 64 x NT with the 128-byte swizzle
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
+  const cuuint32_t box[2] = {kKB, NT};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.act), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (a.wkind == kW2) return launch_tm<kFmtW2, NT>(a, map, P, s);
+  return launch_tm<kFmtE4M3, NT>(a, map, P, s);
+}
+
+}  // namespace moe

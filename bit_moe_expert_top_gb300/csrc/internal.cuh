@@ -79,6 +79,9 @@ int lut_workspace_rows(int stage, size_t bytes, int N, int K);
 cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s);
 bool gemm_supported(const MMArgs& a);
 cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
+// tensor-core grouped matmul with the dequantised weights in TMEM (gemm_tmem.cu)
+bool tmem_mm_supported(const MMArgs& a);
+cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 
 // ---- the table GEMV on the library's own fixed scratch (noalloc.cu)
 // Device address of the scratch array on the current device (looked up on the
