@@ -48,7 +48,9 @@ constexpr int kTmWarps = 14;
 constexpr int kTmThreads = kTmWarps * 32;
 constexpr int kKB = 64;    // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kTS = 3;     // pipeline stages
-constexpr int kPre = 16384;  // shared bytes for barriers and the tile tables (before the LUT window)
+constexpr int kTab = 16384;             // barriers and tile tables
+constexpr int kStg = 128 * 128 * 2;     // epilogue staging: [NT tokens][128 outputs] bf16
+constexpr int kPre = kTab + kStg;       // shared bytes before the LUT window
 
 enum { kFmtW2 = 0, kFmtE4M3 = 1 };
 
@@ -356,121 +358,137 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     auto wrow = [&](int blk) {
       return fc1 ? (bsel ? P.N : 0) + blk * 128 + m : blk * 256 + bsel * 128 + m;
     };
-    uint32_t L = 0;
+    // this CTA's tiles are blockIdx.x, +gridDim.x, ...; flat stage index L
+    const int ntile = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const uint32_t Ltot = static_cast<uint32_t>(ntile) * static_cast<uint32_t>(KB);
+    // prefetch cursor: (tile pi, k-block pkb) of the next stage to load
+    int pi = blockIdx.x, pkb = 0, pe = 0, pblk = 0, pmt = 0;
+    if (pi < total) decode_tile(pi, pe, pblk, pmt);
+    auto advance = [&]() {
+      if (++pkb == KB) {
+        pkb = 0;
+        pi += gridDim.x;
+        if (pi < total) decode_tile(pi, pe, pblk, pmt);
+      }
+    };
     bool ok = true;
     if (WF == kFmtW2) {
+      constexpr int D = 3;  // stages of codes in flight per thread
       const int SW = w2l_sw(P.K), NLn = SW / 16, Gs = SW / 32;
       const int64_t mat_words = static_cast<int64_t>(P.R) * (P.K / 16);
       const int64_t mat_sc = static_cast<int64_t>(P.R) * (P.K / 32);
       const uint32_t* codes32 = reinterpret_cast<const uint32_t*>(P.wq);
-      // codes (4 words) and the two group scales of (tile i, k-block kb)
-      auto load = [&](int e, int r, int kb, uint32_t (&w)[4], uint32_t& sc) {
-        const int k0 = kb * kKB;
+      uint32_t wb[D][4], sb[D];
+      // codes (4 words) and the two group scales of the cursor's stage
+      auto load = [&](uint32_t (&w)[4], uint32_t& sc) {
+        if (pi >= total) return;
+        const int r = wrow(pblk);
+        const int k0 = pkb * kKB;
         const int sl = k0 / SW, lb = (k0 % SW) / 16;
-        const uint32_t* wp = codes32 + e * mat_words + static_cast<int64_t>(sl) * (P.R * NLn) +
+        const uint32_t* wp = codes32 + pe * mat_words + static_cast<int64_t>(sl) * (P.R * NLn) +
                              static_cast<int64_t>(r / 4) * (4 * NLn) + lb * 4 + (r & 3);
 #pragma unroll
         for (int j = 0; j < 4; ++j) w[j] = __ldg(wp + 4 * j);
         const int g = (k0 % SW) / 32;
-        const uint16_t* sp = P.wscale + e * mat_sc + static_cast<int64_t>(sl) * (P.R * Gs) +
+        const uint16_t* sp = P.wscale + pe * mat_sc + static_cast<int64_t>(sl) * (P.R * Gs) +
                              static_cast<int64_t>(r / 4) * (4 * Gs) + g * 4 + (r & 3);
         sc = static_cast<uint32_t>(__ldg(sp)) | (static_cast<uint32_t>(__ldg(sp + 4)) << 16);
+        advance();
       };
-      uint32_t w[4], sc = 0;
-      int i = blockIdx.x;
-      int e = 0, blk = 0, mt = 0;
-      if (i < total) {
-        decode_tile(i, e, blk, mt);
-        load(e, wrow(blk), 0, w, sc);
-      }
-      for (; i < total && ok && !aborted(); i += gridDim.x) {
-        int ni = i + gridDim.x, ne = 0, nblk = 0, nmt = 0;
-        if (ni < total) decode_tile(ni, ne, nblk, nmt);
-        for (int kb = 0; kb < KB; ++kb, ++L) {
-          // the next stage's codes go out before this one is decoded
-          uint32_t wn[4] = {0, 0, 0, 0}, scn = 0;
-          if (kb + 1 < KB) load(e, wrow(blk), kb + 1, wn, scn);
-          else if (ni < total) load(ne, wrow(nblk), 0, wn, scn);
-          const int s = L % kTS;
-          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tm_fence_after();  // the MMAs that read this A stage are complete
-          uint32_t o[32];
-          const uint32_t s_lo = (sc & 0xffffu) | (sc << 16), s_hi = (sc >> 16) | (sc & 0xffff0000u);
-          w2_decode_word(w[0], lanebase, s_lo, o);
-          w2_decode_word(w[1], lanebase, s_lo, o + 8);
-          w2_decode_word(w[2], lanebase, s_hi, o + 16);
-          w2_decode_word(w[3], lanebase, s_hi, o + 24);
-          tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
-          tm_st_wait();
-          tm_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full_a[s]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) w[j] = wn[j];
-          sc = scn;
-        }
-        e = ne;
-        blk = nblk;
-        mt = nmt;
-      }
-    } else {  // E4M3 workspace: [slot][R][K] bytes, scale folded in
-      const int64_t mat = static_cast<int64_t>(P.R) * P.K;
-      uint4 v[4];
-      auto load = [&](int e, int r, int kb, uint4 (&x)[4]) {
-        const uint4* p = reinterpret_cast<const uint4*>(P.wq + wslot[e] * mat + static_cast<int64_t>(r) * P.K + kb * kKB);
+      for (int d0 = 0; d0 < D; ++d0) load(wb[d0], sb[d0]);
+      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = __ldg(p + j);
-      };
-      int i = blockIdx.x;
-      int e = 0, blk = 0, mt = 0;
-      if (i < total) {
-        decode_tile(i, e, blk, mt);
-        load(e, wrow(blk), 0, v);
-      }
-      for (; i < total && ok && !aborted(); i += gridDim.x) {
-        int ni = i + gridDim.x, ne = 0, nblk = 0, nmt = 0;
-        if (ni < total) decode_tile(ni, ne, nblk, nmt);
-        for (int kb = 0; kb < KB; ++kb, ++L) {
-          uint4 vn[4];
-          if (kb + 1 < KB) load(e, wrow(blk), kb + 1, vn);
-          else if (ni < total) load(ne, wrow(nblk), 0, vn);
-          const int s = L % kTS;
-          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tm_fence_after();  // the MMAs that read this A stage are complete
-          uint32_t o[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t ww[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              o[8 * j + 2 * h] = e4m3x2_to_bf16x2(ww[h] & 0xffffu);
-              o[8 * j + 2 * h + 1] = e4m3x2_to_bf16x2(ww[h] >> 16);
+        for (int d0 = 0; d0 < D; ++d0) {
+          const uint32_t L = L0 + d0;
+          if (L < Ltot && ok) {
+            const int s = L % kTS;
+            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+              ok = false;
+            } else {
+              tm_fence_after();  // the MMAs that read this A stage are complete
+              uint32_t o[32];
+              const uint32_t sc = sb[d0];
+              const uint32_t s_lo = (sc & 0xffffu) | (sc << 16), s_hi = (sc >> 16) | (sc & 0xffff0000u);
+              w2_decode_word(wb[d0][0], lanebase, s_lo, o);
+              w2_decode_word(wb[d0][1], lanebase, s_lo, o + 8);
+              w2_decode_word(wb[d0][2], lanebase, s_hi, o + 16);
+              w2_decode_word(wb[d0][3], lanebase, s_hi, o + 24);
+              load(wb[d0], sb[d0]);  // stage L + D
+              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+              tm_st_wait();
+              tm_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&full_a[s]);
             }
           }
-          tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
-          tm_st_wait();
-          tm_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full_a[s]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = vn[j];
         }
-        e = ne;
-        blk = nblk;
-        mt = nmt;
+      }
+    } else {  // E4M3 workspace: [slot][R][K] bytes, scale folded in
+      constexpr int D = 2;
+      const int64_t mat = static_cast<int64_t>(P.R) * P.K;
+      uint4 vb[D][4];
+      auto load = [&](uint4 (&x)[4]) {
+        if (pi >= total) return;
+        const uint4* p = reinterpret_cast<const uint4*>(P.wq + wslot[pe] * mat +
+                                                        static_cast<int64_t>(wrow(pblk)) * P.K + pkb * kKB);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = __ldg(p + j);
+        advance();
+      };
+#pragma unroll
+      for (int d0 = 0; d0 < D; ++d0) load(vb[d0]);
+      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
+#pragma unroll
+        for (int d0 = 0; d0 < D; ++d0) {
+          const uint32_t L = L0 + d0;
+          if (L < Ltot && ok) {
+            const int s = L % kTS;
+            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+              ok = false;
+            } else {
+              tm_fence_after();
+              uint32_t o[32];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t ww[4] = {vb[d0][j].x, vb[d0][j].y, vb[d0][j].z, vb[d0][j].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  o[8 * j + 2 * h] = e4m3x2_to_bf16x2(ww[h] & 0xffffu);
+                  o[8 * j + 2 * h + 1] = e4m3x2_to_bf16x2(ww[h] >> 16);
+                }
+              }
+              load(vb[d0]);
+              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+              tm_st_wait();
+              tm_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&full_a[s]);
+            }
+          }
+        }
       }
     }
     if (!ok) abort_all();
   } else {
     // ================= epilogue =================
+    // bf16 outputs go through a shared staging tile [token][128 outputs] so
+    // that the accumulator is released as soon as it is read (FC1) and the
+    // global stores are whole 256-byte row pieces (16 bytes per lane)
     const int q = warp & 3;
+    const int et = tid - 10 * 32;  // 0..127
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
+    uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kTab);
+    const int nl = 32 * q + lane;  // output within the 128-row block
+    auto store_stage = [&](int p0, int nvalid, int nbase) {
+      named_bar_sync(1, 128);  // staging complete
+      for (int idx = et; idx < nvalid * 16; idx += 128) {
+        const int j = idx >> 4, seg = idx & 15;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + j * 128 + seg * 8);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + static_cast<size_t>(p0 + j) * P.N + nbase + seg * 8) = v;
+      }
+      named_bar_sync(1, 128);  // staging free again
+    };
     int t = 0;
     for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
       int e, blk, mt;
@@ -482,36 +500,58 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       tm_fence_after();
       const int p0 = P.offsets[e] + mt * NT;
       const int nvalid = min(NT, P.offsets[e + 1] - p0);
-      const int n0 = fc1 ? blk * 128 + 32 * q + lane : blk * 256 + 32 * q + lane;
+      const bool bf16_out = P.out_fmt != MOE_FMT_F32;
+      if (bf16_out) {
+        const int nb0 = fc1 ? blk * 128 : blk * 256;
+        for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
 #pragma unroll 1
-      for (int c = 0; c < NT; c += 32) {
-        uint32_t r0[32], r1[32];
-        tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
-        tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
-        tm_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (c + j < nvalid) {
-            const size_t prow = static_cast<size_t>(p0 + c + j) * P.N;
+          for (int c = 0; c < NT; c += 32) {
+            uint32_t r0[32], r1[32];
             if (fc1) {
-              const float h = silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
-              if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[prow + n0] = h;
-              else static_cast<uint16_t*>(P.out)[prow + n0] = f32_to_bf16_rne(h);
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
             } else {
-              if (P.out_fmt == MOE_FMT_F32) {
-                static_cast<float*>(P.out)[prow + n0] = __uint_as_float(r0[j]);
-                static_cast<float*>(P.out)[prow + n0 + 128] = __uint_as_float(r1[j]);
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
+            }
+            tm_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float v = fc1 ? silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
+              stg[(c + j) * 128 + nl] = f32_to_bf16_rne(v);
+            }
+          }
+          if (fc1 || half == 1) {  // the accumulator has been read
+            tm_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+          }
+          store_stage(p0, nvalid, nb0 + half * 128);
+        }
+      } else {
+        const int n0 = fc1 ? blk * 128 + nl : blk * 256 + nl;
+#pragma unroll 1
+        for (int c = 0; c < NT; c += 32) {
+          uint32_t r0[32], r1[32];
+          tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
+          tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
+          tm_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c + j < nvalid) {
+              float* o = static_cast<float*>(P.out) + static_cast<size_t>(p0 + c + j) * P.N;
+              if (fc1) {
+                o[n0] = silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
               } else {
-                static_cast<uint16_t*>(P.out)[prow + n0] = f32_to_bf16_rne(__uint_as_float(r0[j]));
-                static_cast<uint16_t*>(P.out)[prow + n0 + 128] = f32_to_bf16_rne(__uint_as_float(r1[j]));
+                o[n0] = __uint_as_float(r0[j]);
+                o[n0 + 128] = __uint_as_float(r1[j]);
               }
             }
           }
         }
+        tm_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
       }
-      tm_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
     }
   }
 
