@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_WS_SMALL, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3, 4
 DEVERR_BAD_ID, DEVERR_NAN_LOGIT, DEVERR_NAN_SCALE, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 1, 2, 4, 8, 16
-FMT_NONE, FMT_BF16, FMT_F32, FMT_MXFP8 = 0, 1, 2, 3
+FMT_NONE, FMT_BF16, FMT_F32, FMT_MXFP8, FMT_MXFP8_BF16 = 0, 1, 2, 3, 4
 STAGE_FC1_SWIGLU, STAGE_FC2 = 1, 2
 MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
 

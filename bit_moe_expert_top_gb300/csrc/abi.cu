@@ -104,7 +104,8 @@ int moe_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32
     return fail(MOE_ERR_ARG, "moe_permute: bad shape");
   if (!offsets || (T > 0 && (!ids || !perm || !inv))) return fail(MOE_ERR_ARG, "moe_permute: NULL pointer");
   if (act_fmt != MOE_FMT_NONE) {
-    if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "moe_permute: act_fmt");
+    if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8 && act_fmt != MOE_FMT_MXFP8_BF16)
+      return fail(MOE_ERR_ARG, "moe_permute: act_fmt");
     if (H <= 0 || H % 128) return fail(MOE_ERR_ARG, "moe_permute: H must be a positive multiple of 128");
     if (T > 0 && (!x || !x_perm || !aligned(x, 16) || !aligned(x_perm, 16)))
       return fail(MOE_ERR_ARG, "moe_permute: x / x_perm NULL or not 16-byte aligned");
@@ -182,8 +183,10 @@ static int check_mm(const char* who, int stage, int mode, const void* act, int a
   if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "%s: act_fmt", who);
   if (act_fmt == MOE_FMT_MXFP8 && !act_scale) return fail(MOE_ERR_ARG, "%s: act_scale is NULL", who);
   if (!act || !offsets || !out || !aligned(act, 16)) return fail(MOE_ERR_ARG, "%s: NULL or misaligned pointer", who);
-  if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32 && out_fmt != MOE_FMT_MXFP8)
+  if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32 && out_fmt != MOE_FMT_MXFP8 && out_fmt != MOE_FMT_MXFP8_BF16)
     return fail(MOE_ERR_ARG, "%s: out_fmt", who);
+  if (out_fmt == MOE_FMT_MXFP8_BF16 && stage != MOE_STAGE_FC1_SWIGLU)
+    return fail(MOE_ERR_ARG, "%s: MXFP8_BF16 output is for FC1", who);
   if (out_fmt == MOE_FMT_MXFP8 && (stage != MOE_STAGE_FC1_SWIGLU || !out_scale))
     return fail(MOE_ERR_ARG, "%s: MXFP8 output is for FC1 with out_scale", who);
   return check_device();

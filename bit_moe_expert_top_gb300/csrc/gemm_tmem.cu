@@ -61,6 +61,7 @@ struct TmParams {
   const int32_t* select_map;
   int select;
   const int32_t* offsets;
+  int ebeg, eend;           // experts processed: [ebeg, eend)
   int E, N, K, R;
   int fc1;
   void* out;
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   // ---- setup
   for (int e = tid; e < P.E; e += kTmThreads) {
     int sl = -1;
-    if (P.offsets[e + 1] > P.offsets[e]) {
+    if (e >= P.ebeg && e < P.eend && P.offsets[e + 1] > P.offsets[e]) {
       if (WF == kFmtW2) {
         sl = e;
         if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
@@ -501,6 +502,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const int p0 = P.offsets[e] + mt * NT;
       const int nvalid = min(NT, P.offsets[e + 1] - p0);
       const bool bf16_out = P.out_fmt != MOE_FMT_F32;
+      const bool mx_out = P.out_fmt == MOE_FMT_MXFP8_BF16;
       if (bf16_out) {
         const int nb0 = fc1 ? blk * 128 : blk * 256;
         for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
@@ -514,10 +516,33 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
             }
             tm_ld_wait();
+            if (mx_out) {
+              // MXFP8 rounding: token j's block of 32 outputs is this warp's 32 lanes
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float v = fc1 ? silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
-              stg[(c + j) * 128 + nl] = f32_to_bf16_rne(v);
+              for (int j = 0; j < 32; j += 2) {
+                const float v0 = silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                const float v1 = silu_f32(__uint_as_float(r0[j + 1])) * __uint_as_float(r1[j + 1]);
+                float m0 = fabsf(v0), m1 = fabsf(v1);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                const int X0 = mx_scale_exp(m0), X1 = mx_scale_exp(m1);
+                const uint16_t qq = f32x2_to_e4m3x2(v0 * exp2i(-X0), v1 * exp2i(-X1));
+                const float2 d = e4m3x2_to_f32x2(qq);
+                uint32_t b2;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(d.y * exp2i(X1)), "f"(d.x * exp2i(X0)));
+                stg[(c + j) * 128 + nl] = static_cast<uint16_t>(b2 & 0xffffu);
+                stg[(c + j + 1) * 128 + nl] = static_cast<uint16_t>(b2 >> 16);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float v =
+                    fc1 ? silu_f32(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
+                stg[(c + j) * 128 + nl] = f32_to_bf16_rne(v);
+              }
             }
           }
           if (fc1 || half == 1) {  // the accumulator has been read
@@ -599,13 +624,14 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const TmParams& P
 }  // namespace
 
 bool tmem_mm_supported(const MMArgs& a) {
-  if (a.act_fmt != MOE_FMT_BF16 || a.act_row != nullptr) return false;
-  if (a.out_fmt != MOE_FMT_BF16 && a.out_fmt != MOE_FMT_F32) return false;
-  if (a.expert_begin != 0 || a.expert_end != a.E || a.E > 1024) return false;
+  if (a.act_fmt != MOE_FMT_BF16 || a.act_row != nullptr || a.E > 1024) return false;
+  if (a.out_fmt != MOE_FMT_BF16 && a.out_fmt != MOE_FMT_F32 &&
+      !(a.out_fmt == MOE_FMT_MXFP8_BF16 && a.stage == MOE_STAGE_FC1_SWIGLU))
+    return false;
   if (a.K % kKB) return false;
   if (a.stage == MOE_STAGE_FC1_SWIGLU ? a.N % 128 : a.N % 256) return false;
-  if (a.wkind == kW2) return a.K % w2l_sw(a.K) == 0;
-  if (a.wkind == kFP8) return a.select == 0;  // the workspace slot map does the selection
+  if (a.wkind == kW2) return a.expert_begin == 0 && a.expert_end == a.E && a.K % w2l_sw(a.K) == 0;
+  if (a.wkind == kFP8) return a.wslot_of != nullptr;  // the slot map selects (slot < 0: skipped)
   return false;
 }
 
@@ -619,6 +645,8 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.select_map = a.select_map;
   P.select = a.select;
   P.offsets = a.offsets;
+  P.ebeg = a.expert_begin;
+  P.eend = a.expert_end;
   P.E = a.E;
   P.N = a.N;
   P.K = a.K;

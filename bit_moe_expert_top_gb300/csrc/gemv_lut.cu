@@ -461,7 +461,8 @@ int lut_workspace_rows(int stage, size_t bytes, int N, int K) {
 }
 
 bool lut_supported(const MMArgs& a) {
-  if (a.wkind != kW2 || a.act_fmt != MOE_FMT_BF16 || a.out_fmt == MOE_FMT_MXFP8) return false;
+  if (a.wkind != kW2 || a.act_fmt != MOE_FMT_BF16) return false;
+  if (a.out_fmt != MOE_FMT_BF16 && a.out_fmt != MOE_FMT_F32) return false;
   if (a.expert_begin != 0 || a.expert_end != a.E || a.E > kMaxE) return false;
   return a.K % kSW == 0 && a.N % 32 == 0;
 }

@@ -237,6 +237,8 @@ __global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t
 
 // MXFP8 quantisation fused into the gather: each lane takes 8 consecutive
 // elements, 4 lanes form one block of 32 (block max by two shuffles).
+// AS_BF16: write each element's MXFP8 value q * 2^X as bf16 instead of q + X.
+template <bool AS_BF16>
 __global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
                                     int H, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
   const int lane = threadIdx.x & 31;
@@ -269,8 +271,20 @@ __global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_
           uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
           packed[i] = lo | (hi << 16);
         }
-        *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
-        if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
+        if (AS_BF16) {
+          const float sc2 = exp2i(X);
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 v = e4m3x2_to_f32x2(static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1))));
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(v.y * sc2), "f"(v.x * sc2));
+          }
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + static_cast<size_t>(p) * H + e0) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
+          if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
+        }
       }
     }
   }
@@ -282,8 +296,10 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, 
   const int blocks = min((A + 7) / 8, device_info().sms * 8);
   if (act_fmt == MOE_FMT_BF16) {
     gather_bf16_kernel<<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint16_t*>(x_perm));
+  } else if (act_fmt == MOE_FMT_MXFP8_BF16) {
+    gather_mxfp8_kernel<true><<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), nullptr);
   } else {
-    gather_mxfp8_kernel<<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), x_perm_scale);
+    gather_mxfp8_kernel<false><<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), x_perm_scale);
   }
   return cudaGetLastError();
 }

@@ -98,17 +98,18 @@ class MoELayer:
 
     # ------------------------------------------------------------ buffers
     def use_gemm(self, T: int) -> bool:
-        """Prefill-sized 2-bit steps run FC1/FC2 on the tensor cores over
-        permuted (gathered) activation rows; decode-sized ones on the GEMV."""
-        if self.fmt != "w2" or self.mode == L.MODE_GEMV:
+        """Prefill-sized 2-bit and FP8-workspace steps run FC1/FC2 on the
+        tensor cores over permuted (gathered) activation rows; decode-sized
+        ones on the CUDA-core kernels."""
+        if self.fmt not in ("w2", "fp8") or self.mode == L.MODE_GEMV:
             return False
         return self.mode == L.MODE_GEMM or T * self.k >= self.gemm_min_rows
 
     def buffers(self, T: int) -> StepBuffers:
         dev, E, H, I, k = self.device, self.E, self.H, self.I, self.k
         A = T * k
-        fp8 = self.fmt == "fp8"
         gather = self.use_gemm(T)
+        fp8 = self.fmt == "fp8" and not gather  # MXFP8 bytes + scales (the tensor path keeps bf16 values)
         return StepBuffers(
             ids=torch.empty((T, k), dtype=torch.int32, device=dev),
             w=torch.empty((T, k), dtype=torch.float32, device=dev),
@@ -120,7 +121,7 @@ class MoELayer:
             y=torch.empty((A, H), dtype=torch.int16, device=dev),
             out=torch.empty((T, H), dtype=torch.float32 if self.out_fmt == L.FMT_F32 else torch.int16, device=dev),
             x_perm=(torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else
-                    torch.empty((A, H), dtype=torch.int16, device=dev) if gather else None),
+                    torch.empty((A, H), dtype=torch.int16, device=dev) if gather or self.fmt == "fp8" else None),
             x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
             ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed") and not gather else None,
@@ -147,9 +148,11 @@ class MoELayer:
         E, H, I, k = self.E, self.H, self.I, self.k
         L.moe_route(logits, k, b.ids, b.w, b.dev_err)
         if self.fmt == "fp8":
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
-                          x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
-            self._fp8_experts(b)
+            tc = self.use_gemm(T)
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x,
+                          act_fmt=L.FMT_MXFP8_BF16 if tc else L.FMT_MXFP8, x_perm=b.x_perm,
+                          x_perm_scale=None if tc else b.x_perm_scale, dev_err=b.dev_err)
+            self._fp8_experts(b, tc)
         elif self.use_gemm(T):
             L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                           dev_err=b.dev_err)
@@ -209,7 +212,11 @@ class MoELayer:
     def _timed(self, label):
         return MoELayer._Timer(getattr(self, "_ev", None), label)
 
-    def _fp8_experts(self, b: StepBuffers):
+    def _fp8_experts(self, b: StepBuffers, tc: bool = False):
+        """Expert batches: MXFP4 -> FP8 workspace conversion on a side stream,
+        ring of `fp8_ring` batches, matmuls of batch i after its conversion.
+        tc: the tensor-core matmuls on bf16 activation rows holding the MXFP8
+        values (FC1 writes h MXFP8-rounded the same way)."""
         E, H, I = self.E, self.H, self.I
         main = torch.cuda.current_stream(self.device)
         conv = self.conv_stream
@@ -233,15 +240,25 @@ class MoELayer:
             e0 = i * self.batch
             e1 = min(E, e0 + self.batch)
             main.wait_event(converted[i])
-            with self._timed("fp8_fc1"):
-                L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h, L.FMT_MXFP8,
-                               fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot, act_scale=b.x_perm_scale,
-                               expert_begin=e0, expert_end=e1, out_scale=b.h_scale, mode=self.mode,
-                               dev_err=b.dev_err)
-            with self._timed("fp8_fc2"):
-                L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
-                               fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot, act_scale=b.h_scale,
-                               expert_begin=e0, expert_end=e1, mode=self.mode, dev_err=b.dev_err)
+            if tc:
+                with self._timed("fp8_fc1_gemm"):
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, b.offsets, E, I, H, b.h,
+                                   L.FMT_MXFP8_BF16, fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot,
+                                   expert_begin=e0, expert_end=e1, mode=L.MODE_GEMM, dev_err=b.dev_err)
+                with self._timed("fp8_fc2_gemm"):
+                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                                   fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot,
+                                   expert_begin=e0, expert_end=e1, mode=L.MODE_GEMM, dev_err=b.dev_err)
+            else:
+                with self._timed("fp8_fc1"):
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h,
+                                   L.FMT_MXFP8, fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot,
+                                   act_scale=b.x_perm_scale, expert_begin=e0, expert_end=e1, out_scale=b.h_scale,
+                                   mode=self.mode, dev_err=b.dev_err)
+                with self._timed("fp8_fc2"):
+                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                                   fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot, act_scale=b.h_scale,
+                                   expert_begin=e0, expert_end=e1, mode=self.mode, dev_err=b.dev_err)
             consumed[i].record(main)
             if i + self.ring < nb:
                 convert(i + self.ring)

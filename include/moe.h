@@ -91,6 +91,10 @@ extern "C" {
 #define MOE_FMT_BF16 1   /* uint16 bf16 bit patterns, [rows][cols]                       */
 #define MOE_FMT_F32 2    /* float, [rows][cols]                                          */
 #define MOE_FMT_MXFP8 3  /* E4M3 bytes [rows][cols] + E8M0 bytes [rows][cols/32] (OCP MX)  */
+#define MOE_FMT_MXFP8_BF16 4  /* MXFP8-quantised values (OCP MX rounding, as MOE_FMT_MXFP8)
+                                 stored as bf16 [rows][cols]: each element is q * 2^X exactly
+                                 (for |values| >= 2^-133).  The tensor-core path's form of
+                                 MXFP8 activations: its matmul reads bf16. */
 
 /* expert matmul stage */
 #define MOE_STAGE_FC1_SWIGLU 1  /* h[p][n] = silu(g)*u, g/u = gate/up rows of W1, n < I */
@@ -135,6 +139,7 @@ MOE_API int moe_route(const float* logits, int T, int E, int k, int32_t* ids, fl
  *   inv      int32 [A]      out: inv[perm[p]] = p
  *   x        bf16 [T][H]    optional activations (NULL when act_fmt = NONE)
  *   act_fmt  MOE_FMT_NONE: no gather; MOE_FMT_BF16: x_perm[p] = x[perm[p]/k]
+ *            (MOE_FMT_MXFP8_BF16: the same rows MXFP8-rounded, stored as bf16);
  *            (bf16 [A][H]); MOE_FMT_MXFP8: x_perm[p] = MXFP8(x[perm[p]/k]),
  *            E4M3 [A][H] + E8M0 x_perm_scale [A][H/32] (OCP MX: per block of 32,
  *            scale 2^(floor(log2 amax) - 8), elements RNE + saturate).
@@ -203,7 +208,9 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  *               out[p][n] = silu(g_n) * u_n, n < N (N = I); weights have 2N rows
  *   FC2:        out[p][n] = W2_e[n] . a_p, n < N (N = H); weights have N rows
  * Formats: act_fmt BF16 or MXFP8 (act_scale = E8M0 [rows][K/32]); out_fmt BF16
- * or F32, and MXFP8 for FC1 (out_scale receives E8M0 [rows][N/32]).  Rounding:
+ * or F32, and MXFP8 for FC1 (out_scale receives E8M0 [rows][N/32]); FC1 on the
+ * tensor-core path (GEMM) also takes out_fmt MXFP8_BF16 (h MXFP8-rounded, as
+ * bf16), the form its FC2 reads.  Rounding:
  * out = RNE of the fp32 result into out_fmt.  Rows of unselected experts are
  * left untouched.
  * Modes: GEMV = CUDA-core kernels (2-bit with a workspace and K a multiple
