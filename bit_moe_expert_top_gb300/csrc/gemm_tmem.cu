@@ -22,6 +22,8 @@
 //               SwiGLU for FC1, rounding, stores (32 lanes = 32 consecutive
 //               outputs of one token row: coalesced)
 //
+// MXFP4 decode (delta-cache experts): a per-lane 256-entry byte -> 2 bf16
+// E2M1 table (same window), scaled by 2^(E8M0-127) as bf16 (exact).
 // 2-bit decode: a per-lane copy of the 256-entry byte -> 4 bf16 codebook
 // table (64 KB at a 64 KB-aligned shared address, lane l's copy in banks
 // 2l, 2l+1) is read with one PRMT-formed address per code byte, then scaled
@@ -52,11 +54,11 @@ constexpr int kTab = 16384;             // barriers and tile tables
 constexpr int kStg = 128 * 128 * 2;     // epilogue staging: [NT tokens][128 outputs] bf16
 constexpr int kPre = kTab + kStg;       // shared bytes before the LUT window
 
-enum { kFmtW2 = 0, kFmtE4M3 = 1 };
+enum { kFmtW2 = 0, kFmtE4M3 = 1, kFmtMX4 = 2 };
 
 struct TmParams {
-  const uint8_t* wq;        // W2: w2l codes; E4M3: workspace bytes [slots][R][K]
-  const uint16_t* wscale;   // W2: w2l bf16 scales
+  const uint8_t* wq;        // W2: w2l codes; E4M3: workspace bytes [slots][R][K]; MX4: E2M1 [slots][R][K/2]
+  const uint16_t* wscale;   // W2: w2l bf16 scales; MX4: E8M0 bytes [slots][R][K/32]
   const int32_t* wslot_of;  // E4M3: expert -> workspace slot (< 0: skipped)
   const int32_t* select_map;
   int select;
@@ -184,12 +186,14 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                                                                 const TmParams P) {
   constexpr int kBTile = NT * kKB * 2;  // token tile bytes per stage
   constexpr uint32_t kColA = 2 * NT;   // first A column (after D0, D1)
+  constexpr uint32_t kCols = (2 * NT + kTS * 64 <= 256) ? 256 : 512;  // TMEM columns allocated
+  constexpr bool kLut = WF == kFmtW2 || WF == kFmtMX4;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
   // [barriers, tile table][LUT window (W2), 64 KB aligned][token tiles, 1024 aligned]
   const uint32_t win = (base + kPre + 65535u) & ~65535u;
   const uint32_t tiles_off =
-      (WF == kFmtW2) ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
+      kLut ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
   uint8_t* tiles = smem + tiles_off;
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
   uint64_t* full_b = full_a + kTS;
@@ -214,10 +218,18 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         sl = e;
         if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
       } else {
-        sl = P.wslot_of ? P.wslot_of[e] : e;
+        sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
       }
     }
     wslot[e] = sl;
+  }
+  if (WF == kFmtMX4) {  // per-lane E2M1 pair LUT: byte b -> bf16x2 (lo nibble first) at win + 256 b + 8 l
+    const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
+    for (int i = tid; i < 256 * 32; i += kTmThreads) {
+      const uint32_t b = static_cast<uint32_t>(i >> 5);
+      const uint32_t lo = mag[b & 7] | ((b & 8u) << 12), hi = mag[(b >> 4) & 7] | ((b & 0x80u) << 8);
+      *reinterpret_cast<uint32_t*>(smem + (win - base) + b * 256u + (i & 31) * 8u) = lo | (hi << 16);
+    }
   }
   if (WF == kFmtW2) {  // per-lane codebook LUT: entry b of lane l at win + 256 b + 8 l
     const uint32_t ent[4] = {0xC080u, 0xBF80u, 0x3F80u, 0x4080u};  // -4, -1, 1, 4 as bf16
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     fence_barrier_init();
   }
   if (warp == 1) {
-    tm_alloc(tmem_base_s, 512);
+    tm_alloc(tmem_base_s, kCols);
     tm_relinquish();
   }
   tm_fence_before();
@@ -416,6 +428,73 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               w2_decode_word(wb[d0][2], lanebase, s_hi, o + 16);
               w2_decode_word(wb[d0][3], lanebase, s_hi, o + 24);
               load(wb[d0], sb[d0]);  // stage L + D
+              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+              tm_st_wait();
+              tm_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&full_a[s]);
+            }
+          }
+        }
+      }
+    } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2], E8M0 [slot][R][K/32]
+      constexpr int D = 3;
+      const int64_t mat_q = static_cast<int64_t>(P.R) * (P.K / 2);
+      const int64_t mat_s = static_cast<int64_t>(P.R) * (P.K / 32);
+      const uint8_t* e8 = reinterpret_cast<const uint8_t*>(P.wscale);
+      uint4 qb[D][2];
+      uint32_t sb[D];
+      auto load = [&](uint4 (&x)[2], uint32_t& sc) {
+        if (pi >= total) return;
+        const int r = wrow(pblk);
+        const int64_t slot = wslot[pe];
+        const uint4* pq = reinterpret_cast<const uint4*>(P.wq + slot * mat_q + static_cast<int64_t>(r) * (P.K / 2) + pkb * 32);
+        x[0] = __ldg(pq);
+        x[1] = __ldg(pq + 1);
+        sc = __ldg(reinterpret_cast<const uint16_t*>(e8 + slot * mat_s + static_cast<int64_t>(r) * (P.K / 32) + pkb * 2));
+        advance();
+      };
+      // 2^(x-127) as bf16x2 (x = 0: the subnormal 2^-127; x = 255: NaN, flagged)
+      auto scale2 = [&](uint32_t x) -> uint32_t {
+        const uint32_t b = x == 0 ? 0x0040u : (x == 255 ? 0x7FC0u : (x << 7));
+        return b | (b << 16);
+      };
+#pragma unroll
+      for (int d0 = 0; d0 < D; ++d0) load(qb[d0], sb[d0]);
+      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
+#pragma unroll
+        for (int d0 = 0; d0 < D; ++d0) {
+          const uint32_t L = L0 + d0;
+          if (L < Ltot && ok) {
+            const int s = L % kTS;
+            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+              ok = false;
+            } else {
+              tm_fence_after();
+              const uint32_t sc = sb[d0];
+              if ((sc & 0xffu) == 255u || (sc >> 8) == 255u) set_err(P.dev_err, MOE_DEVERR_NAN_SCALE);
+              const uint32_t s0 = scale2(sc & 0xffu), s1 = scale2(sc >> 8);
+              uint32_t o[32];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t ww[4] = {qb[d0][h].x, qb[d0][h].y, qb[d0][h].z, qb[d0][h].w};
+                const uint32_t sh = h ? s1 : s0;  // bytes 0..15: group 0, 16..31: group 1
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                  uint32_t a[4];
+                  asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(a[0]) : "r"(ww[wi]), "r"(lanebase));
+                  asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(a[1]) : "r"(ww[wi]), "r"(lanebase));
+                  asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(a[2]) : "r"(ww[wi]), "r"(lanebase));
+                  asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(a[3]) : "r"(ww[wi]), "r"(lanebase));
+#pragma unroll
+                  for (int bb = 0; bb < 4; ++bb) {
+                    uint32_t ent;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ent) : "r"(a[bb]));
+                    o[16 * h + 4 * wi + bb] = bf16x2_mul(ent, sh);
+                  }
+                }
+              }
+              load(qb[d0], sb[d0]);
               tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
               tm_st_wait();
               tm_fence_before();
@@ -585,7 +664,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   __syncthreads();
   if (warp == 1) {
     tm_fence_after();
-    tm_dealloc(tmem, 512);
+    tm_dealloc(tmem, kCols);
   }
 }
 
@@ -608,7 +687,8 @@ EncodeFn encode_fn() {
 
 template <int WF, int NT>
 cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const TmParams& P, cudaStream_t s) {
-  const size_t smem = (WF == kFmtW2 ? static_cast<size_t>(kPre) + 65536 + 65536 : static_cast<size_t>(kPre)) +
+  const bool lut = WF == kFmtW2 || WF == kFmtMX4;
+  const size_t smem = (lut ? static_cast<size_t>(kPre) + 65536 + 65536 : static_cast<size_t>(kPre)) +
                       static_cast<size_t>(kTS) * NT * kKB * 2 + 1024;
   static bool attr_done = false;
   if (!attr_done) {
@@ -632,6 +712,7 @@ bool tmem_mm_supported(const MMArgs& a) {
   if (a.stage == MOE_STAGE_FC1_SWIGLU ? a.N % 128 : a.N % 256) return false;
   if (a.wkind == kW2) return a.expert_begin == 0 && a.expert_end == a.E && a.K % w2l_sw(a.K) == 0;
   if (a.wkind == kFP8) return a.wslot_of != nullptr;  // the slot map selects (slot < 0: skipped)
+  if (a.wkind == kMXFP4) return a.select == 0 || a.select == 2;  // cache slot map (NULL: slot = e)
   return false;
 }
 
@@ -655,19 +736,22 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
-  constexpr int NT = 128;
+  // token tile: 128 rows for prefill-sized groups, 32 for decode-sized ones
+  const int NT = rows_total <= 48 * a.E ? 32 : 128;
   // tokens: [rows_total][K] bf16, box 64 x NT with the 128-byte swizzle
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
-  const cuuint32_t box[2] = {kKB, NT};
+  const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(NT)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.act), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  if (a.wkind == kW2) return launch_tm<kFmtW2, NT>(a, map, P, s);
-  return launch_tm<kFmtE4M3, NT>(a, map, P, s);
+  if (a.wkind == kW2) return NT == 32 ? launch_tm<kFmtW2, 32>(a, map, P, s) : launch_tm<kFmtW2, 128>(a, map, P, s);
+  if (a.wkind == kMXFP4)
+    return NT == 32 ? launch_tm<kFmtMX4, 32>(a, map, P, s) : launch_tm<kFmtMX4, 128>(a, map, P, s);
+  return NT == 32 ? launch_tm<kFmtE4M3, 32>(a, map, P, s) : launch_tm<kFmtE4M3, 128>(a, map, P, s);
 }
 
 }  // namespace moe

@@ -105,6 +105,13 @@ class MoELayer:
             return False
         return self.mode == L.MODE_GEMM or T * self.k >= self.gemm_min_rows
 
+    def mx_tensor_path(self) -> bool:
+        """Delta-cache (MXFP4) experts of a mixed layer run on the tensor-core
+        kernel over gathered bf16 rows (any group size), unless GEMV mode is
+        forced or the shape is not one it takes."""
+        return (self.fmt == "mixed" and self.mode != L.MODE_GEMV and self.I % 128 == 0 and self.H % 256 == 0
+                and self.H % 64 == 0 and self.I % 64 == 0)
+
     def buffers(self, T: int) -> StepBuffers:
         dev, E, H, I, k = self.device, self.E, self.H, self.I, self.k
         A = T * k
@@ -121,7 +128,8 @@ class MoELayer:
             y=torch.empty((A, H), dtype=torch.int16, device=dev),
             out=torch.empty((T, H), dtype=torch.float32 if self.out_fmt == L.FMT_F32 else torch.int16, device=dev),
             x_perm=(torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else
-                    torch.empty((A, H), dtype=torch.int16, device=dev) if gather or self.fmt == "fp8" else None),
+                    torch.empty((A, H), dtype=torch.int16, device=dev)
+                    if gather or self.fmt == "fp8" or self.mx_tensor_path() else None),
             x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
             ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed") and not gather else None,
@@ -163,12 +171,22 @@ class MoELayer:
                 L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
                             mode=L.MODE_GEMM, dev_err=b.dev_err)
         else:
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+            mx_tc = self.mx_tensor_path()
+            if mx_tc:  # the cache experts' matmuls read gathered rows
+                L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
+                              dev_err=b.dev_err)
+            else:
+                L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
             with self._timed("w2_fc1"):
                 L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
                             L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
                             mode=self.mode, ws=b.ws, dev_err=b.dev_err)
-            if self.fmt == "mixed":
+            if self.fmt == "mixed" and mx_tc:
+                with self._timed("mx_fc1"):
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
+                                   e2m1=self.q1, e8m0=self.e1, expert_slot=self.expert_slot, mode=L.MODE_GEMM,
+                                   dev_err=b.dev_err)
+            elif self.fmt == "mixed":
                 with self._timed("mx_fc1"):
                     L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
                                    e2m1=self.q1, e8m0=self.e1, act_row=b.perm, act_row_div=k,
@@ -179,8 +197,8 @@ class MoELayer:
             if self.fmt == "mixed":
                 with self._timed("mx_fc2"):
                     L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
-                                   e2m1=self.q2, e8m0=self.e2, expert_slot=self.expert_slot, mode=self.mode,
-                                   dev_err=b.dev_err)
+                                   e2m1=self.q2, e8m0=self.e2, expert_slot=self.expert_slot,
+                                   mode=L.MODE_GEMM if mx_tc else self.mode, dev_err=b.dev_err)
         L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
         return b.out
 

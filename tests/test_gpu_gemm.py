@@ -88,3 +88,18 @@ def test_fp8_workspace_gemm_full_parity(E, H, I, k, T):
     MXFP8-rounded (the oracle's fp8 profile)."""
     w = synth.get_workload("prefill_fp8").replace(E=E, H=H, I=I, k=k, T=T)
     _check_full(w, mode=L.MODE_GEMM)
+
+
+@pytest.mark.parametrize("E,H,I,k,T,n_hot", [(24, 512, 256, 4, 48, 6), (40, 1024, 512, 8, 200, 12)])
+def test_mixed_delta_cache_tensor_path_full_parity(E, H, I, k, T, n_hot):
+    """Mixed layer with the MXFP4 cache experts on the tensor-core path
+    (E2M1 LUT decode into TMEM, 32-token tiles) and the 2-bit experts on
+    the table GEMV."""
+    w = synth.get_workload("mixed_decode").replace(E=E, H=H, I=I, k=k, T=T, n_hot=n_hot)
+    _check_full(w, mode=L.MODE_AUTO)
+
+
+def test_gemm_decode_sized_groups_full_parity():
+    """Few tokens per expert: 32-token tiles, most of each tile past the group end."""
+    w = synth.get_workload("tiny").replace(E=64, H=512, I=256, k=2, T=40, logits="uniform")
+    _check_full(w, mode=L.MODE_GEMM)
