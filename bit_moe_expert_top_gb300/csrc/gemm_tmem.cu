@@ -374,15 +374,17 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     // this CTA's tiles are blockIdx.x, +gridDim.x, ...; flat stage index L
     const int ntile = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
     const uint32_t Ltot = static_cast<uint32_t>(ntile) * static_cast<uint32_t>(KB);
-    // prefetch cursor: (tile pi, k-block pkb) of the next stage to load
+    // prefetch cursor: (tile pi, k-block pkb) of the next stage to load; the
+    // formats keep running pointers (no divisions per stage) and re-base them
+    // when the cursor moves to the next tile
     int pi = blockIdx.x, pkb = 0, pe = 0, pblk = 0, pmt = 0;
     if (pi < total) decode_tile(pi, pe, pblk, pmt);
-    auto advance = [&]() {
-      if (++pkb == KB) {
-        pkb = 0;
-        pi += gridDim.x;
-        if (pi < total) decode_tile(pi, pe, pblk, pmt);
-      }
+    auto next_tile = [&]() -> bool {  // true when the cursor moved to a new tile
+      if (++pkb < KB) return false;
+      pkb = 0;
+      pi += gridDim.x;
+      if (pi < total) decode_tile(pi, pe, pblk, pmt);
+      return true;
     };
     bool ok = true;
     if (WF == kFmtW2) {
@@ -392,21 +394,37 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const int64_t mat_sc = static_cast<int64_t>(P.R) * (P.K / 32);
       const uint32_t* codes32 = reinterpret_cast<const uint32_t*>(P.wq);
       uint32_t wb[D][4], sb[D];
+      // running pointers of the cursor's row: words of k-lanes lb..lb+3 and the
+      // scales of groups g, g+1; kbs k-blocks per w2l slice
+      const int kbs = SW / kKB;
+      const int64_t wstep = static_cast<int64_t>(P.R) * NLn - 16 * (kbs - 1);  // to the next slice
+      const int64_t sstep = static_cast<int64_t>(P.R) * Gs - 8 * (kbs - 1);
+      const uint32_t* wp = codes32;
+      const uint16_t* sp = P.wscale;
+      int kin = 0;  // k-block within the slice
+      auto rebase = [&]() {
+        const int r = wrow(pblk);
+        wp = codes32 + pe * mat_words + static_cast<int64_t>(r >> 2) * (4 * NLn) + (r & 3);
+        sp = P.wscale + pe * mat_sc + static_cast<int64_t>(r >> 2) * (4 * Gs) + (r & 3);
+        kin = 0;
+      };
+      if (pi < total) rebase();
       // codes (4 words) and the two group scales of the cursor's stage
       auto load = [&](uint32_t (&w)[4], uint32_t& sc) {
         if (pi >= total) return;
-        const int r = wrow(pblk);
-        const int k0 = pkb * kKB;
-        const int sl = k0 / SW, lb = (k0 % SW) / 16;
-        const uint32_t* wp = codes32 + pe * mat_words + static_cast<int64_t>(sl) * (P.R * NLn) +
-                             static_cast<int64_t>(r / 4) * (4 * NLn) + lb * 4 + (r & 3);
 #pragma unroll
         for (int j = 0; j < 4; ++j) w[j] = __ldg(wp + 4 * j);
-        const int g = (k0 % SW) / 32;
-        const uint16_t* sp = P.wscale + pe * mat_sc + static_cast<int64_t>(sl) * (P.R * Gs) +
-                             static_cast<int64_t>(r / 4) * (4 * Gs) + g * 4 + (r & 3);
         sc = static_cast<uint32_t>(__ldg(sp)) | (static_cast<uint32_t>(__ldg(sp + 4)) << 16);
-        advance();
+        if (next_tile()) {
+          if (pi < total) rebase();
+        } else if (++kin == kbs) {
+          kin = 0;
+          wp += wstep;
+          sp += sstep;
+        } else {
+          wp += 16;
+          sp += 8;
+        }
       };
 #pragma unroll
       for (int d0 = 0; d0 < D; ++d0) load(wb[d0], sb[d0]);
@@ -444,15 +462,27 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const uint8_t* e8 = reinterpret_cast<const uint8_t*>(P.wscale);
       uint4 qb[D][2];
       uint32_t sb[D];
-      auto load = [&](uint4 (&x)[2], uint32_t& sc) {
-        if (pi >= total) return;
+      const uint8_t* qp = P.wq;
+      const uint8_t* ep = e8;
+      auto rebase = [&]() {
         const int r = wrow(pblk);
         const int64_t slot = wslot[pe];
-        const uint4* pq = reinterpret_cast<const uint4*>(P.wq + slot * mat_q + static_cast<int64_t>(r) * (P.K / 2) + pkb * 32);
+        qp = P.wq + slot * mat_q + static_cast<int64_t>(r) * (P.K / 2);
+        ep = e8 + slot * mat_s + static_cast<int64_t>(r) * (P.K / 32);
+      };
+      if (pi < total) rebase();
+      auto load = [&](uint4 (&x)[2], uint32_t& sc) {
+        if (pi >= total) return;
+        const uint4* pq = reinterpret_cast<const uint4*>(qp);
         x[0] = __ldg(pq);
         x[1] = __ldg(pq + 1);
-        sc = __ldg(reinterpret_cast<const uint16_t*>(e8 + slot * mat_s + static_cast<int64_t>(r) * (P.K / 32) + pkb * 2));
-        advance();
+        sc = __ldg(reinterpret_cast<const uint16_t*>(ep));
+        if (next_tile()) {
+          if (pi < total) rebase();
+        } else {
+          qp += 32;
+          ep += 2;
+        }
       };
       // 2^(x-127) as bf16x2 (x = 0: the subnormal 2^-127; x = 255: NaN, flagged)
       auto scale2 = [&](uint32_t x) -> uint32_t {
@@ -508,13 +538,19 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       constexpr int D = 2;
       const int64_t mat = static_cast<int64_t>(P.R) * P.K;
       uint4 vb[D][4];
+      const uint8_t* vp = P.wq;
+      auto rebase = [&]() { vp = P.wq + wslot[pe] * mat + static_cast<int64_t>(wrow(pblk)) * P.K; };
+      if (pi < total) rebase();
       auto load = [&](uint4 (&x)[4]) {
         if (pi >= total) return;
-        const uint4* p = reinterpret_cast<const uint4*>(P.wq + wslot[pe] * mat +
-                                                        static_cast<int64_t>(wrow(pblk)) * P.K + pkb * kKB);
+        const uint4* p = reinterpret_cast<const uint4*>(vp);
 #pragma unroll
         for (int j = 0; j < 4; ++j) x[j] = __ldg(p + j);
-        advance();
+        if (next_tile()) {
+          if (pi < total) rebase();
+        } else {
+          vp += kKB;
+        }
       };
 #pragma unroll
       for (int d0 = 0; d0 < D; ++d0) load(vb[d0]);
