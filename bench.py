@@ -95,12 +95,33 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workloads
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, FC1/FC2
+# mean) of the table GEMV on the decode workload, from the ncu capture
+# summarised in profiles/w2_lut_kernel_decode.md; reported only while the
+# kernel source is the one that was captured (sha256 of csrc/gemv_lut.cu).
+_LUT_TRAFFIC = {"workload": "decode", "bytes": 251.3e6,
+                "src_sha256": "8e4daf084889b0c093d4b020071a2c2a2903ffae3780e50e9fcc943bf1a2fcb3"}
+
+
+def _decode_traffic(w):
+    import hashlib
+    src = os.path.join(ROOT, "bit_moe_expert_top_gb300", "csrc", "gemv_lut.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    if w.name != _LUT_TRAFFIC["workload"] or digest != _LUT_TRAFFIC["src_sha256"]:
+        return None
+    return _LUT_TRAFFIC["bytes"]
+
+
 def flops_per_assignment(w):
     return 6 * w.H * w.I
 
 
-def build_workload(name, layers, batches, device):
-    """Device weights (MoELayer per distinct layer) and token batches."""
+def build_workload(name, layers, batches, device, tokens=None):
+    """Device weights (MoELayer per distinct layer) and token batches
+    (tokens: a smaller token count for profiling captures)."""
     import torch
 
     from bit_moe_expert_top_gb300 import _lib as L
@@ -108,6 +129,8 @@ def build_workload(name, layers, batches, device):
     from bit_moe_expert_top_gb300.layer import MoELayer
 
     w = synth.get_workload(name)
+    if tokens:
+        w = w.replace(T=tokens)
     mls = []
     for l in range(layers):
         if w.weights == "w2":
@@ -147,7 +170,7 @@ def run_gpu(args):
 
     layers = args.layers
     batches = max(layers, 4)
-    w, mls, xs_h, lgs_h = build_workload(args.workload, layers, batches, device)
+    w, mls, xs_h, lgs_h = build_workload(args.workload, layers, batches, device, args.tokens)
     xs = [torch.from_numpy(x.view(np.int16)).to(device) for x in xs_h]
     lgs = [torch.from_numpy(lg).to(device) for lg in lgs_h]
     bufs = [ml.buffers(w.T) for ml in mls]
@@ -223,10 +246,11 @@ def run_gpu(args):
 
     peaks = _peaks()
     decode = w.T * w.k < 4096
+    traffic = _decode_traffic(w) if decode else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": "expert matmuls (moe_w2_mm FC1+FC2)", "peak_src": peaks["src"],
                 "bytes_per_launch": round(graph_bytes / n_mm), "launch_us": round(mm_ms / n_mm * 1e3, 2)}
     else:
@@ -251,7 +275,7 @@ def run_gpu(args):
         "roofline": roof,
         "kernels_us": kernels_us,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step(w),
+        "gpu_launches": args.steps * launches_per_step(mls[0], w.T),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -262,14 +286,18 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def launches_per_step(w):
-    # route, permute, FC1, FC2, combine (+ MXFP4 FC1/FC2 for the delta cache;
-    # + gather and per-batch conversions / matmuls on the FP8 path)
-    if w.weights == "w2":
-        return 5
-    if w.weights == "mixed":
-        return 7
-    nb = (w.E + 15) // 16
+def launches_per_step(ml, T):
+    """Kernel launches of one layer step on the path the layer takes:
+    route + permute (+ the row gather) + combine, and per expert matmul the
+    table GEMV with its summing kernel (2-bit decode) or one tensor-core
+    kernel, plus two workspace conversions per expert batch on the FP8 path."""
+    tc = ml.use_gemm(T)
+    if ml.fmt == "w2":
+        return 6 if tc else 7
+    if ml.fmt == "mixed":
+        mx_tc = ml.mx_tensor_path()
+        return 3 + (1 if mx_tc else 0) + 2 * 2 + 2 * 1
+    nb = (ml.E + ml.batch - 1) // ml.batch
     return 4 + 4 * nb
 
 
@@ -398,6 +426,8 @@ def main():
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8"])
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-sample", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -773,7 +773,9 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
   // token tile: 128 rows for prefill-sized groups, 32 for decode-sized ones
-  const int NT = rows_total <= 48 * a.E ? 32 : 128;
+  // (the decode of each weight block repeats per token tile, so 32-row tiles
+  // only pay off when groups are small)
+  const int NT = rows_total <= 16 * a.E ? 32 : 128;
   // tokens: [rows_total][K] bf16, box 64 x NT with the 128-byte swizzle
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1)};
