@@ -50,9 +50,11 @@ constexpr int kTmWarps = 14;
 constexpr int kTmThreads = kTmWarps * 32;
 constexpr int kKB = 64;    // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kTS = 3;     // pipeline stages
-constexpr int kTab = 16384;             // barriers and tile tables
+constexpr int kTab = 12288;             // barriers and tile tables (E <= 1024)
 constexpr int kStg = 128 * 128 * 2;     // epilogue staging: [NT tokens][128 outputs] bf16
-constexpr int kPre = kTab + kStg;       // shared bytes before the LUT window
+constexpr int kCodeStage = 4096 + 1024; // 2-bit: codes [2 blocks][32 quads][64 B] + scales [2][32][16 B]
+constexpr int kCodes = kTS * kCodeStage;
+constexpr int kPre = kTab + kStg + kCodes;  // shared bytes before the LUT window
 
 enum { kFmtW2 = 0, kFmtE4M3 = 1, kFmtMX4 = 2 };
 
@@ -183,6 +185,8 @@ MOE_D uint32_t e4m3x2_to_bf16x2(uint32_t two) {
 
 template <int WF, int NT>
 __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_constant__ CUtensorMap tmap_b,
+                                                                const __grid_constant__ CUtensorMap tmap_c,
+                                                                const __grid_constant__ CUtensorMap tmap_s,
                                                                 const TmParams P) {
   constexpr int kBTile = NT * kKB * 2;  // token tile bytes per stage
   constexpr uint32_t kColA = 2 * NT;   // first A column (after D0, D1)
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const uint32_t tiles_off =
       kLut ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
   uint8_t* tiles = smem + tiles_off;
+  uint8_t* codes_s = smem + kTab + kStg;  // 2-bit: per-stage code / scale tiles (TMA)
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
   uint64_t* full_b = full_a + kTS;
   uint64_t* empty = full_b + kTS;
@@ -206,6 +211,14 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   int* wslot = tile_start + (P.E + 1);  // [E] weight slot of each expert (-1: skipped)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (tiles_off + static_cast<uint32_t>(kTS * kBTile) > dyn) {  // layout assumption broken: refuse
+      if (tid == 0) set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
+      return;
+    }
+  }
   const bool fc1 = P.fc1 != 0;
   const int NBLK = fc1 ? P.N / 128 : P.N / 256;  // weight-block pairs
   const int KB = P.K / kKB;
@@ -296,8 +309,11 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
   };
 
+  const int SWc = w2l_sw(P.K);        // 2-bit: w2l slice width
+  const int kbs = SWc / kKB;           // k-blocks per slice
+  const int NSL = P.K / SWc;
   if (warp == 0) {
-    // ================= token tiles by TMA =================
+    // ================= token tiles (and 2-bit codes) by TMA =================
     if (lane == 0) {
       uint32_t L = 0;
       for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
@@ -311,8 +327,21 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_b[s], kBTile);
-          tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+          if (WF == kFmtW2) {  // + the stage's codes and scales of both weight blocks
+            mbar_arrive_expect_tx(&full_b[s], kBTile + kCodeStage);
+            tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+            const int sl = kb / kbs, kin = kb - sl * kbs;
+            const int qrow = (e * NSL + sl) * (P.R >> 2);
+#pragma unroll
+            for (int bs = 0; bs < 2; ++bs) {
+              const int q0 = qrow + (fc1 ? (bs ? (P.N >> 2) : 0) + blk * 32 : blk * 64 + bs * 32);
+              tma_load_tile(codes_s + s * kCodeStage + bs * 2048, &tmap_c, kin * 64, q0, &full_b[s]);
+              tma_load_tile(codes_s + s * kCodeStage + 4096 + bs * 512, &tmap_s, kin * 16, q0, &full_b[s]);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full_b[s], kBTile);
+            tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+          }
         }
         if (!ok) {
           abort_all();
@@ -388,72 +417,37 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     };
     bool ok = true;
     if (WF == kFmtW2) {
-      constexpr int D = 3;  // stages of codes in flight per thread
-      const int SW = w2l_sw(P.K), NLn = SW / 16, Gs = SW / 32;
-      const int64_t mat_words = static_cast<int64_t>(P.R) * (P.K / 16);
-      const int64_t mat_sc = static_cast<int64_t>(P.R) * (P.K / 32);
-      const uint32_t* codes32 = reinterpret_cast<const uint32_t*>(P.wq);
-      uint32_t wb[D][4], sb[D];
-      // running pointers of the cursor's row: words of k-lanes lb..lb+3 and the
-      // scales of groups g, g+1; kbs k-blocks per w2l slice
-      const int kbs = SW / kKB;
-      const int64_t wstep = static_cast<int64_t>(P.R) * NLn - 16 * (kbs - 1);  // to the next slice
-      const int64_t sstep = static_cast<int64_t>(P.R) * Gs - 8 * (kbs - 1);
-      const uint32_t* wp = codes32;
-      const uint16_t* sp = P.wscale;
-      int kin = 0;  // k-block within the slice
-      auto rebase = [&]() {
-        const int r = wrow(pblk);
-        wp = codes32 + pe * mat_words + static_cast<int64_t>(r >> 2) * (4 * NLn) + (r & 3);
-        sp = P.wscale + pe * mat_sc + static_cast<int64_t>(r >> 2) * (4 * Gs) + (r & 3);
-        kin = 0;
-      };
-      if (pi < total) rebase();
-      // codes (4 words) and the two group scales of the cursor's stage
-      auto load = [&](uint32_t (&w)[4], uint32_t& sc) {
-        if (pi >= total) return;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = __ldg(wp + 4 * j);
-        sc = static_cast<uint32_t>(__ldg(sp)) | (static_cast<uint32_t>(__ldg(sp + 4)) << 16);
-        if (next_tile()) {
-          if (pi < total) rebase();
-        } else if (++kin == kbs) {
-          kin = 0;
-          wp += wstep;
-          sp += sstep;
-        } else {
-          wp += 16;
-          sp += 8;
+      // codes and scales of this thread's row come from the TMA-filled stage
+      // tiles: quad qd = block bsel's quad m/4, row rr = m % 4
+      const uint32_t cbase = smem_u32(codes_s) + static_cast<uint32_t>(bsel * 2048 + (m >> 2) * 64 + (m & 3) * 4);
+      const uint32_t sbase = smem_u32(codes_s) + static_cast<uint32_t>(4096 + bsel * 512 + (m >> 2) * 16 + (m & 3) * 2);
+      for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
+        const int s = L % kTS;
+        if ((L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) || !mbar_wait(&full_b[s], (L / kTS) & 1)) {
+          ok = false;
+          break;
         }
-      };
-#pragma unroll
-      for (int d0 = 0; d0 < D; ++d0) load(wb[d0], sb[d0]);
-      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
-#pragma unroll
-        for (int d0 = 0; d0 < D; ++d0) {
-          const uint32_t L = L0 + d0;
-          if (L < Ltot && ok) {
-            const int s = L % kTS;
-            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
-              ok = false;
-            } else {
-              tm_fence_after();  // the MMAs that read this A stage are complete
-              uint32_t o[32];
-              const uint32_t sc = sb[d0];
-              const uint32_t s_lo = (sc & 0xffffu) | (sc << 16), s_hi = (sc >> 16) | (sc & 0xffff0000u);
-              w2_decode_word(wb[d0][0], lanebase, s_lo, o);
-              w2_decode_word(wb[d0][1], lanebase, s_lo, o + 8);
-              w2_decode_word(wb[d0][2], lanebase, s_hi, o + 16);
-              w2_decode_word(wb[d0][3], lanebase, s_hi, o + 24);
-              load(wb[d0], sb[d0]);  // stage L + D
-              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
-              tm_st_wait();
-              tm_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&full_a[s]);
-            }
-          }
-        }
+        tm_fence_after();  // the MMAs that read this A stage are complete
+        uint32_t w[4], sc0, sc1;
+        const uint32_t co = cbase + static_cast<uint32_t>(s * kCodeStage);
+        const uint32_t so = sbase + static_cast<uint32_t>(s * kCodeStage);
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(co));
+        asm volatile("ld.shared.u32 %0, [%1+16];" : "=r"(w[1]) : "r"(co));
+        asm volatile("ld.shared.u32 %0, [%1+32];" : "=r"(w[2]) : "r"(co));
+        asm volatile("ld.shared.u32 %0, [%1+48];" : "=r"(w[3]) : "r"(co));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so));
+        asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so));
+        uint32_t o[32];
+        const uint32_t s_lo = sc0 | (sc0 << 16), s_hi = sc1 | (sc1 << 16);
+        w2_decode_word(w[0], lanebase, s_lo, o);
+        w2_decode_word(w[1], lanebase, s_lo, o + 8);
+        w2_decode_word(w[2], lanebase, s_hi, o + 16);
+        w2_decode_word(w[3], lanebase, s_hi, o + 24);
+        tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+        tm_st_wait();
+        tm_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[s]);
       }
     } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2], E8M0 [slot][R][K/32]
       constexpr int D = 3;
@@ -722,10 +716,15 @@ EncodeFn encode_fn() {
 }
 
 template <int WF, int NT>
-cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const TmParams& P, cudaStream_t s) {
+cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap& cmap, const CUtensorMap& smap,
+                      const TmParams& P, cudaStream_t s) {
+  (void)a;
   const bool lut = WF == kFmtW2 || WF == kFmtMX4;
-  const size_t smem = (lut ? static_cast<size_t>(kPre) + 65536 + 65536 : static_cast<size_t>(kPre)) +
-                      static_cast<size_t>(kTS) * NT * kKB * 2 + 1024;
+  // the shared window starts 1 KB in (the reserved block): the LUT window is
+  // the first 64 KB-aligned address past kPre; the kernel checks the layout
+  const size_t pre = lut ? ((1024 + static_cast<size_t>(kPre) + 65535) & ~size_t(65535)) - 1024 + 65536
+                         : static_cast<size_t>(kPre) + 1024;
+  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + 1024;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -733,7 +732,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const TmParams& P
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  tmem_mm_kernel<WF, NT><<<device_info().sms, kTmThreads, smem, s>>>(map, P);
+  tmem_mm_kernel<WF, NT><<<device_info().sms, kTmThreads, smem, s>>>(map, cmap, smap, P);
   return cudaGetLastError();
 }
 
@@ -786,10 +785,28 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  if (a.wkind == kW2) return NT == 32 ? launch_tm<kFmtW2, 32>(a, map, P, s) : launch_tm<kFmtW2, 128>(a, map, P, s);
+  CUtensorMap cmap = map, smap = map;  // unused by the formats without TMA-fed codes
+  if (a.wkind == kW2) {
+    // w2l codes / scales as 2-D byte arrays: one row per (expert, slice, row quad)
+    const int SW = w2l_sw(a.K);
+    const cuuint64_t qrows = static_cast<cuuint64_t>(a.E) * (a.K / SW) * (P.R / 4);
+    const cuuint64_t cd[2] = {static_cast<cuuint64_t>(SW), qrows}, cs[1] = {static_cast<cuuint64_t>(SW)};
+    const cuuint64_t sd[2] = {static_cast<cuuint64_t>(SW / 4), qrows}, ss[1] = {static_cast<cuuint64_t>(SW / 4)};
+    const cuuint32_t cbox[2] = {64, 32}, sbox[2] = {16, 32};
+    if (enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), cd, cs, cbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.wscale), sd, ss, sbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (a.wkind == kW2)
+    return NT == 32 ? launch_tm<kFmtW2, 32>(a, map, cmap, smap, P, s) : launch_tm<kFmtW2, 128>(a, map, cmap, smap, P, s);
   if (a.wkind == kMXFP4)
-    return NT == 32 ? launch_tm<kFmtMX4, 32>(a, map, P, s) : launch_tm<kFmtMX4, 128>(a, map, P, s);
-  return NT == 32 ? launch_tm<kFmtE4M3, 32>(a, map, P, s) : launch_tm<kFmtE4M3, 128>(a, map, P, s);
+    return NT == 32 ? launch_tm<kFmtMX4, 32>(a, map, cmap, smap, P, s) : launch_tm<kFmtMX4, 128>(a, map, cmap, smap, P, s);
+  return NT == 32 ? launch_tm<kFmtE4M3, 32>(a, map, cmap, smap, P, s)
+                  : launch_tm<kFmtE4M3, 128>(a, map, cmap, smap, P, s);
 }
 
 }  // namespace moe
