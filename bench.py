@@ -191,13 +191,21 @@ def run_gpu(args):
             raise RuntimeError("device error flags set during warm-up")
 
     # ---- the timed steps run from a CUDA graph: S consecutive steps (layer
-    # i mod L, batch i mod B) are captured once, with an event pair around the
-    # expert matmuls of every step; the timed region replays it K/S times.
+    # i mod L, batch i mod B) captured once; the timed region replays it K/S
+    # times.  A second graph of the same steps carries an event pair around
+    # every expert matmul (the roofline's per-kernel durations); it is
+    # replayed after the timed region, because event nodes between kernels
+    # would serialise the programmatic launches of the timed graph.
     S = max(d for d in range(1, min(args.steps, 64) + 1) if args.steps % d == 0)
-    graph_ev = []
     g = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(g):
+        for i in range(S):
+            step(i)
+    graph_ev = []
+    g_ev = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_ev):
         for i in range(S):
             step(i, graph_ev)
     torch.cuda.synchronize()
@@ -222,9 +230,12 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    for _ in range(2):  # the event graph: the last replay's durations are read below
+        g_ev.replay()
+    torch.cuda.synchronize()
 
     # per-launch durations of the expert matmul kernels (the dominant ones),
-    # from the event pairs of the last replay
+    # from the event pairs of the event graph's last replay
     mm_ms = sum(a.elapsed_time(b) for _, a, b in graph_ev)
     n_mm = len(graph_ev)
     per_label = {}

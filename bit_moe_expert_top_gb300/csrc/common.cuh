@@ -78,6 +78,13 @@ MOE_D void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op when the kernel was not
+// launched as a dependent), then let the next grid be scheduled.  Kernels call
+// pdl_wait() before their first global-memory access.
+MOE_D void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_D void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 MOE_D void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -223,19 +223,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const int NBLK = fc1 ? P.N / 128 : P.N / 256;  // weight-block pairs
   const int KB = P.K / kKB;
 
-  // ---- setup
-  for (int e = tid; e < P.E; e += kTmThreads) {
-    int sl = -1;
-    if (e >= P.ebeg && e < P.eend && P.offsets[e + 1] > P.offsets[e]) {
-      if (WF == kFmtW2) {
-        sl = e;
-        if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
-      } else {
-        sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
-      }
-    }
-    wslot[e] = sl;
-  }
+  // ---- setup (shared memory only until pdl_wait: it overlaps the previous kernel)
   if (WF == kFmtMX4) {  // per-lane E2M1 pair LUT: byte b -> bf16x2 (lo nibble first) at win + 256 b + 8 l
     const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
     for (int i = tid; i < 256 * 32; i += kTmThreads) {
@@ -252,6 +240,20 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           make_uint2(ent[b & 3] | (ent[(b >> 2) & 3] << 16), ent[(b >> 4) & 3] | (ent[b >> 6] << 16));
       *reinterpret_cast<uint2*>(smem + (win - base) + b * 256u + (i & 31) * 8u) = v;
     }
+  }
+  pdl_wait();
+  pdl_trigger();
+  for (int e = tid; e < P.E; e += kTmThreads) {
+    int sl = -1;
+    if (e >= P.ebeg && e < P.eend && P.offsets[e + 1] > P.offsets[e]) {
+      if (WF == kFmtW2) {
+        sl = e;
+        if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
+      } else {
+        sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
+      }
+    }
+    wslot[e] = sl;
   }
   __syncthreads();
   if (warp == 0) {
@@ -732,8 +734,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  tmem_mm_kernel<WF, NT><<<device_info().sms, kTmThreads, smem, s>>>(map, cmap, smap, P);
-  return cudaGetLastError();
+  return launch_pdl(tmem_mm_kernel<WF, NT>, dim3(device_info().sms), dim3(kTmThreads), smem, s, map, cmap, smap, P);
 }
 
 }  // namespace

@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   extern __shared__ __align__(1024) uint8_t smem[];
   int* pref = reinterpret_cast<int*>(smem);  // [E+1] selected permuted rows before expert e
 
+  pdl_wait();  // offsets, activations and the scratch belong to earlier kernels
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
   const uint32_t table_win = (base + kPrologue + 65535u) & ~65535u;
@@ -193,9 +195,6 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     if (tid == kLutThreads - 1) pref[P.E] = excl + local;  // the total (also for E = 1024)
   }
   __syncthreads();
-  // the finishing kernel may be scheduled now; it waits for this grid's
-  // completion (and memory flush) before it reads the scratch
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- the permuted row of every selected row for the finishing kernel
   // (-1 where the row is skipped: beyond the scratch, or a bad token index)
@@ -398,7 +397,8 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
 // ... and outputs [256 j, 256 j + 256); one thread per output.
 __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
   // everything read here is written by the preceding (primary) grid
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
+  pdl_trigger();
   const int NSL = P.NSL, NB = P.NB;
   const int n = blockIdx.y * 256 + threadIdx.x;
   if (n >= P.N) return;
@@ -496,23 +496,12 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int sms = device_info().sms;
-  w2_lut_kernel<<<sms, kLutThreads, kLutSmem, s>>>(P);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(w2_lut_kernel, dim3(device_info().sms), dim3(kLutThreads), kLutSmem, s, P);
   if (e != cudaSuccess) return e;
   // the finishing kernel as a programmatic dependent: its launch overlaps the
-  // main kernel's tail; griddepcontrol.wait orders its scratch reads
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.ws_rows < 4096 ? a.ws_rows : 4096), static_cast<unsigned>((a.N + 255) / 256));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w2_lut_finish_kernel, P);
+  // main kernel's tail; its pdl_wait orders the scratch reads
+  const dim3 fgrid(static_cast<unsigned>(a.ws_rows < 4096 ? a.ws_rows : 4096), static_cast<unsigned>((a.N + 255) / 256));
+  return launch_pdl(w2_lut_finish_kernel, fgrid, dim3(256), 0, s, P);
 }
 
 }  // namespace moe

@@ -40,6 +40,8 @@ template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                     int32_t* __restrict__ ids, float* __restrict__ w,
                                                     uint32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -97,11 +99,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
                          cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const dim3 grid((T + 7) / 8), block(256);
-  if (E <= 128) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
-  else if (E <= 256) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
-  else if (E <= 512) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
-  else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, dev_err);
-  return cudaGetLastError();
+  if (E <= 128) return launch_pdl(route_kernel<4>, grid, block, 0, s, logits, T, E, k, ids, w, dev_err);
+  if (E <= 256) return launch_pdl(route_kernel<8>, grid, block, 0, s, logits, T, E, k, ids, w, dev_err);
+  if (E <= 512) return launch_pdl(route_kernel<16>, grid, block, 0, s, logits, T, E, k, ids, w, dev_err);
+  return launch_pdl(route_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w, dev_err);
 }
 
 // ------------------------------------------------------------------ grouping
@@ -120,6 +121,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   int* hist = s_perm;                    // [32][E]
   int* tot = s_perm + kPermWarps * E;    // [E]
   __shared__ int warp_sums[32];
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
   int chunk = (A + kPermWarps - 1) / kPermWarps;
@@ -219,13 +222,14 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  permute_kernel<<<1, 1024, smem, s>>>(ids, A, E, offsets, perm, inv, dev_err);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(1), dim3(1024), smem, s, ids, A, E, offsets, perm, inv, dev_err);
 }
 
 // ------------------------------------------------------------------ gather
 __global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
                                    int H, uint16_t* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int vec = H / 8;  // uint4 per row
   for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
@@ -241,6 +245,8 @@ __global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t
 template <bool AS_BF16>
 __global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
                                     int H, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
     const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
@@ -294,14 +300,14 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, 
                           uint8_t* x_perm_scale, cudaStream_t s) {
   if (A == 0) return cudaSuccess;
   const int blocks = min((A + 7) / 8, device_info().sms * 8);
-  if (act_fmt == MOE_FMT_BF16) {
-    gather_bf16_kernel<<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint16_t*>(x_perm));
-  } else if (act_fmt == MOE_FMT_MXFP8_BF16) {
-    gather_mxfp8_kernel<true><<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), nullptr);
-  } else {
-    gather_mxfp8_kernel<false><<<blocks, 256, 0, s>>>(x, perm, A, k, H, static_cast<uint8_t*>(x_perm), x_perm_scale);
-  }
-  return cudaGetLastError();
+  if (act_fmt == MOE_FMT_BF16)
+    return launch_pdl(gather_bf16_kernel, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+                      static_cast<uint16_t*>(x_perm));
+  if (act_fmt == MOE_FMT_MXFP8_BF16)
+    return launch_pdl(gather_mxfp8_kernel<true>, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+                      static_cast<uint8_t*>(x_perm), static_cast<uint8_t*>(nullptr));
+  return launch_pdl(gather_mxfp8_kernel<false>, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+                    static_cast<uint8_t*>(x_perm), x_perm_scale);
 }
 
 __global__ void unpermute_kernel(const uint8_t* __restrict__ src, const int32_t* __restrict__ inv, int A,
@@ -352,6 +358,8 @@ template <bool kYF32, bool kOutF32>
 __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
                                                       const int32_t* __restrict__ inv, int T, int k, int H,
                                                       void* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int c0 = blockIdx.x * 2048 + threadIdx.x * 8;
   if (t >= T || c0 >= H) return;
@@ -361,6 +369,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
   const int32_t* iv = inv + static_cast<size_t>(t) * k;
   const float* wt = w + static_cast<size_t>(t) * k;
   int j = 0;
+  for (; j + 8 <= k; j += 8) {  // all eight slots' rows in flight at once, summed in slot order
+    int p[8];
+    float wj[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      p[u] = iv[j + u];
+      wj[u] = wt[j + u];
+    }
+    float v[8][8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (p[u] >= 0) load8<kYF32>(y, static_cast<size_t>(p[u]) * H + c0, v[u]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (p[u] < 0) continue;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
+    }
+  }
   for (; j + 4 <= k; j += 4) {
     float v[4][8];
     int p[4];
@@ -406,11 +433,10 @@ cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32
   if (T == 0) return cudaSuccess;
   const dim3 grid((H + 2047) / 2048, T);
   const bool yf = y_fmt == MOE_FMT_F32, of = out_fmt == MOE_FMT_F32;
-  if (yf && of) combine_kernel<true, true><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else if (yf) combine_kernel<true, false><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else if (of) combine_kernel<false, true><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  else combine_kernel<false, false><<<grid, 256, 0, s>>>(y, w, inv, T, k, H, out);
-  return cudaGetLastError();
+  if (yf && of) return launch_pdl(combine_kernel<true, true>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
+  if (yf) return launch_pdl(combine_kernel<true, false>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
+  if (of) return launch_pdl(combine_kernel<false, true>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
+  return launch_pdl(combine_kernel<false, false>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
 }
 
 }  // namespace moe
