@@ -46,15 +46,16 @@ namespace moe {
 
 namespace {
 
-constexpr int kTmWarps = 14;
+constexpr int kTmWarps = 15;  // TMA, MMA, 8 decode, 4 epilogue, code TMA
 constexpr int kTmThreads = kTmWarps * 32;
 constexpr int kKB = 64;    // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kTS = 3;     // pipeline stages
+constexpr int kTS = 4;     // pipeline stages (TMEM: 2 x 128 accumulator + 4 x 64 A columns = 512)
 constexpr int kTab = 12288;             // barriers and tile tables (E <= 1024)
 constexpr int kStg = 128 * 128 * 2;     // epilogue staging: [NT tokens][128 outputs] bf16
 constexpr int kCodeStage = 4096 + 1024; // 2-bit: codes [2 blocks][32 quads][64 B] + scales [2][32][16 B]
-constexpr int kCodes = kTS * kCodeStage;
-constexpr int kPre = kTab + kStg + kCodes;  // shared bytes before the LUT window
+constexpr int kCS = 6;                  // 2-bit: code ring stages (runs ahead of the TMEM stages)
+constexpr int kCodes = kCS * kCodeStage; // after the token tiles
+constexpr int kPre = kTab + kStg;           // shared bytes before the LUT window
 
 enum { kFmtW2 = 0, kFmtE4M3 = 1, kFmtMX4 = 2 };
 
@@ -199,13 +200,15 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const uint32_t tiles_off =
       kLut ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
   uint8_t* tiles = smem + tiles_off;
-  uint8_t* codes_s = smem + kTab + kStg;  // 2-bit: per-stage code / scale tiles (TMA)
+  uint8_t* codes_s = tiles + kTS * kBTile;  // 2-bit: per-stage code / scale tiles (TMA)
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
   uint64_t* full_b = full_a + kTS;
   uint64_t* empty = full_b + kTS;
   uint64_t* acc_full = empty + kTS;
   uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* code_full = acc_empty + 1;    // [kCS] 2-bit code ring
+  uint64_t* code_empty = code_full + kCS; // [kCS]
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(code_empty + kCS);
   int* flags = reinterpret_cast<int*>(tmem_base_s + 2);
   int* tile_start = flags + 8;  // [E+1]
   int* wslot = tile_start + (P.E + 1);  // [E] weight slot of each expert (-1: skipped)
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   {
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    if (tiles_off + static_cast<uint32_t>(kTS * kBTile) > dyn) {  // layout assumption broken: refuse
+    if (tiles_off + static_cast<uint32_t>(kTS * kBTile + (WF == kFmtW2 ? kCodes : 0)) > dyn) {  // refuse
       if (tid == 0) set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
       return;
     }
@@ -280,6 +283,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
+    for (int c = 0; c < kCS; ++c) {
+      mbar_init(&code_full[c], 1);
+      mbar_init(&code_empty[c], 8);
+    }
     flags[0] = 0;
     fence_barrier_init();
   }
@@ -315,7 +322,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const int kbs = SWc / kKB;           // k-blocks per slice
   const int NSL = P.K / SWc;
   if (warp == 0) {
-    // ================= token tiles (and 2-bit codes) by TMA =================
+    // ================= token tiles (lane 0) and 2-bit codes (lane 1) by TMA =================
     if (lane == 0) {
       uint32_t L = 0;
       for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
@@ -329,20 +336,37 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
             ok = false;
             break;
           }
-          if (WF == kFmtW2) {  // + the stage's codes and scales of both weight blocks
-            mbar_arrive_expect_tx(&full_b[s], kBTile + kCodeStage);
-            tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
-            const int sl = kb / kbs, kin = kb - sl * kbs;
-            const int qrow = (e * NSL + sl) * (P.R >> 2);
+          mbar_arrive_expect_tx(&full_b[s], kBTile);
+          tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+        }
+        if (!ok) {
+          abort_all();
+          break;
+        }
+      }
+    }
+  } else if (warp == 14) {
+    if (lane == 0 && WF == kFmtW2) {
+      // the stage's codes and scales of both weight blocks, up to kCS stages ahead
+      uint32_t L = 0;
+      for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
+        int e, blk, mt;
+        decode_tile(i, e, blk, mt);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          const int c = L % kCS;
+          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&code_full[c], kCodeStage);
+          const int sl = kb / kbs, kin = kb - sl * kbs;
+          const int qrow = (e * NSL + sl) * (P.R >> 2);
 #pragma unroll
-            for (int bs = 0; bs < 2; ++bs) {
-              const int q0 = qrow + (fc1 ? (bs ? (P.N >> 2) : 0) + blk * 32 : blk * 64 + bs * 32);
-              tma_load_tile(codes_s + s * kCodeStage + bs * 2048, &tmap_c, kin * 64, q0, &full_b[s]);
-              tma_load_tile(codes_s + s * kCodeStage + 4096 + bs * 512, &tmap_s, kin * 16, q0, &full_b[s]);
-            }
-          } else {
-            mbar_arrive_expect_tx(&full_b[s], kBTile);
-            tma_load_tile(tiles + s * kBTile, &tmap_b, kb * kKB, row0, &full_b[s]);
+          for (int bs = 0; bs < 2; ++bs) {
+            const int q0 = qrow + (fc1 ? (bs ? (P.N >> 2) : 0) + blk * 32 : blk * 64 + bs * 32);
+            tma_load_tile(codes_s + c * kCodeStage + bs * 2048, &tmap_c, kin * 64, q0, &code_full[c]);
+            tma_load_tile(codes_s + c * kCodeStage + 4096 + bs * 512, &tmap_s, kin * 16, q0, &code_full[c]);
           }
         }
         if (!ok) {
@@ -354,10 +378,15 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   } else if (warp == 1) {
     // ================= MMA issue =================
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_mn(128, NT);
       uint32_t L = 0;
       int t = 0;
       for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
+        // N of this tile's MMAs: its tokens rounded up to 16 (a group's last
+        // tile is usually partial; the tensor time scales with N)
+        int e, blk, mt;
+        decode_tile(i, e, blk, mt);
+        const int nvalid = min(NT, P.offsets[e + 1] - P.offsets[e] - mt * NT);
+        const uint32_t idesc = idesc_bf16_mn(128, min(NT, (nvalid + 15) & ~15));
         if (t >= 1 && !mbar_wait(acc_empty, (t - 1) & 1)) {
           abort_all();
           break;
@@ -424,21 +453,27 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const uint32_t cbase = smem_u32(codes_s) + static_cast<uint32_t>(bsel * 2048 + (m >> 2) * 64 + (m & 3) * 4);
       const uint32_t sbase = smem_u32(codes_s) + static_cast<uint32_t>(4096 + bsel * 512 + (m >> 2) * 16 + (m & 3) * 2);
       for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
-        const int s = L % kTS;
-        if ((L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) || !mbar_wait(&full_b[s], (L / kTS) & 1)) {
+        const int s = L % kTS, c = L % kCS;
+        if (!mbar_wait(&code_full[c], (L / kCS) & 1)) {
+          ok = false;
+          break;
+        }
+        uint32_t w[4], sc0, sc1;
+        const uint32_t co = cbase + static_cast<uint32_t>(c * kCodeStage);
+        const uint32_t so = sbase + static_cast<uint32_t>(c * kCodeStage);
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(co) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1+16];" : "=r"(w[1]) : "r"(co) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1+32];" : "=r"(w[2]) : "r"(co) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1+48];" : "=r"(w[3]) : "r"(co) : "memory");
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so) : "memory");
+        asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so) : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&code_empty[c]);  // the code slot is free again
+        if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
           ok = false;
           break;
         }
         tm_fence_after();  // the MMAs that read this A stage are complete
-        uint32_t w[4], sc0, sc1;
-        const uint32_t co = cbase + static_cast<uint32_t>(s * kCodeStage);
-        const uint32_t so = sbase + static_cast<uint32_t>(s * kCodeStage);
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(co));
-        asm volatile("ld.shared.u32 %0, [%1+16];" : "=r"(w[1]) : "r"(co));
-        asm volatile("ld.shared.u32 %0, [%1+32];" : "=r"(w[2]) : "r"(co));
-        asm volatile("ld.shared.u32 %0, [%1+48];" : "=r"(w[3]) : "r"(co));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so));
-        asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so));
         uint32_t o[32];
         const uint32_t s_lo = sc0 | (sc0 << 16), s_hi = sc1 | (sc1 << 16);
         w2_decode_word(w[0], lanebase, s_lo, o);
@@ -726,7 +761,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
   // the first 64 KB-aligned address past kPre; the kernel checks the layout
   const size_t pre = lut ? ((1024 + static_cast<size_t>(kPre) + 65535) & ~size_t(65535)) - 1024 + 65536
                          : static_cast<size_t>(kPre) + 1024;
-  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + 1024;
+  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + (WF == kFmtW2 ? kCodes : 0) + 1024;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
