@@ -46,7 +46,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTmWarps = 15;  // TMA, MMA, 8 decode, 4 epilogue, code TMA
+constexpr int kTmWarps = 16;  // TMA, MMA (block 0), 8 decode, 4 epilogue, code TMA, MMA (block 1)
 constexpr int kTmThreads = kTmWarps * 32;
 constexpr int kKB = 64;    // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kTS = 4;     // pipeline stages (TMEM: 2 x 128 accumulator + 4 x 64 A columns = 512)
@@ -201,10 +201,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       kLut ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
   uint8_t* tiles = smem + tiles_off;
   uint8_t* codes_s = tiles + kTS * kBTile;  // 2-bit: per-stage code / scale tiles (TMA)
-  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* full_b = full_a + kTS;
-  uint64_t* empty = full_b + kTS;
-  uint64_t* acc_full = empty + kTS;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);  // [2][kTS] A stage of weight block b decoded
+  uint64_t* full_b = full_a + 2 * kTS;                     // [kTS] token tile landed
+  uint64_t* empty = full_b + kTS;                          // [2][kTS] block b's MMAs of the stage done
+  uint64_t* acc_full = empty + 2 * kTS;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* code_full = acc_empty + 1;    // [kCS] 2-bit code ring
   uint64_t* code_empty = code_full + kCS; // [kCS]
@@ -277,11 +277,13 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   }
   if (tid == 0) {
     for (int s = 0; s < kTS; ++s) {
-      mbar_init(&full_a[s], 8);
+      mbar_init(&full_a[s], 4);
+      mbar_init(&full_a[kTS + s], 4);
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&empty[kTS + s], 1);
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);
     mbar_init(acc_empty, 4);
     for (int c = 0; c < kCS; ++c) {
       mbar_init(&code_full[c], 1);
@@ -332,7 +334,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kTS;
-          if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+          if (L >= kTS && (!mbar_wait(&empty[s], ((L / kTS) - 1) & 1) ||
+                           !mbar_wait(&empty[kTS + s], ((L / kTS) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -375,9 +378,11 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         }
       }
     }
-  } else if (warp == 1) {
-    // ================= MMA issue =================
+  } else if (warp == 1 || warp == 15) {
+    // ================= MMA issue: weight block 0 from warp 1, block 1 from warp 15 =================
+    // (one thread's MMAs run back to back; two issuers keep the tensor pipe fed)
     if (lane == 0) {
+      const int bs = warp == 1 ? 0 : 1;
       uint32_t L = 0;
       int t = 0;
       for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
@@ -396,21 +401,20 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kTS;
           const uint32_t par = (L / kTS) & 1;
-          if (!mbar_wait(&full_b[s], par) || !mbar_wait(&full_a[s], par)) {
+          if (!mbar_wait(&full_b[s], par) || !mbar_wait(&full_a[bs * kTS + s], par)) {
             ok = false;
             break;
           }
           tm_fence_after();
           const uint32_t sb = smem_u32(tiles + s * kBTile);
-          const uint32_t a0 = tmem + kColA + static_cast<uint32_t>(s * 64);
+          const uint32_t a0 = tmem + kColA + static_cast<uint32_t>(s * 64 + bs * 32);
 #pragma unroll
           for (int ks = 0; ks < kKB / 16; ++ks) {
             const uint64_t bd = desc_sw128(sb + ks * 32);
             const uint32_t acc = (kb | ks) != 0;
-            umma_ts(tmem, a0 + ks * 8, bd, idesc, acc);
-            umma_ts(tmem + NT, a0 + 32 + ks * 8, bd, idesc, acc);
+            umma_ts(tmem + static_cast<uint32_t>(bs * NT), a0 + ks * 8, bd, idesc, acc);
           }
-          umma_commit_to(&empty[s]);
+          umma_commit_to(&empty[bs * kTS + s]);
         }
         if (!ok) {
           abort_all();
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so) : "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&code_empty[c]);  // the code slot is free again
-        if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
           ok = false;
           break;
         }
@@ -484,7 +488,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         tm_st_wait();
         tm_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[s]);
+        if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
       }
     } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2], E8M0 [slot][R][K/32]
       constexpr int D = 3;
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           const uint32_t L = L0 + d0;
           if (L < Ltot && ok) {
             const int s = L % kTS;
-            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
               ok = false;
             } else {
               tm_fence_after();
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               tm_st_wait();
               tm_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&full_a[s]);
+              if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
             }
           }
         }
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           const uint32_t L = L0 + d0;
           if (L < Ltot && ok) {
             const int s = L % kTS;
-            if (L >= kTS && !mbar_wait(&empty[s], ((L / kTS) - 1) & 1)) {
+            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
               ok = false;
             } else {
               tm_fence_after();
@@ -610,7 +614,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               tm_st_wait();
               tm_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&full_a[s]);
+              if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
             }
           }
         }
@@ -653,7 +657,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         const int nb0 = fc1 ? blk * 128 : blk * 256;
         for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
 #pragma unroll 1
-          for (int c = 0; c < NT; c += 32) {
+          for (int c = 0; c < nvalid; c += 32) {
             uint32_t r0[32], r1[32];
             if (fc1) {
               tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       } else {
         const int n0 = fc1 ? blk * 128 + nl : blk * 256 + nl;
 #pragma unroll 1
-        for (int c = 0; c < NT; c += 32) {
+        for (int c = 0; c < nvalid; c += 32) {
           uint32_t r0[32], r1[32];
           tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
           tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
