@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   uint64_t* full_b = full_a + 2 * kTS;                     // [kTS] token tile landed
   uint64_t* empty = full_b + kTS;                          // [2][kTS] block b's MMAs of the stage done
   uint64_t* acc_full = empty + 2 * kTS;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* code_full = acc_empty + 1;    // [kCS] 2-bit code ring
+  uint64_t* acc_empty = acc_full + 1;    // [2] weight block b's accumulator read
+  uint64_t* code_full = acc_empty + 2;    // [kCS] 2-bit code ring
   uint64_t* code_empty = code_full + kCS; // [kCS]
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(code_empty + kCS);
   int* flags = reinterpret_cast<int*>(tmem_base_s + 2);
@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       mbar_init(&empty[kTS + s], 1);
     }
     mbar_init(acc_full, 2);
-    mbar_init(acc_empty, 4);
+    mbar_init(&acc_empty[0], 4);
+    mbar_init(&acc_empty[1], 4);
     for (int c = 0; c < kCS; ++c) {
       mbar_init(&code_full[c], 1);
       mbar_init(&code_empty[c], 8);
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         decode_tile(i, e, blk, mt);
         const int nvalid = min(NT, P.offsets[e + 1] - P.offsets[e] - mt * NT);
         const uint32_t idesc = idesc_bf16_mn(128, min(NT, (nvalid + 15) & ~15));
-        if (t >= 1 && !mbar_wait(acc_empty, (t - 1) & 1)) {
+        if (t >= 1 && !mbar_wait(&acc_empty[bs], (t - 1) & 1)) {
           abort_all();
           break;
         }
@@ -630,8 +631,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   } else {
     // ================= epilogue =================
     // bf16 outputs go through a shared staging tile [token][128 outputs] so
-    // that the accumulator is released as soon as it is read (FC1) and the
-    // global stores are whole 256-byte row pieces (16 bytes per lane)
+    // that the global stores are whole 256-byte row pieces (16 bytes per
+    // lane); storing 2 bytes per lane straight from registers measured slower
     const int q = warp & 3;
     const int et = tid - 10 * 32;  // 0..127
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
@@ -659,6 +660,16 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const int nvalid = min(NT, P.offsets[e + 1] - p0);
       const bool bf16_out = P.out_fmt != MOE_FMT_F32;
       const bool mx_out = P.out_fmt == MOE_FMT_MXFP8_BF16;
+      // a weight block's accumulator is free once its last column chunk is
+      // read (FC1: gate and up together), before that chunk's math
+      auto release = [&](int which) {  // 0 / 1: that block, 2: both
+        tm_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (which != 1) mbar_arrive(&acc_empty[0]);
+          if (which != 0) mbar_arrive(&acc_empty[1]);
+        }
+      };
       if (bf16_out) {
         const int nb0 = fc1 ? blk * 128 : blk * 256;
         for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
@@ -672,6 +683,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
             }
             tm_ld_wait();
+            if (c + 32 >= nvalid) release(fc1 ? 2 : half);
             if (mx_out) {
               // MXFP8 rounding: token j's block of 32 outputs is this warp's 32 lanes
 #pragma unroll
@@ -701,11 +713,6 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               }
             }
           }
-          if (fc1 || half == 1) {  // the accumulator has been read
-            tm_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
-          }
           store_stage(p0, nvalid, nb0 + half * 128);
         }
       } else {
@@ -716,6 +723,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
           tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
           tm_ld_wait();
+          if (c + 32 >= nvalid) release(2);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (c + j < nvalid) {
@@ -729,9 +737,6 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
             }
           }
         }
-        tm_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
       }
     }
   }
