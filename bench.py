@@ -95,24 +95,29 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workloads
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, FC1/FC2
-# mean) of the table GEMV on the decode workload, from the ncu capture
-# summarised in profiles/w2_lut_kernel_decode.md; reported only while the
-# kernel source is the one that was captured (sha256 of csrc/gemv_lut.cu).
-_LUT_TRAFFIC = {"workload": "decode", "bytes": 251.3e6,
-                "src_sha256": "8e4daf084889b0c093d4b020071a2c2a2903ffae3780e50e9fcc943bf1a2fcb3"}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean of
+# the FC1 and FC2 launches) of the dominant kernel, from the ncu captures
+# summarised under profiles/; reported only while the kernel source is the
+# one that was captured (sha256 of the file named).
+_TRAFFIC = {
+    "decode": {"bytes": 249.97e6, "src": "gemv_lut.cu",
+               "src_sha256": "3404a565738da824c143a8dc3243badbd86d2bf164ec745645115fb5339342e2"},
+    "prefill_bf16": {"bytes": 2313.37e6, "src": "gemm_tmem.cu",
+                     "src_sha256": "36b411fd15619d7d673f43b2c3e941b1da70f41edd58dbb4d6913f4124b4006b"},
+}
 
 
-def _decode_traffic(w):
+def _traffic(w):
     import hashlib
-    src = os.path.join(ROOT, "bit_moe_expert_top_gb300", "csrc", "gemv_lut.cu")
+    ent = _TRAFFIC.get(w.name)
+    if not ent or ent["bytes"] is None:
+        return None
+    src = os.path.join(ROOT, "bit_moe_expert_top_gb300", "csrc", ent["src"])
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
-    if w.name != _LUT_TRAFFIC["workload"] or digest != _LUT_TRAFFIC["src_sha256"]:
-        return None
-    return _LUT_TRAFFIC["bytes"]
+    return ent["bytes"] if digest == ent["src_sha256"] else None
 
 
 def flops_per_assignment(w):
@@ -257,7 +262,7 @@ def run_gpu(args):
 
     peaks = _peaks()
     decode = w.T * w.k < 4096
-    traffic = _decode_traffic(w) if decode else None
+    traffic = _traffic(w) if args.tokens is None else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -267,7 +272,7 @@ def run_gpu(args):
     else:
         achieved = S * A * flops_per_assignment(w) / (mm_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": traffic,
                 "kernel": "expert matmuls", "peak_src": peaks["src"], "launch_us": round(mm_ms / n_mm * 1e3, 2)}
 
     # ---------------- end to end: host buffers through the public API

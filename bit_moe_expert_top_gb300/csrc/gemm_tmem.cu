@@ -55,9 +55,13 @@ constexpr int kStg = 128 * 128 * 2;     // epilogue staging: [NT tokens][128 out
 constexpr int kCodeStage = 4096 + 1024; // 2-bit: codes [2 blocks][32 quads][64 B] + scales [2][32][16 B]
 constexpr int kCS = 6;                  // 2-bit: code ring stages (runs ahead of the TMEM stages)
 constexpr int kCodes = kCS * kCodeStage; // after the token tiles
+constexpr int kWStage = 2 * 128 * kKB;  // E4M3: both blocks' rows x 64 K bytes per ring stage
 constexpr int kPre = kTab + kStg;           // shared bytes before the LUT window
 
 enum { kFmtW2 = 0, kFmtE4M3 = 1, kFmtMX4 = 2 };
+// TMA-fed weight ring (2-bit codes + scales, or E4M3 bytes) after the token tiles
+template <int WF>
+__host__ __device__ constexpr int ring_bytes() { return WF == kFmtW2 ? kCodes : (WF == kFmtE4M3 ? kCS * kWStage : 0); }
 
 struct TmParams {
   const uint8_t* wq;        // W2: w2l codes; E4M3: workspace bytes [slots][R][K]; MX4: E2M1 [slots][R][K/2]
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const uint32_t tiles_off =
       kLut ? (win - base + 65536u) : (((base + static_cast<uint32_t>(kPre) + 1023u) & ~1023u) - base);
   uint8_t* tiles = smem + tiles_off;
-  uint8_t* codes_s = tiles + kTS * kBTile;  // 2-bit: per-stage code / scale tiles (TMA)
+  uint8_t* codes_s = tiles + kTS * kBTile;  // per-stage weight tiles (TMA): 2-bit codes / scales, E4M3 bytes
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);  // [2][kTS] A stage of weight block b decoded
   uint64_t* full_b = full_a + 2 * kTS;                     // [kTS] token tile landed
   uint64_t* empty = full_b + kTS;                          // [2][kTS] block b's MMAs of the stage done
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   {
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    if (tiles_off + static_cast<uint32_t>(kTS * kBTile + (WF == kFmtW2 ? kCodes : 0)) > dyn) {  // refuse
+    if (tiles_off + static_cast<uint32_t>(kTS * kBTile + ring_bytes<WF>()) > dyn) {  // refuse
       if (tid == 0) set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
       return;
     }
@@ -260,6 +264,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
       } else {
         sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
+        if (WF == kFmtE4M3 && sl >= P.E) {    // beyond the E slots the weight tensor map spans
+          set_err(P.dev_err, MOE_DEVERR_BAD_ID);
+          sl = -1;
+        }
       }
     }
     wslot[e] = sl;
@@ -356,6 +364,33 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       }
     }
   } else if (warp == 14) {
+    if (lane == 0 && WF == kFmtE4M3) {
+      // the stage's E4M3 bytes of both weight blocks (128 rows x 64 K each), up to kCS stages ahead
+      uint32_t L = 0;
+      for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
+        int e, blk, mt;
+        decode_tile(i, e, blk, mt);
+        const int rbase = wslot[e] * P.R;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          const int c = L % kCS;
+          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&code_full[c], kWStage);
+#pragma unroll
+          for (int bs = 0; bs < 2; ++bs) {
+            const int r0 = rbase + (fc1 ? (bs ? P.N : 0) + blk * 128 : blk * 256 + bs * 128);
+            tma_load_tile(codes_s + c * kWStage + bs * (kWStage / 2), &tmap_c, kb * kKB, r0, &code_full[c]);
+          }
+        }
+        if (!ok) {
+          abort_all();
+          break;
+        }
+      }
+    }
     if (lane == 0 && WF == kFmtW2) {
       // the stage's codes and scales of both weight blocks, up to kCS stages ahead
       uint32_t L = 0;
@@ -460,8 +495,12 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     bool ok = true;
     if (WF == kFmtW2) {
       // codes and scales of this thread's row come from the TMA-filled stage
-      // tiles: quad qd = block bsel's quad m/4, row rr = m % 4
+      // tiles: quad qd = block bsel's quad m/4, row rr = m % 4.  The code tile
+      // is written with the 64-byte swizzle (16-byte chunk w of tile row qd at
+      // chunk w ^ ((qd >> 1) & 3)), so the warp's 32 word reads hit 32 banks
       const uint32_t cbase = smem_u32(codes_s) + static_cast<uint32_t>(bsel * 2048 + (m >> 2) * 64 + (m & 3) * 4);
+      const uint32_t cx = static_cast<uint32_t>((m >> 3) & 3);
+      const uint32_t cw0 = (0u ^ cx) << 4, cw1 = (1u ^ cx) << 4, cw2 = (2u ^ cx) << 4, cw3 = (3u ^ cx) << 4;
       const uint32_t sbase = smem_u32(codes_s) + static_cast<uint32_t>(4096 + bsel * 512 + (m >> 2) * 16 + (m & 3) * 2);
       for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
         const int s = L % kTS, c = L % kCS;
@@ -472,10 +511,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         uint32_t w[4], sc0, sc1;
         const uint32_t co = cbase + static_cast<uint32_t>(c * kCodeStage);
         const uint32_t so = sbase + static_cast<uint32_t>(c * kCodeStage);
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(co) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1+16];" : "=r"(w[1]) : "r"(co) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1+32];" : "=r"(w[2]) : "r"(co) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1+48];" : "=r"(w[3]) : "r"(co) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(co + cw0) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[1]) : "r"(co + cw1) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[2]) : "r"(co + cw2) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[3]) : "r"(co + cw3) : "memory");
         asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so) : "memory");
         asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so) : "memory");
         __syncwarp();
@@ -576,55 +615,48 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           }
         }
       }
-    } else {  // E4M3 workspace: [slot][R][K] bytes, scale folded in
-      constexpr int D = 2;
-      const int64_t mat = static_cast<int64_t>(P.R) * P.K;
-      uint4 vb[D][4];
-      const uint8_t* vp = P.wq;
-      auto rebase = [&]() { vp = P.wq + wslot[pe] * mat + static_cast<int64_t>(wrow(pblk)) * P.K; };
-      if (pi < total) rebase();
-      auto load = [&](uint4 (&x)[4]) {
-        if (pi >= total) return;
-        const uint4* p = reinterpret_cast<const uint4*>(vp);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = __ldg(p + j);
-        if (next_tile()) {
-          if (pi < total) rebase();
-        } else {
-          vp += kKB;
+    } else {  // E4M3 workspace: [slot][R][K] bytes, scale folded in, fed by TMA
+      // this thread's row: tile row m of block bsel, 64 bytes written with the
+      // 64-byte swizzle (16-byte chunk j at chunk j ^ ((m >> 1) & 3)); a
+      // quarter-warp's 8 rows then cover all 32 banks
+      const uint32_t rb = smem_u32(codes_s) + static_cast<uint32_t>(bsel * (kWStage / 2) + m * 64);
+      const uint32_t rx = static_cast<uint32_t>((m >> 1) & 3);
+      for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
+        const int s = L % kTS, c = L % kCS;
+        if (!mbar_wait(&code_full[c], (L / kCS) & 1)) {
+          ok = false;
+          break;
         }
-      };
+        uint4 vb[4];
+        const uint32_t ro = rb + static_cast<uint32_t>(c * kWStage);
 #pragma unroll
-      for (int d0 = 0; d0 < D; ++d0) load(vb[d0]);
-      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
+        for (int j = 0; j < 4; ++j)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(vb[j].x), "=r"(vb[j].y), "=r"(vb[j].z), "=r"(vb[j].w)
+                       : "r"(ro + ((static_cast<uint32_t>(j) ^ rx) << 4))
+                       : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&code_empty[c]);  // the ring slot is free again
+        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tm_fence_after();  // the MMAs that read this A stage are complete
+        uint32_t o[32];
 #pragma unroll
-        for (int d0 = 0; d0 < D; ++d0) {
-          const uint32_t L = L0 + d0;
-          if (L < Ltot && ok) {
-            const int s = L % kTS;
-            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
-              ok = false;
-            } else {
-              tm_fence_after();
-              uint32_t o[32];
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t ww[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint32_t ww[4] = {vb[d0][j].x, vb[d0][j].y, vb[d0][j].z, vb[d0][j].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  o[8 * j + 2 * h] = e4m3x2_to_bf16x2(ww[h] & 0xffffu);
-                  o[8 * j + 2 * h + 1] = e4m3x2_to_bf16x2(ww[h] >> 16);
-                }
-              }
-              load(vb[d0]);
-              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
-              tm_st_wait();
-              tm_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
-            }
+          for (int h = 0; h < 4; ++h) {
+            o[8 * j + 2 * h] = e4m3x2_to_bf16x2(ww[h] & 0xffffu);
+            o[8 * j + 2 * h + 1] = e4m3x2_to_bf16x2(ww[h] >> 16);
           }
         }
+        tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+        tm_st_wait();
+        tm_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
       }
     }
     if (!ok) abort_all();
@@ -776,7 +808,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
   // the first 64 KB-aligned address past kPre; the kernel checks the layout
   const size_t pre = lut ? ((1024 + static_cast<size_t>(kPre) + 65535) & ~size_t(65535)) - 1024 + 65536
                          : static_cast<size_t>(kPre) + 1024;
-  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + (WF == kFmtW2 ? kCodes : 0) + 1024;
+  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + ring_bytes<WF>() + 1024;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -845,10 +877,21 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
     const cuuint64_t sd[2] = {static_cast<cuuint64_t>(SW / 4), qrows}, ss[1] = {static_cast<cuuint64_t>(SW / 4)};
     const cuuint32_t cbox[2] = {64, 32}, sbox[2] = {16, 32};
     if (enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), cd, cs, cbox, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
         enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.wscale), sd, ss, sbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (a.wkind == kFP8) {
+    // E4M3 workspace as a 2-D byte array [E slots x R rows][K]; box 64 bytes x
+    // 128 rows (one weight block), 64-byte swizzle
+    const cuuint64_t wd[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.E) * P.R};
+    const cuuint64_t ws[1] = {static_cast<cuuint64_t>(a.K)};
+    const cuuint32_t wbox[2] = {kKB, 128};
+    if (enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), wd, ws, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

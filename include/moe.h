@@ -280,7 +280,9 @@ MOE_API int moe_w2_mm_noalloc(int stage,
  *       expert_slot NULL means slot = e).
  *   fp8_ws non-NULL: E4M3 workspace, expert e uses slot ws_slot_of_expert[e]
  *       (rows*K bytes per slot, as written by mxfp4_to_fp8_ws); experts with a
- *       negative slot are skipped.
+ *       negative slot are skipped.  Slots are below E (a workspace holds at
+ *       most one slot per expert); on the tensor-core path (MOE_MODE_GEMM) a
+ *       slot >= E sets MOE_DEVERR_BAD_ID and its expert is skipped.
  * Only experts e in [expert_begin, expert_end) are processed. */
 MOE_API int moe_mxfp4_mm(int stage, int mode,
                  const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
