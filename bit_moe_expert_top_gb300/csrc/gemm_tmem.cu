@@ -56,12 +56,19 @@ constexpr int kCodeStage = 4096 + 1024; // 2-bit: codes [2 blocks][32 quads][64 
 constexpr int kCS = 6;                  // 2-bit: code ring stages (runs ahead of the TMEM stages)
 constexpr int kCodes = kCS * kCodeStage; // after the token tiles
 constexpr int kWStage = 2 * 128 * kKB;  // E4M3: both blocks' rows x 64 K bytes per ring stage
+constexpr int kQStage = 2 * 128 * kKB / 2;  // MXFP4: both blocks' rows x 64 K nibbles per ring stage
 constexpr int kPre = kTab + kStg;           // shared bytes before the LUT window
 
 enum { kFmtW2 = 0, kFmtE4M3 = 1, kFmtMX4 = 2 };
-// TMA-fed weight ring (2-bit codes + scales, or E4M3 bytes) after the token tiles
-template <int WF>
-__host__ __device__ constexpr int ring_bytes() { return WF == kFmtW2 ? kCodes : (WF == kFmtE4M3 ? kCS * kWStage : 0); }
+// TMA-fed weight ring after the token tiles: 2-bit codes + scales, E4M3
+// bytes or E2M1 nibbles; stages in flight (MXFP4 with 128-token tiles: 4, as
+// its LUT window leaves less room)
+template <int WF, int NT>
+__host__ __device__ constexpr int ring_depth() { return (WF == kFmtMX4 && NT == 128) ? 4 : kCS; }
+template <int WF, int NT>
+__host__ __device__ constexpr int ring_bytes() {
+  return ring_depth<WF, NT>() * (WF == kFmtW2 ? kCodeStage : (WF == kFmtE4M3 ? kWStage : kQStage));
+}
 
 struct TmParams {
   const uint8_t* wq;        // W2: w2l codes; E4M3: workspace bytes [slots][R][K]; MX4: E2M1 [slots][R][K/2]
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   {
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    if (tiles_off + static_cast<uint32_t>(kTS * kBTile + ring_bytes<WF>()) > dyn) {  // refuse
+    if (tiles_off + static_cast<uint32_t>(kTS * kBTile + ring_bytes<WF, NT>()) > dyn) {  // refuse
       if (tid == 0) set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
       return;
     }
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
       } else {
         sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
-        if (WF == kFmtE4M3 && sl >= P.E) {    // beyond the E slots the weight tensor map spans
+        if (sl >= P.E) {                      // beyond the E slots the weight tensor map spans
           set_err(P.dev_err, MOE_DEVERR_BAD_ID);
           sl = -1;
         }
@@ -383,6 +390,34 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           for (int bs = 0; bs < 2; ++bs) {
             const int r0 = rbase + (fc1 ? (bs ? P.N : 0) + blk * 128 : blk * 256 + bs * 128);
             tma_load_tile(codes_s + c * kWStage + bs * (kWStage / 2), &tmap_c, kb * kKB, r0, &code_full[c]);
+          }
+        }
+        if (!ok) {
+          abort_all();
+          break;
+        }
+      }
+    }
+    if (lane == 0 && WF == kFmtMX4) {
+      // the stage's E2M1 nibbles of both weight blocks (128 rows x 32 bytes each)
+      constexpr int RD = ring_depth<WF, NT>();
+      uint32_t L = 0;
+      for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x) {
+        int e, blk, mt;
+        decode_tile(i, e, blk, mt);
+        const int rbase = wslot[e] * P.R;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++L) {
+          const int c = L % RD;
+          if (L >= RD && !mbar_wait(&code_empty[c], ((L / RD) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&code_full[c], kQStage);
+#pragma unroll
+          for (int bs = 0; bs < 2; ++bs) {
+            const int r0 = rbase + (fc1 ? (bs ? P.N : 0) + blk * 128 : blk * 256 + bs * 128);
+            tma_load_tile(codes_s + c * kQStage + bs * (kQStage / 2), &tmap_c, kb * (kKB / 2), r0, &code_full[c]);
           }
         }
         if (!ok) {
@@ -517,8 +552,6 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[3]) : "r"(co + cw3) : "memory");
         asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so) : "memory");
         asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so) : "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&code_empty[c]);  // the code slot is free again
         if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
           ok = false;
           break;
@@ -534,50 +567,62 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         tm_st_wait();
         tm_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
+        // the ring slot is released only now: tcgen05.st consumed values
+        // derived from every word read from it, so those reads are complete
+        // before the TMA may refill the slot
+        if (lane == 0) {
+          mbar_arrive(&code_empty[c]);
+          mbar_arrive(&full_a[bsel * kTS + s]);
+        }
       }
-    } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2], E8M0 [slot][R][K/32]
-      constexpr int D = 3;
-      const int64_t mat_q = static_cast<int64_t>(P.R) * (P.K / 2);
+    } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2] fed by TMA, E8M0 [slot][R][K/32] loaded here
+      constexpr int RD = ring_depth<WF, NT>();
+      constexpr int D = 6;  // scale loads in flight (two E8M0 bytes per stage)
       const int64_t mat_s = static_cast<int64_t>(P.R) * (P.K / 32);
       const uint8_t* e8 = reinterpret_cast<const uint8_t*>(P.wscale);
-      uint4 qb[D][2];
       uint32_t sb[D];
-      const uint8_t* qp = P.wq;
       const uint8_t* ep = e8;
-      auto rebase = [&]() {
-        const int r = wrow(pblk);
-        const int64_t slot = wslot[pe];
-        qp = P.wq + slot * mat_q + static_cast<int64_t>(r) * (P.K / 2);
-        ep = e8 + slot * mat_s + static_cast<int64_t>(r) * (P.K / 32);
-      };
+      auto rebase = [&]() { ep = e8 + wslot[pe] * mat_s + static_cast<int64_t>(wrow(pblk)) * (P.K / 32); };
       if (pi < total) rebase();
-      auto load = [&](uint4 (&x)[2], uint32_t& sc) {
+      auto load = [&](uint32_t& sc) {
         if (pi >= total) return;
-        const uint4* pq = reinterpret_cast<const uint4*>(qp);
-        x[0] = __ldg(pq);
-        x[1] = __ldg(pq + 1);
         sc = __ldg(reinterpret_cast<const uint16_t*>(ep));
         if (next_tile()) {
           if (pi < total) rebase();
         } else {
-          qp += 32;
           ep += 2;
         }
       };
+      // this thread's row: tile row m of block bsel, 32 bytes written with the
+      // 32-byte swizzle (16-byte chunk h at chunk h ^ ((m >> 2) & 1)); a
+      // quarter-warp's 8 rows then cover all 32 banks
+      const uint32_t qrow = smem_u32(codes_s) + static_cast<uint32_t>(bsel * (kQStage / 2) + m * 32);
+      const uint32_t qx = static_cast<uint32_t>((m >> 2) & 1);
       // 2^(x-127) as bf16x2 (x = 0: the subnormal 2^-127; x = 255: NaN, flagged)
       auto scale2 = [&](uint32_t x) -> uint32_t {
         const uint32_t b = x == 0 ? 0x0040u : (x == 255 ? 0x7FC0u : (x << 7));
         return b | (b << 16);
       };
 #pragma unroll
-      for (int d0 = 0; d0 < D; ++d0) load(qb[d0], sb[d0]);
+      for (int d0 = 0; d0 < D; ++d0) load(sb[d0]);
       for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
 #pragma unroll
         for (int d0 = 0; d0 < D; ++d0) {
           const uint32_t L = L0 + d0;
           if (L < Ltot && ok) {
-            const int s = L % kTS;
+            const int s = L % kTS, c = L % RD;
+            if (!mbar_wait(&code_full[c], (L / RD) & 1)) {
+              ok = false;
+              break;
+            }
+            uint4 q[2];
+            const uint32_t qo = qrow + static_cast<uint32_t>(c * kQStage);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
+                           : "r"(qo + ((static_cast<uint32_t>(h) ^ qx) << 4))
+                           : "memory");
             if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
               ok = false;
             } else {
@@ -588,7 +633,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               uint32_t o[32];
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint32_t ww[4] = {qb[d0][h].x, qb[d0][h].y, qb[d0][h].z, qb[d0][h].w};
+                const uint32_t ww[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
                 const uint32_t sh = h ? s1 : s0;  // bytes 0..15: group 0, 16..31: group 1
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
@@ -605,12 +650,15 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                   }
                 }
               }
-              load(qb[d0], sb[d0]);
+              load(sb[d0]);
               tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
               tm_st_wait();
               tm_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
+              if (lane == 0) {
+                mbar_arrive(&code_empty[c]);  // after tcgen05.st consumed values from every word read
+                mbar_arrive(&full_a[bsel * kTS + s]);
+              }
             }
           }
         }
@@ -635,8 +683,6 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                        : "=r"(vb[j].x), "=r"(vb[j].y), "=r"(vb[j].z), "=r"(vb[j].w)
                        : "r"(ro + ((static_cast<uint32_t>(j) ^ rx) << 4))
                        : "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&code_empty[c]);  // the ring slot is free again
         if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
           ok = false;
           break;
@@ -656,7 +702,13 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         tm_st_wait();
         tm_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[bsel * kTS + s]);
+        // the ring slot is released only now: tcgen05.st consumed values
+        // derived from every word read from it, so those reads are complete
+        // before the TMA may refill the slot
+        if (lane == 0) {
+          mbar_arrive(&code_empty[c]);
+          mbar_arrive(&full_a[bsel * kTS + s]);
+        }
       }
     }
     if (!ok) abort_all();
@@ -808,7 +860,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
   // the first 64 KB-aligned address past kPre; the kernel checks the layout
   const size_t pre = lut ? ((1024 + static_cast<size_t>(kPre) + 65535) & ~size_t(65535)) - 1024 + 65536
                          : static_cast<size_t>(kPre) + 1024;
-  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + ring_bytes<WF>() + 1024;
+  const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + ring_bytes<WF, NT>() + 1024;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -881,6 +933,17 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
         enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.wscale), sd, ss, sbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (a.wkind == kMXFP4) {
+    // E2M1 nibbles as a 2-D byte array [E slots x R rows][K/2]; box 32 bytes x
+    // 128 rows (one weight block), 32-byte swizzle
+    const cuuint64_t qd[2] = {static_cast<cuuint64_t>(a.K / 2), static_cast<cuuint64_t>(a.E) * P.R};
+    const cuuint64_t qs[1] = {static_cast<cuuint64_t>(a.K / 2)};
+    const cuuint32_t qbox[2] = {kKB / 2, 128};
+    if (enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), qd, qs, qbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

@@ -277,7 +277,9 @@ MOE_API int moe_w2_mm_noalloc(int stage,
  * Weight source, exactly one of:
  *   e2m1/e8m0 non-NULL: MXFP4 slots [S][rows][K/2], [S][rows][K/32]; expert e
  *       uses slot expert_slot[e] (experts with expert_slot[e] < 0 are skipped;
- *       expert_slot NULL means slot = e).
+ *       expert_slot NULL means slot = e).  Slots are below E; on the
+ *       tensor-core path a slot >= E sets MOE_DEVERR_BAD_ID and its expert is
+ *       skipped.
  *   fp8_ws non-NULL: E4M3 workspace, expert e uses slot ws_slot_of_expert[e]
  *       (rows*K bytes per slot, as written by mxfp4_to_fp8_ws); experts with a
  *       negative slot are skipped.  Slots are below E (a workspace holds at
