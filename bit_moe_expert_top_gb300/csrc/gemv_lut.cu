@@ -51,6 +51,13 @@ constexpr int kPrologue = 8192;               // shared bytes below the table wi
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
+// prologue layout: pref [E+1] ints, then the CTA's segment table and the
+// double-buffered activation slice of the table builds
+constexpr int kSegTabOff = 4352;              // int2 [kSegCap]: (permuted row, token row or -1)
+constexpr int kSegCap = 128;
+constexpr int kXBufOff = kSegTabOff + 8 * kSegCap;  // bf16 [2][kSW]
+static_assert(kXBufOff + 2 * kSW * 2 <= kPrologue, "prologue overflow");
+static_assert(4 * (kMaxE + 1) <= kSegTabOff, "prologue overflow");
 
 struct LutParams {
   const uint16_t* act;
@@ -116,6 +123,13 @@ MOE_D float2 word_pair(uint32_t wa, uint32_t wb, uint32_t sc, uint32_t lanebase)
   const float2 s23 = fadd2(make_float2(ta.z, tb.z), make_float2(ta.w, tb.w));
   return fmul2(fadd2(s01, s23), make_float2(__uint_as_float(sc << 16), __uint_as_float(sc & 0xffff0000u)));
 }
+
+// 8-byte asynchronous global -> shared copy (completion by cp.async groups).
+MOE_D void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+MOE_D void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+MOE_D void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 MOE_D uint4 ldg_stream(const void* p) {
   uint4 v;
@@ -262,6 +276,52 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   };
 
   if (u_beg >= u_end) return;
+
+  // ---- the CTA's segments (one per (selected row, slice) table): their
+  // permuted row and token row, looked up once for all of them in parallel
+  // (a lookup per segment would stall every warp at each table build), and
+  // each segment's 512 activations brought into shared memory by cp.async
+  // one segment ahead
+  const int64_t seg_first = u_beg / NB;
+  const int64_t nseg = (u_end - 1) / NB - seg_first + 1;
+  int2* seg_tab = reinterpret_cast<int2*>(smem + kSegTabOff);
+  const uint16_t* xbuf = reinterpret_cast<const uint16_t*>(smem + kXBufOff);
+  auto seg_lookup = [&](int64_t sg) -> int2 {  // (p, row; row = -1 if the segment is skipped)
+    const int ps = static_cast<int>(sg / NSL);
+    const int ee = expert_of(ps);
+    const int pp = P.offsets[ee] + (ps - pref[ee]);
+    if (pp >= P.A) {  // the scratch does not cover this row: report and skip
+      set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
+      return make_int2(pp, -1);
+    }
+    const int rr = P.act_row ? P.act_row[pp] / P.act_row_div : pp;
+    if (rr < 0 || rr >= P.act_rows) {
+      set_err(P.dev_err, MOE_DEVERR_BAD_ID);
+      return make_int2(pp, -1);
+    }
+    return make_int2(pp, rr);
+  };
+  for (int i = tid; i < nseg && i < kSegCap; i += kLutThreads) seg_tab[i] = seg_lookup(seg_first + i);
+  __syncthreads();
+  auto seg_info = [&](int64_t sg) -> int2 {
+    const int64_t i = sg - seg_first;
+    return i < kSegCap ? seg_tab[i] : seg_lookup(sg);
+  };
+  // activations of segment sg into buffer sg & 1: 128 threads x 8 bytes; one
+  // cp.async group per call on every thread (empty where nothing is copied)
+  auto prefetch_x = [&](int64_t sg) {
+    if (sg < seg_first + nseg && tid < kSW / 4) {
+      const int2 si = seg_info(sg);
+      if (si.y >= 0) {
+        const int sl = static_cast<int>(sg % NSL);
+        cp_async8(smem_u32(xbuf) + static_cast<uint32_t>(((sg - seg_first) & 1) * kSW * 2 + 8 * tid),
+                  P.act + static_cast<size_t>(si.y) * P.K + sl * kSW + 4 * tid);
+      }
+    }
+    cp_async_commit();
+  };
+  prefetch_x(seg_first);
+  prefetch_x(seg_first + 1);
   // A warp's units: batches warp, warp + 16, ... of each segment (one segment
   // = one (row, slice) table) of the CTA's range.  The loads of a warp's next
   // unit go out while the current one is consumed, also across a segment
@@ -284,18 +344,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     const int64_t seg0 = seg * NB;
     const bool has_next = seg_end < u_end;
     const int64_t nseg_end = min(u_end, seg_end + NB);
-    const int p = P.offsets[e] + (psel - pref[e]);
-    int row = 0;
-    bool valid = p < P.A;
-    if (!valid) {  // the scratch does not cover this row: report and skip
-      if (tid == 0) set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
-    } else {
-      row = P.act_row ? P.act_row[p] / P.act_row_div : p;
-      if (row < 0 || row >= P.act_rows) {
-        valid = false;
-        if (tid == 0) set_err(P.dev_err, MOE_DEVERR_BAD_ID);
-      }
-    }
+    const int2 si = seg_info(seg);
+    const int p = si.x;
+    const bool valid = si.y >= 0;
     if (!pending && uw < seg_end) {
       issue(gcodes, gscales, static_cast<int>(uw - seg0));
       pending = true;
@@ -303,11 +354,11 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
 
     // ---- (re)build the tables for (row, s): warp w writes byte-in-word j = w & 3
     // and code bytes b in [64*(w>>2), +64); lane l is byte position 4l + j
+    cp_async_wait1();  // this segment's activations have landed (the next one's may be in flight)
     __syncthreads();  // nobody still reads the previous segment's tables
     if (valid) {
       const int j = warp & 3, bq = warp >> 2;
-      const uint2 xv = *reinterpret_cast<const uint2*>(P.act + static_cast<size_t>(row) * P.K + s * kSW + 16 * lane +
-                                                       4 * j);
+      const uint2 xv = *reinterpret_cast<const uint2*>(xbuf + ((seg - seg_first) & 1) * kSW + 16 * lane + 4 * j);
       const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
       const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
       const float cb[4] = {-4.f, -1.f, 1.f, 4.f};
@@ -327,6 +378,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
       }
     }
     __syncthreads();
+    prefetch_x(seg + 2);  // into the buffer this build has finished reading
 
     while (uw < seg_end) {
       const int rb = static_cast<int>(uw - seg0);
