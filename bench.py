@@ -101,9 +101,9 @@ class ClockSampler:
 # one that was captured (sha256 of the file named).
 _TRAFFIC = {
     "decode": {"bytes": 249.97e6, "src": "gemv_lut.cu",
-               "src_sha256": "3404a565738da824c143a8dc3243badbd86d2bf164ec745645115fb5339342e2"},
-    "prefill_bf16": {"bytes": 2313.37e6, "src": "gemm_tmem.cu",
-                     "src_sha256": "36b411fd15619d7d673f43b2c3e941b1da70f41edd58dbb4d6913f4124b4006b"},
+               "src_sha256": "b5d4dae93aec10a2191d557ae6ea818fae9193484cd77a022523784ce1b3cb08"},
+    "prefill_bf16": {"bytes": 2306.04e6, "src": "gemm_tmem.cu",
+                     "src_sha256": "64ec621e352148d220643305c5ca4c428b838c678578f1a42c7be658e7c1ff66"},
 }
 
 
