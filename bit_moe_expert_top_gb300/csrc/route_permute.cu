@@ -250,46 +250,56 @@ __global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_
   const int lane = threadIdx.x & 31;
   for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
     const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
-    for (int base = 0; base < H; base += 256) {
-      const int e0 = base + lane * 8;
-      const bool ok = e0 < H;
-      float f[8];
-      float amax = 0.f;
-      if (ok) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(src + e0));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    // four 256-element chunks per round: their loads are in flight together
+    for (int base0 = 0; base0 < H; base0 += 1024) {
+      uint4 raw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          f[2 * i] = __uint_as_float(wv[i] << 16);
-          f[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
-          amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-        }
+      for (int u = 0; u < 4; ++u) {
+        const int e0 = base0 + 256 * u + lane * 8;
+        if (e0 < H) raw[u] = __ldg(reinterpret_cast<const uint4*>(src + e0));
       }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      if (ok) {
-        const int X = mx_scale_exp(amax);
-        const float inv = exp2i(-X);
-        uint32_t packed[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t lo = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
-          uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-          packed[i] = lo | (hi << 16);
-        }
-        if (AS_BF16) {
-          const float sc2 = exp2i(X);
-          uint32_t o[4];
+      for (int u = 0; u < 4; ++u) {
+        const int e0 = base0 + 256 * u + lane * 8;
+        if (base0 + 256 * u >= H) break;  // warp-uniform
+        const bool ok = e0 < H;
+        float f[8];
+        float amax = 0.f;
+        if (ok) {
+          const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 v = e4m3x2_to_f32x2(static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1))));
-            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(v.y * sc2), "f"(v.x * sc2));
+            f[2 * i] = __uint_as_float(wv[i] << 16);
+            f[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
+            amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
           }
-          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + static_cast<size_t>(p) * H + e0) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-          *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
-          if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (ok) {
+          const int X = mx_scale_exp(amax);
+          const float inv = exp2i(-X);
+          uint32_t packed[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint32_t lo = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+            uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+            packed[i] = lo | (hi << 16);
+          }
+          if (AS_BF16) {
+            const float sc2 = exp2i(X);
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 v = e4m3x2_to_f32x2(static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1))));
+              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(v.y * sc2), "f"(v.x * sc2));
+            }
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + static_cast<size_t>(p) * H + e0) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+          } else {
+            *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
+            if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
+          }
         }
       }
     }
@@ -355,13 +365,13 @@ MOE_D void load8(const void* y, size_t off, float (&v)[8]) {
 }
 
 template <bool kYF32, bool kOutF32>
-__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
+__global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y, const float* __restrict__ w,
                                                       const int32_t* __restrict__ inv, int T, int k, int H,
                                                       void* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
-  const int c0 = blockIdx.x * 2048 + threadIdx.x * 8;
+  const int c0 = blockIdx.x * 1024 + threadIdx.x * 8;
   if (t >= T || c0 >= H) return;
   float acc[8];
 #pragma unroll
@@ -377,15 +387,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
       p[u] = iv[j + u];
       wj[u] = wt[j + u];
     }
-    float v[8][8];
+    if (!kYF32) {  // bf16 rows stay packed until used: 4 registers per row in flight instead of 8
+      uint4 raw[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (p[u] >= 0) load8<kYF32>(y, static_cast<size_t>(p[u]) * H + c0, v[u]);
+      for (int u = 0; u < 8; ++u)
+        if (p[u] >= 0)
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                        static_cast<size_t>(p[u]) * H + c0));
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (p[u] < 0) continue;
+      for (int u = 0; u < 8; ++u) {
+        if (p[u] < 0) continue;
+        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wj[u], __uint_as_float(wv[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wj[u], __uint_as_float(wv[i] & 0xffff0000u), acc[2 * i + 1]);
+        }
+      }
+    } else {
+      float v[8][8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p[u] >= 0) load8<kYF32>(y, static_cast<size_t>(p[u]) * H + c0, v[u]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (p[u] < 0) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
+      }
     }
   }
   for (; j + 4 <= k; j += 4) {
@@ -431,12 +460,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
 cudaError_t launch_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H,
                            void* out, int out_fmt, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid((H + 2047) / 2048, T);
+  const dim3 grid((H + 1023) / 1024, T);  // 128 threads x 8 outputs per block
   const bool yf = y_fmt == MOE_FMT_F32, of = out_fmt == MOE_FMT_F32;
-  if (yf && of) return launch_pdl(combine_kernel<true, true>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
-  if (yf) return launch_pdl(combine_kernel<true, false>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
-  if (of) return launch_pdl(combine_kernel<false, true>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
-  return launch_pdl(combine_kernel<false, false>, grid, dim3(256), 0, s, y, w, inv, T, k, H, out);
+  if (yf && of) return launch_pdl(combine_kernel<true, true>, grid, dim3(128), 0, s, y, w, inv, T, k, H, out);
+  if (yf) return launch_pdl(combine_kernel<true, false>, grid, dim3(128), 0, s, y, w, inv, T, k, H, out);
+  if (of) return launch_pdl(combine_kernel<false, true>, grid, dim3(128), 0, s, y, w, inv, T, k, H, out);
+  return launch_pdl(combine_kernel<false, false>, grid, dim3(128), 0, s, y, w, inv, T, k, H, out);
 }
 
 }  // namespace moe
