@@ -113,6 +113,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
 // first output row of each of its groups; the second walk writes perm/inv in
 // increasing assignment order within each expert (stable).
 constexpr int kPermWarps = 32;
+constexpr int kPermU = 8;  // 32-id tiles whose loads a warp keeps in flight
 
 __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ ids, int A, int E,
                                                        int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
@@ -134,18 +135,29 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   for (int i = tid; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
 
+  // the warp walks its chunk in tiles of 32 ids, kPermU tiles' loads in flight at once
   bool bad = false;
-  for (int base = beg; base < end; base += 32) {
-    const int a = base + lane;
-    int e = (a < end) ? ids[a] : -1;
-    if (a < end && (e < 0 || e >= E)) {
-      bad = true;
-      e = -1;
+  for (int base0 = beg; base0 < end; base0 += 32 * kPermU) {
+    int ev[kPermU];
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      const int a = base0 + 32 * u + lane;
+      ev[u] = (a < end) ? ids[a] : -1;
     }
-    const int key = (e >= 0) ? e : (E + lane);  // invalid lanes form singleton groups
-    const unsigned m = __match_any_sync(0xffffffffu, key);
-    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      if (base0 + 32 * u >= end) break;  // warp-uniform: past the chunk
+      const int a = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (a < end && (e < 0 || e >= E)) {
+        bad = true;
+        e = -1;
+      }
+      const int key = (e >= 0) ? e : (E + lane);  // invalid lanes form singleton groups
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp();
+    }
   }
   if (bad) set_err(dev_err, MOE_DEVERR_BAD_ID);
   __syncthreads();
@@ -193,20 +205,30 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   for (int i = tid; i < nw * E; i += blockDim.x) hist[i] += tot[i % E];
   __syncthreads();
 
-  for (int base = beg; base < end; base += 32) {
-    const int a = base + lane;
-    int e = (a < end) ? ids[a] : -1;
-    if (a < end && (e < 0 || e >= E)) e = -1;
-    const int key = (e >= 0) ? e : (E + lane);
-    const unsigned m = __match_any_sync(0xffffffffu, key);
-    int pos = -1;
-    if (e >= 0) pos = hist[warp * E + e] + __popc(m & lt_mask);
-    __syncwarp();
-    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
-    __syncwarp();
-    if (a < end) {
-      inv[a] = pos;
-      if (pos >= 0) perm[pos] = a;
+  for (int base0 = beg; base0 < end; base0 += 32 * kPermU) {
+    int ev[kPermU];
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      const int a = base0 + 32 * u + lane;
+      ev[u] = (a < end) ? ids[a] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      if (base0 + 32 * u >= end) break;  // warp-uniform: past the chunk
+      const int a = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (a < end && (e < 0 || e >= E)) e = -1;
+      const int key = (e >= 0) ? e : (E + lane);
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      int pos = -1;
+      if (e >= 0) pos = hist[warp * E + e] + __popc(m & lt_mask);
+      __syncwarp();
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp();
+      if (a < end) {
+        inv[a] = pos;
+        if (pos >= 0) perm[pos] = a;
+      }
     }
   }
 }
