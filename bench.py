@@ -102,8 +102,8 @@ class ClockSampler:
 _TRAFFIC = {
     "decode": {"bytes": 249.97e6, "src": "gemv_lut.cu",
                "src_sha256": "b5d4dae93aec10a2191d557ae6ea818fae9193484cd77a022523784ce1b3cb08"},
-    "prefill_bf16": {"bytes": 2306.04e6, "src": "gemm_tmem.cu",
-                     "src_sha256": "64ec621e352148d220643305c5ca4c428b838c678578f1a42c7be658e7c1ff66"},
+    "prefill_bf16": {"bytes": 2312.48e6, "src": "gemm_tmem.cu",
+                     "src_sha256": "4292d89beb2abcaa3c62c7a8a09ab21dcc449f60c802d89fb86d8408498d6fa3"},
 }
 
 

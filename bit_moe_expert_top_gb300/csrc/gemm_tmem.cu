@@ -187,11 +187,19 @@ MOE_D void w2_decode_word(uint32_t w, uint32_t lanebase, uint32_t sc2, uint32_t*
   o[7] = bf16x2_mul(e3.y, sc2);
 }
 
-// SiLU from the hardware exponential and an approximate divide: within about
-// 1e-6 of the fp32 value before the epilogue rounds it to bf16 / E4M3 (the
-// exact-division form costs about a sixth of FC1's time here, the epilogue
-// being on the accumulator's critical path).
-MOE_D float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+// SiLU g / (1 + e^-g) from the hardware exponential and the hardware
+// reciprocal refined by one Newton-Raphson step on the quotient (q' = q +
+// r (g - q d), Markstein's correction): the approximate divide alone moved
+// some h across a bf16 rounding midpoint, the IEEE divide cost about a sixth
+// of FC1's time here (the epilogue is on the accumulator's critical path).
+// d is capped below infinity so that g < -88 gives a tiny value, not NaN.
+MOE_D float silu_fast(float g) {
+  const float d = fminf(1.0f + __expf(-g), 1e38f);
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+  const float q = g * r;
+  return fmaf(fmaf(-q, d, g), r, q);
+}
 
 // Two E4M3 bytes -> bf16x2 (exact: every E4M3 value is a bf16 value).
 MOE_D uint32_t e4m3x2_to_bf16x2(uint32_t two) {
