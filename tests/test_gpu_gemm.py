@@ -116,7 +116,8 @@ def test_gemm_prefill_bf16_full_size_sampled():
     _check_sampled("prefill_bf16", [0, 4099, 8191], mode=L.MODE_GEMM)
 
 
-@pytest.mark.parametrize("E,H,I,k,T", [(12, 512, 256, 4, 90), (8, 1024, 512, 8, 300), (5, 768, 384, 2, 77)])
+@pytest.mark.parametrize("E,H,I,k,T", [(12, 512, 256, 4, 90), (8, 1024, 512, 8, 300), (5, 768, 384, 2, 77),
+                                       (16, 512, 256, 2, 20)])  # the last: decode-sized groups, 32-token tiles
 def test_fp8_workspace_gemm_full_parity(E, H, I, k, T):
     """FP8-workspace experts on the tensor-core path: MXFP8-rounded bf16
     activation rows, E4M3 weights decoded into TMEM, FC1 writes h
