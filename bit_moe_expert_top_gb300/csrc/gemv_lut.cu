@@ -18,20 +18,19 @@
 // aligned shared-window address so that byte 1 of every lookup address is
 // free for the code byte (one PRMT builds the address).
 //
-// Work: units (permuted row p, K slice s, batch of 32 weight rows) in
+// Work: units (permuted row p, K slice s, batch of 16 weight rows) in
 // (p, s, batch) order, split into one contiguous range per CTA (one CTA per
 // SM).  A CTA walks its range segment by segment (one segment = one (p, s)
 // table) with 16 warps; a warp takes every 16th batch of the segment.  Per
-// batch a lane loads its word of 8 row quads straight from global memory
+// batch a lane loads its word of 4 row quads straight from global memory
 // (one 16-byte load per quad: the w2l layout puts word l of a quad's 4 rows
 // side by side) plus the 4 matching bf16 scales, and issues the loads of its
-// next batch while it consumes the current one, so about 100 KB per SM are in
-// flight.  (Bulk copies of a few KB into a shared ring stream far slower on
-// this part, and would also spend shared-memory bandwidth twice.)  A shuffle
-// reduce-scatter turns the 32 lanes x 32 rows of partials into one slice sum
-// per row and lane, which the warp stores to a global scratch with plain
-// stores: no atomics and no fences, so nothing ever waits for the loads in
-// flight.  A second, small kernel (launched as a programmatic dependent of
+// next batch while it consumes the current one.  (Bulk copies of a few KB
+// into a shared ring stream far slower on this part, and would also spend
+// shared-memory bandwidth twice.)  A shuffle reduce-scatter turns the 32
+// lanes x 16 rows of partials into one slice sum per row (held by two
+// lanes), which the warp stores to a global scratch with plain stores: no
+// atomics and no fences, so nothing ever waits for the loads in flight.  A second, small kernel (launched as a programmatic dependent of
 // the first) sums each row's slices in slice order (deterministic), applies
 // SwiGLU for FC1, rounds and stores.  Neither kernel waits on another CTA.
 #include <cuda_runtime.h>
@@ -44,8 +43,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kLutWarps = 16;
+constexpr int kLutWarps = 16;                // (20 or 24 warps with fewer registers each measured slower)
 constexpr int kLutThreads = kLutWarps * 32;
+constexpr int kBuildWarps = 16;               // warps that build a segment's tables
+constexpr int kBR = 16;                       // weight rows per batch (4 row quads; 32-row batches measured slower)
 constexpr int kSW = 512;                      // K elements per slice
 constexpr int kPrologue = 8192;               // shared bytes below the table window
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
@@ -71,10 +72,10 @@ struct LutParams {
   const int32_t* offsets;
   int E, N, K, R;           // R = weight rows per expert
   int NSL;                  // K slices
-  int NB;                   // row batches per permuted row (FC1: N/16, FC2: N/32)
+  int NB;                   // row batches per permuted row (FC1: N/8, FC2: N/16)
   int fc1;
   int* rows_hdr;            // [0]: selected rows; then prow[A]: permuted row of selected row i, or -1
-  float* scratch;           // [A][NB][NSL][32] per-slice row sums
+  float* scratch;           // [A][NB][NSL][kBR] per-slice row sums
   int A;                    // permuted rows the scratch covers
   void* out;
   int out_fmt;
@@ -243,9 +244,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   const int64_t slice_codes = static_cast<int64_t>(P.R) * (kSW / 4);
   const int64_t slice_scales = static_cast<int64_t>(P.R) * (kSW / 32);
 
-  uint4 v[8];
-  uint2 sc[8];
-  float2 acc[16];  // row pairs (2i, 2i+1) of the batch
+  uint4 v[4];
+  uint2 sc[4];
+  float2 acc[8];  // row pairs (2i, 2i+1) of the batch
 
   auto expert_of = [&](int psel) {  // largest e with pref[e] <= psel
     int lo = 0, hi = P.E;
@@ -256,10 +257,10 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     return lo;
   };
   // quad index (rows 4Q..4Q+3 of the expert) of quad q of batch rb: FC1
-  // batches are 16 gate rows then the 16 matching up rows
+  // batches are 8 gate rows then the 8 matching up rows
   auto quad_of = [&](int rb, int q) -> uint32_t {
-    if (fc1) return static_cast<uint32_t>(q < 4 ? rb * 4 + q : (P.N >> 2) + rb * 4 + (q - 4));
-    return static_cast<uint32_t>(rb * 8 + q);
+    if (fc1) return static_cast<uint32_t>(q < 2 ? rb * 2 + q : (P.N >> 2) + rb * 2 + (q - 2));
+    return static_cast<uint32_t>(rb * 4 + q);
   };
   // this lane's code / scale addresses in slice s of expert e
   auto codes_at = [&](int e, int sl) { return P.codes + e * mat_codes + sl * slice_codes + lane * 16; };
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   };
   auto issue = [&](const uint8_t* gc, const uint8_t* gs, int rb) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const uint32_t Q = quad_of(rb, q);
       v[q] = ldg_stream(gc + Q * 512u);
       sc[q] = ldg_stream2(gs + Q * 128u);
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     // and code bytes b in [64*(w>>2), +64); lane l is byte position 4l + j
     cp_async_wait1();  // this segment's activations have landed (the next one's may be in flight)
     __syncthreads();  // nobody still reads the previous segment's tables
-    if (valid) {
+    if (valid && warp < kBuildWarps) {
       const int j = warp & 3, bq = warp >> 2;
       const uint2 xv = *reinterpret_cast<const uint2*>(xbuf + ((seg - seg_first) & 1) * kSW + 16 * lane + 4 * j);
       const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
       }
       if (valid) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           const uint4 w4 = v[q];
           const uint2 s4 = sc[q];
           acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
@@ -414,17 +415,18 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
             sc[q] = ldg_stream2(ns + Q * 128u);
           }
         }
-        // ---- reduce-scatter: afterwards lane l holds the slice sum of batch row l
-        rs_level2<8>(acc, lane, 16);
-        rs_level2<4>(acc, lane, 8);
-        rs_level2<2>(acc, lane, 4);
-        rs_level2<1>(acc, lane, 2);
-        const bool odd = (lane & 1) != 0;
-        const float keep = odd ? acc[0].y : acc[0].x;
-        const float send = odd ? acc[0].x : acc[0].y;
-        const float sum = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        // ---- reduce-scatter: afterwards lanes 2r and 2r + 1 hold the slice
+        // sum of batch row r
+        rs_level2<4>(acc, lane, 16);
+        rs_level2<2>(acc, lane, 8);
+        rs_level2<1>(acc, lane, 4);
+        const bool hi = (lane & 2) != 0;
+        const float keep = hi ? acc[0].y : acc[0].x;
+        const float send = hi ? acc[0].x : acc[0].y;
+        float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         const size_t cell = static_cast<size_t>(p) * NB + rb;
-        __stcg(P.scratch + (cell * NSL + s) * 32 + lane, sum);
+        if ((lane & 1) == 0) __stcg(P.scratch + (cell * NSL + s) * kBR + (lane >> 1), sum);
       } else if (more) {
         issue(nc, ns, rbn);
       }
@@ -459,20 +461,20 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
     const int p = __ldcg(P.rows_hdr + 1 + i);
     if (p < 0) continue;
     float t;
-    if (P.fc1) {  // batch n/16: lanes 0..15 gate rows, 16..31 the matching up rows
-      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * 32 + (n & 15);
+    if (P.fc1) {  // batch n/8: rows 0..7 gate rows, 8..15 the matching up rows
+      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 3)) * NSL * kBR + (n & 7);
       float g = 0.f, u = 0.f;
 #pragma unroll 4
       for (int q = 0; q < NSL; ++q) {
-        g += __ldcg(sp + q * 32);
-        u += __ldcg(sp + q * 32 + 16);
+        g += __ldcg(sp + q * kBR);
+        u += __ldcg(sp + q * kBR + 8);
       }
       t = silu_f32(g) * u;
     } else {
-      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 5)) * NSL * 32 + (n & 31);
+      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * kBR + (n & 15);
       t = 0.f;
 #pragma unroll 4
-      for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * 32);
+      for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * kBR);
     }
     const size_t o = static_cast<size_t>(p) * P.N + n;
     if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
@@ -484,11 +486,11 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
 
 // Scratch of the table GEMV: a row header (the selected-row count, then the
 // permuted row of each selected row; 256-byte padded) and the per-slice row
-// sums [rows][NB][NSL][32] (fp32).  Everything is written before it is read;
-// no initial contents needed.  NB = N/16 batches for FC1 (16 gate + 16 up
-// rows each), N/32 for FC2.
+// sums [rows][NB][NSL][kBR] (fp32).  Everything is written before it is read;
+// no initial contents needed.  NB = N/8 batches for FC1 (8 gate + 8 up rows
+// each), N/16 for FC2.
 static void lut_geometry(int stage, int N, int K, int& nb, int& nsl) {
-  nb = stage == MOE_STAGE_FC1_SWIGLU ? N / 16 : N / 32;
+  nb = stage == MOE_STAGE_FC1_SWIGLU ? N / 8 : N / 16;
   nsl = K / kSW;
 }
 
@@ -498,14 +500,14 @@ size_t lut_workspace_bytes(int stage, int rows, int N, int K) {
   int nb, nsl;
   lut_geometry(stage, N, K, nb, nsl);
   if (nsl == 0 || rows <= 0) return 0;
-  return lut_header_bytes(rows) + static_cast<size_t>(rows) * nb * nsl * 32 * sizeof(float);
+  return lut_header_bytes(rows) + static_cast<size_t>(rows) * nb * nsl * kBR * sizeof(float);
 }
 
 int lut_workspace_rows(int stage, size_t bytes, int N, int K) {
   int nb, nsl;
   lut_geometry(stage, N, K, nb, nsl);
   if (nsl == 0) return 0;
-  const size_t per = static_cast<size_t>(nb) * nsl * 32 * sizeof(float) + sizeof(int);
+  const size_t per = static_cast<size_t>(nb) * nsl * kBR * sizeof(float) + sizeof(int);
   int64_t rows = static_cast<int64_t>(bytes / per);
   if (rows > 0x7ffffffe) rows = 0x7ffffffe;
   while (rows > 0 && lut_workspace_bytes(stage, static_cast<int>(rows), N, K) > bytes) --rows;
