@@ -157,6 +157,26 @@ def build_workload(name, layers, batches, device, tokens=None):
     return w, mls, xs, lgs
 
 
+# --------------------------------------------------------------------------- ranks
+def max_over_ranks(x, device):
+    """The largest x over the ranks of the default process group (x itself
+    with one rank): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(steps, tokens_per_step, world, seconds):
+    """Whole-job throughput: every rank runs `steps` steps of
+    `tokens_per_step` tokens (replicas, weak scaling) in `seconds` (the
+    slowest rank's time)."""
+    return steps * tokens_per_step * world / seconds
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -252,13 +272,8 @@ def run_gpu(args):
     A = w.A
     tot_flops = args.steps * A * flops_per_assignment(w)
 
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    tokens = args.steps * w.T * world
-    value = tokens / (t_max / 1e3)
+    t_max = max_over_ranks(ms, device)
+    value = job_tokens_per_s(args.steps, w.T, world, t_max / 1e3)
 
     peaks = _peaks()
     decode = w.T * w.k < 4096
@@ -347,8 +362,8 @@ def run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world):
         g.replay()
         out_h.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    return {"value": round(steps * w.T * world / dt, 1), "unit": "tokens/s",
+    dt = max_over_ranks(time.perf_counter() - t0, device)
+    return {"value": round(job_tokens_per_s(steps, w.T, world, dt), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(hx[0].numel() * 2 + hl[0].numel() * 4),
             "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps}
 
