@@ -216,9 +216,14 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * Modes: GEMV = CUDA-core kernels (2-bit with a workspace and K a multiple
  * of 512: shared-memory partial-sum tables with K split in 512-element
  * slices over CTAs; otherwise, and for MXFP4 / FP8: register decode); GEMM =
- * tcgen05 tensor-core kernel (2-bit weights, bf16 activations already
- * permuted: act_row must be NULL); AUTO = GEMM when act_row is NULL,
- * act_rows >= 2048 and the shape is supported, else GEMV.
+ * tcgen05 tensor-core kernel with the dequantised weights in tensor memory,
+ * for 2-bit, MXFP4 and FP8-workspace weights, on bf16 activations already
+ * permuted (act_row must be NULL), K a multiple of 64, N a multiple of 128
+ * (FC1) or 256 (FC2); 2-bit FC2 with N a multiple of 128 only goes to an
+ * older tcgen05 kernel with the weights in shared memory; a call that fits
+ * neither runs as GEMV (MXFP8_BF16 output excepted: MOE_ERR_UNSUPPORTED).
+ * AUTO = GEMM when act_row is NULL, act_rows >= 2048 and the shape is
+ * supported, else GEMV.
  *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
  *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
  *        256-byte aligned.  Its contents on entry do not matter (every value
