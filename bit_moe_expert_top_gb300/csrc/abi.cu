@@ -26,7 +26,9 @@ int cuda_status(cudaError_t e, const char* where) {
     return MOE_OK;
   }
   std::snprintf(g_err, sizeof(g_err), "%s: %s", where, cudaGetErrorString(e));
-  return MOE_ERR_CUDA;
+  // the dispatchers answer cudaErrorNotSupported for a combination no kernel
+  // takes (e.g. MXFP8_BF16 output off the tensor-core path)
+  return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

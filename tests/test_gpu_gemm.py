@@ -139,3 +139,20 @@ def test_gemm_decode_sized_groups_full_parity():
     """Few tokens per expert: 32-token tiles, most of each tile past the group end."""
     w = synth.get_workload("tiny").replace(E=64, H=512, I=256, k=2, T=40, logits="uniform")
     _check_full(w, mode=L.MODE_GEMM)
+
+
+def test_mxfp8_bf16_output_off_the_tensor_path_is_unsupported():
+    """FC1's MXFP8_BF16 output exists only on the tensor-core path: asked of
+    the GEMV it is refused as unsupported, not run and not a CUDA error."""
+    w = synth.get_workload("tiny")
+    ml, _, _ = make_layer(w, mode=L.MODE_GEMV)
+    b = ml.buffers(w.T)
+    x = dev(synth.make_x(w).view(np.int16))
+    L.moe_route(dev(synth.make_logits(w)), w.k, b.ids, b.w, b.dev_err)
+    L.moe_permute(b.ids, w.E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+    h = torch.empty((w.T * w.k, w.I), dtype=torch.int16, device=DEV)
+    with pytest.raises(L.MoEError) as ei:
+        L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, ml.c1k, ml.s1k, b.offsets, w.E, w.I, w.H, h,
+                    L.FMT_MXFP8_BF16, act_row=b.perm, act_row_div=w.k, mode=L.MODE_GEMV, ws=b.ws,
+                    dev_err=b.dev_err)
+    assert ei.value.code == L.MOE_ERR_UNSUPPORTED
