@@ -103,7 +103,7 @@ _TRAFFIC = {
     "decode": {"bytes": 250.31e6, "src": "gemv_lut.cu",
                "src_sha256": "8415d1fcfcc286234ba3f206d24193dda346e22e404a9c5f80995019f668640f"},
     "prefill_bf16": {"bytes": 2312.48e6, "src": "gemm_tmem.cu",
-                     "src_sha256": "4292d89beb2abcaa3c62c7a8a09ab21dcc449f60c802d89fb86d8408498d6fa3"},
+                     "src_sha256": "c76ee4c57ee6b3e3352415b0bf3e9cc8766c3baf143397685942f1bdf29fe09e"},
 }
 
 

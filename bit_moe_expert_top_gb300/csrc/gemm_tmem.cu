@@ -8,19 +8,30 @@
 // thread of the epilogue holds g and u of the same output; FC2: two
 // consecutive 128-row blocks).  TMEM lane = weight row, column = token.
 //
-//   warp 0      TMA: token tiles [NT rows x 64 K] bf16 (128-byte swizzle)
-//   warp 1      TMEM allocation; one thread issues tcgen05.mma kind::f16
-//               (A from TMEM, B = token tile in shared memory, M=128, N=NT,
-//               K=16) for both blocks, tcgen05.commit frees the stage
+//   warp 0      TMA: token tiles [NT rows x 64 K] bf16 (128-byte swizzle),
+//               one per A stage
+//   warps 1, 15 MMA issue, one weight block each (warp 1 also allocates
+//               TMEM): tcgen05.mma kind::f16, A from TMEM, B = token tile in
+//               shared memory, M=128, N = the tile's tokens rounded up to 16,
+//               K=16; tcgen05.commit frees the block's A stage.  One
+//               thread's MMAs run back to back (~100-120 cycles each at N <=
+//               128, measured), so two issuers keep the tensor pipe fed.
+//   warp 14     TMA: the weight ring, both blocks' share of each 64-K stage
+//               six stages ahead (2-bit codes + bf16 scales, E4M3 bytes, or
+//               E2M1 nibbles; 64- / 32-byte swizzles so the decode warps'
+//               shared loads are conflict-free)
 //   warps 2-9   weight decode: each thread owns one weight row of one block
 //               (its TMEM lane) and per 64-K stage turns the row's codes into
 //               64 bf16 values in registers and writes them to its lane of
-//               the stage's A columns with tcgen05.st.  The decoded weights
-//               never touch shared memory, so the tensor core keeps the
-//               shared-memory bandwidth for the token tiles.
+//               the stage's A columns with tcgen05.st, then hands the ring
+//               slot back (only after that store: it consumed every word read
+//               from the slot).  The decoded weights never touch shared
+//               memory, so the tensor core keeps the shared-memory bandwidth
+//               for the token tiles.
 //   warps 10-13 epilogue: tcgen05.ld of D0/D1 (a warp reads its 32 lanes),
-//               SwiGLU for FC1, rounding, stores (32 lanes = 32 consecutive
-//               outputs of one token row: coalesced)
+//               releases each block's accumulator after its last column
+//               chunk is read, SwiGLU for FC1 / MXFP8 rounding, rounding,
+//               then a shared staging tile and 16-byte row stores
 //
 // MXFP4 decode (delta-cache experts): a per-lane 256-entry byte -> 2 bf16
 // E2M1 table (same window), scaled by 2^(E8M0-127) as bf16 (exact).
