@@ -108,11 +108,13 @@ def test_mixed_decode_full_size_sampled_tensor_path():
     _check_sampled("mixed_decode", [3, 60], mode=L.MODE_AUTO)
 
 
-@pytest.mark.parametrize("name,mode", [("mixed_decode", L.MODE_AUTO), ("prefill_fp8", L.MODE_GEMM)])
+@pytest.mark.parametrize("name,mode", [("mixed_decode", L.MODE_AUTO), ("prefill_fp8", L.MODE_GEMM),
+                                       ("decode", L.MODE_GEMV)])
 def test_layer_repeat_bit_identical(name, mode):
-    """Several steps on the same inputs give the same bits: the TMA weight
+    """Several steps on the same inputs give the same bits (the table GEMV
+    adds its slice sums in slice order; the tensor-core matmul's TMA weight
     rings (MXFP4 nibbles, E4M3 bytes, 2-bit codes) hand a slot back to the
-    producer only after its words are consumed.  Releasing it right after the
+    producer only after its words are consumed).  Releasing it right after the
     shared-memory reads were issued let the next TMA overwrite the slot first
     on some steps (seen as 3-10 differing rows of h on the mixed layer)."""
     w = synth.get_workload(name)
