@@ -9,8 +9,15 @@ format.  Inputs are larger than L2: step i runs on layer (i mod 4) of four
 distinct weight sets (4 x 3.02 GB) with its own token batch, so no step finds
 the previous step's weights in the 129 MB L2.
 
+The same run also times the other workloads of the metric, each on its own
+layer of weights, as sub-records of the line (``workloads``): prefill_bf16
+(8192 tokens, 2-bit experts on the tensor cores), prefill_fp8 (16384 tokens,
+MXFP4 experts through the FP8 workspace) and mixed_decode (64 tokens, 2-bit
+experts plus 64 MXFP4 delta-cache entries).
+
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
-instead (a bounded sample of the same workload on the host cores).
+instead: whole layer steps of the same workload, its tokens split over one
+process per host core.
 """
 from __future__ import annotations
 
@@ -32,12 +39,20 @@ METRIC = "MoE layer tokens/s; decode weight-stream GB/s and prefill TFLOP/s vs G
 
 
 def _peaks():
+    """Roofline denominators: the measured HBM copy rate and cuBLAS bf16 rates
+    of this GPU model (burst: a kernel timed alone or in a short region;
+    sustained: seconds-long loops), else the fallback figures.  FP8 has no
+    measured figure: 2x the bf16 burst rate (the nominal dense FP8 / BF16
+    ratio of the part)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+        pk = {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+              "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    else:
+        pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+    pk["fp8_tflops"] = 2.0 * pk["bf16_tflops"]
+    return pk
 
 
 # --------------------------------------------------------------------------- clocks
@@ -55,7 +70,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -178,24 +193,23 @@ def job_tokens_per_s(steps, tokens_per_step, world, seconds):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def run_gpu(args):
+def _decode_like(w):
+    return w.T * w.k < 4096
+
+
+def measure(name, args, device, world, layers, *, clocks=None, tokens=None):
+    """Time `steps` layer steps of workload `name` from a CUDA graph.
+
+    Returns the record of the workload (tokens/s, ms per step, the roofline
+    of the expert matmuls from per-launch CUDA-event durations, e2e through
+    the API) and the objects the caller may reuse."""
     import torch
     import torch.distributed as dist
 
     from bit_moe_expert_top_gb300 import _lib as L
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    L.lib()
-
-    layers = args.layers
     batches = max(layers, 4)
-    w, mls, xs_h, lgs_h = build_workload(args.workload, layers, batches, device, args.tokens)
+    w, mls, xs_h, lgs_h = build_workload(name, layers, batches, device, tokens)
     xs = [torch.from_numpy(x.view(np.int16)).to(device) for x in xs_h]
     lgs = [torch.from_numpy(lg).to(device) for lg in lgs_h]
     bufs = [ml.buffers(w.T) for ml in mls]
@@ -213,15 +227,16 @@ def run_gpu(args):
         off = bufs[li].offsets.cpu().numpy()
         work_bytes[i] = mls[li].touched_weight_bytes(off)
         if L.moe_get_error(bufs[li].dev_err) != 0:
-            raise RuntimeError("device error flags set during warm-up")
+            raise RuntimeError(f"{name}: device error flags set during warm-up")
 
-    # ---- the timed steps run from a CUDA graph: S consecutive steps (layer
-    # i mod L, batch i mod B) captured once; the timed region replays it K/S
-    # times.  A second graph of the same steps carries an event pair around
-    # every expert matmul (the roofline's per-kernel durations); it is
-    # replayed after the timed region, because event nodes between kernels
-    # would serialise the programmatic launches of the timed graph.
-    S = max(d for d in range(1, min(args.steps, 64) + 1) if args.steps % d == 0)
+    # The timed steps run from a CUDA graph: S consecutive steps (layer i mod
+    # L, batch i mod B) captured once, replayed K/S times.  A second graph of
+    # the same steps carries an event pair around every expert matmul (the
+    # roofline's per-kernel durations); it is replayed after the timed
+    # region, because event nodes between kernels would serialise the
+    # programmatic launches of the timed graph.
+    steps = args.steps
+    S = max(d for d in range(1, min(steps, 64) + 1) if steps % d == 0)
     g = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(g):
@@ -241,26 +256,32 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
+    # Clock samples: nvidia-smi cannot sample a region of a few ms, so the
+    # sampler runs over a window of ~1 s of the same replays that contains
+    # the timed region (replays before and after it keep the GPU under load).
+    if clocks is not None:
+        clocks.start()
+        _spin(g, 0.5)
     stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps // S):
+    for _ in range(steps // S):
         g.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    clk = None
+    if clocks is not None:
+        _spin(g, 0.5)
+        clk = clocks.stop()
+        clk["window"] = "~1 s of the same graph replays around the timed region"
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
     for _ in range(2):  # the event graph: the last replay's durations are read below
         g_ev.replay()
     torch.cuda.synchronize()
 
-    # per-launch durations of the expert matmul kernels (the dominant ones),
-    # from the event pairs of the event graph's last replay
     mm_ms = sum(a.elapsed_time(b) for _, a, b in graph_ev)
     n_mm = len(graph_ev)
     per_label = {}
@@ -268,49 +289,108 @@ def run_gpu(args):
         per_label.setdefault(label, []).append(a.elapsed_time(b) * 1e3)
     kernels_us = {k: round(sum(v) / len(v), 2) for k, v in per_label.items()}
     graph_bytes = sum(work_bytes[i % batches] for i in range(S))
-    tot_bytes = sum(work_bytes[i % batches] for i in range(args.steps))
+    tot_bytes = sum(work_bytes[i % batches] for i in range(steps))
     A = w.A
-    tot_flops = args.steps * A * flops_per_assignment(w)
-
+    tot_flops = steps * A * flops_per_assignment(w)
     t_max = max_over_ranks(ms, device)
-    value = job_tokens_per_s(args.steps, w.T, world, t_max / 1e3)
+    value = job_tokens_per_s(steps, w.T, world, t_max / 1e3)
 
     peaks = _peaks()
-    decode = w.T * w.k < 4096
-    traffic = _traffic(w) if args.tokens is None else None
+    decode = _decode_like(w)
+    traffic = _traffic(w) if tokens is None else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": "expert matmuls (moe_w2_mm FC1+FC2)", "peak_src": peaks["src"],
+                "kernel": "expert matmuls (FC1+FC2 launches of the step)",
+                "peak_src": f"{peaks['src']} HBM copy rate",
                 "bytes_per_launch": round(graph_bytes / n_mm), "launch_us": round(mm_ms / n_mm * 1e3, 2)}
     else:
+        fp8 = w.weights == "mxfp4"
+        peak = peaks["fp8_tflops"] if fp8 else peaks["bf16_tflops"]
         achieved = S * A * flops_per_assignment(w) / (mm_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": traffic,
-                "kernel": "expert matmuls", "peak_src": peaks["src"], "launch_us": round(mm_ms / n_mm * 1e3, 2)}
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "expert matmuls (FC1+FC2 launches of the step)",
+                "peak_src": (f"2 x {peaks['src']} bf16 burst rate (nominal FP8/BF16 ratio)" if fp8 else
+                             f"{peaks['src']} bf16 burst rate (the timed region is well under a second)"),
+                "flops_per_step": A * flops_per_assignment(w), "launch_us": round(mm_ms / n_mm * 1e3, 2),
+                "step_frac": round(tot_flops / (t_max / 1e3) / 1e12 / peak, 4)}
+    rec = {"value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(t_max / steps, 5),
+           "config": {"workload": name, "E": w.E, "H": w.H, "I": w.I, "k": w.k, "T": w.T, "weights": w.weights,
+                      "l2": (f"inputs larger than L2: {layers} distinct layers of weights rotated per step"
+                             if layers > 1 else "inputs larger than L2: one layer of weights "
+                             f"({_layer_gb(mls[0]):.1f} GB) and 4 token batches rotated per step"),
+                      "launch": f"CUDA graph of {S} steps replayed {steps // S} times"},
+           "weight_stream_gbs": round(tot_bytes / (t_max / 1e3) / 1e9 / world, 1) if decode else None,
+           "tflops": round(tot_flops / (t_max / 1e3) / 1e12, 2),
+           "roofline": roof, "kernels_us": kernels_us,
+           "gpu_launches": steps * launches_per_step(mls[0], w.T)}
+    if clk is not None:
+        rec["clocks"] = clk
+    if not args.no_e2e:
+        rec["e2e"] = run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world)
+    del g, g_ev, graph_ev
+    return rec, (w, mls, bufs)
 
-    # ---------------- end to end: host buffers through the public API
-    e2e = run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world)
 
+def _spin(g, seconds):
+    import torch
+    t = time.perf_counter()
+    while time.perf_counter() - t < seconds:
+        g.replay()
+        torch.cuda.synchronize()
+
+
+def _layer_gb(ml):
+    n = 0
+    for a in ("c1k", "s1k", "c2k", "s2k", "q1", "e1", "q2", "e2"):
+        t = getattr(ml, a, None)
+        if t is not None:
+            n += t.numel() * t.element_size()
+    return n / 1e9
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from bit_moe_expert_top_gb300 import _lib as L
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    L.lib()
+
+    head, _ = measure(args.workload, args, device, world, args.layers, clocks=ClockSampler(local),
+                      tokens=args.tokens)
+    subs = {}
+    if args.sub and args.tokens is None:
+        for name in args.sub.split(","):
+            if name and name != args.workload:
+                torch.cuda.empty_cache()
+                rec, objs = measure(name, args, device, world, 1)
+                del objs
+                subs[name] = rec
+                torch.cuda.empty_cache()
+    cfg = dict(head["config"], parallelism=f"replicas{world}")
     res = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "E": w.E, "H": w.H, "I": w.I, "k": w.k, "T": w.T,
-                   "weights": w.weights, "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: {layers} distinct layers of weights rotated per step",
-                   "launch": f"CUDA graph of {S} steps replayed {args.steps // S} times"},
-        "weight_stream_gbs": round(tot_bytes / (t_max / 1e3) / 1e9 / world, 1) if decode else None,
-        "tflops": round(tot_flops / (t_max / 1e3) / 1e12, 2),
-        "roofline": roof,
-        "kernels_us": kernels_us,
-        "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step(mls[0], w.T),
-        "clocks": clk,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "weight_stream_gbs": head["weight_stream_gbs"], "tflops": head["tflops"],
+        "roofline": head["roofline"], "kernels_us": head["kernels_us"], "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values()),
+        "clocks": head.get("clocks"),
     }
+    if subs:
+        res["workloads"] = subs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample)
+        res["cpu_baseline"] = cpu_baseline(args.workload, steps=1)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -333,9 +413,12 @@ def launches_per_step(ml, T):
 
 
 def run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world):
-    """The same steps through the public API with the token batch copied in
-    from pinned host memory and the layer output read back, every step inside
-    the timed region (the step itself replays a captured one-step graph)."""
+    """The same steps end to end through the library's API, each inside the
+    timed region: the token batch and the router logits copied in from pinned
+    host memory, the layer step as its chain of C-ABI calls (route, permute,
+    the expert matmuls, combine; ``MoELayer.step``), and the layer output read
+    back to pinned host memory.  `graph` repeats the measurement with the
+    step replayed from a captured one-step graph instead of the calls."""
     import torch
     steps = max(1, min(args.steps, args.e2e_steps))
     layers = len(mls)
@@ -345,8 +428,24 @@ def run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world):
     dx = [torch.empty_like(hx[0], device=device) for _ in range(layers)]
     dl = [torch.empty_like(hl[0], device=device) for _ in range(layers)]
     out_h = torch.empty(bufs[0].out.shape, dtype=bufs[0].out.dtype).pin_memory()
-    graphs = []
+
+    def eager(i):
+        li = i % layers
+        dx[li].copy_(hx[i % batches], non_blocking=True)
+        dl[li].copy_(hl[i % batches], non_blocking=True)
+        out = mls[li].step(dx[li], dl[li], bufs[li])
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(min(steps, 3)):  # warm: host-side caches of the calls
+        eager(i)
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        eager(i)
+    torch.cuda.synchronize()
+    dt = max_over_ranks(time.perf_counter() - t0, device)
+
+    graphs = []
     for li in range(layers):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -362,66 +461,124 @@ def run_e2e(args, w, mls, bufs, xs_h, lgs_h, device, world):
         g.replay()
         out_h.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
-    dt = max_over_ranks(time.perf_counter() - t0, device)
+    dtg = max_over_ranks(time.perf_counter() - t0, device)
     return {"value": round(job_tokens_per_s(steps, w.T, world, dt), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(hx[0].numel() * 2 + hl[0].numel() * 4),
-            "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps}
+            "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps,
+            "path": "pinned host -> device copies, the layer's C-ABI calls, device -> pinned host, per step",
+            "graph": {"value": round(job_tokens_per_s(steps, w.T, world, dtg), 1), "unit": "tokens/s",
+                      "path": "as above with the step replayed from a captured one-step CUDA graph"}}
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def cpu_baseline(workload, sample_tokens):
-    """Time the oracle on a bounded sample in a fresh single-threaded process."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--cpu-sample", str(sample_tokens)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
-    if r.returncode != 0:
-        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                "sample": f"failed: {r.stderr.strip()[-200:]}"}
-    return json.loads(r.stdout.strip().splitlines()[-1])
+# The oracle (numpy, float64) timed on the host cores: a layer step's tokens
+# are split over one process per core (at most one per token); each process
+# prepares its experts' stored weights untimed, then every step starts on a
+# barrier and the step's time is the slowest process's.
 
-
-def oracle_sample(workload, ntok):
+def _oracle_prepare(workload, tokens):
     from bit_moe_expert_top_gb300 import synth
+    from oracle import codecs as C
     from oracle import moe as M
     w = synth.get_workload(workload)
     x = synth.make_x(w, 0)
     logits = synth.make_logits(w, 0, x_bits=x)
-    tokens = list(range(min(ntok, w.T)))
+    ids = M.route(logits, w.k)[0][tokens]
+    raw = {}
     if w.weights == "w2":
-        ids = M.route(logits, w.k)[0][tokens]
-        raw = {}
         for e in np.unique(ids):
             raw[int(e)] = synth.make_w2_expert(w, int(e), 0, 0)
 
         def acc(e):
             c1, s1, c2, s2 = raw[e]
-            from oracle import codecs as C
             return C.decode_w2(c1, s1), C.decode_w2(c2, s2)
         prof = "bf16"
     elif w.weights == "mixed":
         slot = synth.hot_experts(w, 0)
-        from oracle import codecs as C
+        for e in np.unique(ids):
+            raw[int(e)] = (synth.make_mxfp4_expert(w, int(slot[e]), 0, 0) if slot[e] >= 0 else
+                           synth.make_w2_expert(w, int(e), 0, 0))
 
         def acc(e):
+            a, b, c, d = raw[e]
             if slot[e] >= 0:
-                q1, s1, q2, s2 = synth.make_mxfp4_expert(w, int(slot[e]), 0, 0)
-                return C.decode_mxfp4(q1, s1), C.decode_mxfp4(q2, s2)
-            c1, s1, c2, s2 = synth.make_w2_expert(w, e, 0, 0)
-            return C.decode_w2(c1, s1), C.decode_w2(c2, s2)
+                return C.decode_mxfp4(a, b), C.decode_mxfp4(c, d)
+            return C.decode_w2(a, b), C.decode_w2(c, d)
         prof = "bf16"
     else:
-        from oracle import codecs as C
+        for e in np.unique(ids):
+            raw[int(e)] = synth.make_mxfp4_expert(w, int(e), 0, 0)
 
         def acc(e):
-            q1, s1, q2, s2 = synth.make_mxfp4_expert(w, e, 0, 0)
+            q1, s1, q2, s2 = raw[e]
             return C.e4m3_value(C.mxfp4_to_e4m3(q1, s1)), C.e4m3_value(C.mxfp4_to_e4m3(q2, s2))
         prof = "fp8"
-    t0 = time.perf_counter()
-    M.layer(x, logits, w.k, acc, profile=prof, tokens=tokens)
-    dt = time.perf_counter() - t0
-    return {"value": round(len(tokens) / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(tokens)} of {w.T} tokens of one {workload} layer (routing over all tokens), "
-                      f"{dt:.1f} s, numpy fp64, 1 thread"}
+    return w, x, logits, acc, prof
+
+
+def _oracle_proc(workload, tokens, steps, barrier, conn):
+    from oracle import moe as M
+    w, x, logits, acc, prof = _oracle_prepare(workload, tokens)
+    for _ in range(steps):
+        barrier.wait()
+        t0 = time.perf_counter()
+        M.layer(x, logits, w.k, acc, profile=prof, tokens=tokens)
+        conn.send(time.perf_counter() - t0)
+    conn.close()
+
+
+def oracle_steps(workload, steps, max_tokens=None):
+    """Run `steps` oracle steps of `workload` (all its tokens, or the first
+    `max_tokens`) on the host cores; returns (per-step seconds, processes,
+    host cores, tokens per step)."""
+    import multiprocessing as mp
+    from bit_moe_expert_top_gb300 import synth
+    w = synth.get_workload(workload)
+    ntok = w.T if max_tokens is None else min(w.T, max_tokens)
+    cores = len(os.sched_getaffinity(0))
+    procs = max(1, min(cores, ntok))
+    chunks = [c.tolist() for c in np.array_split(np.arange(ntok), procs)]
+    ctx = mp.get_context("spawn")
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        barrier = ctx.Barrier(procs)
+        pipes, ps = [], []
+        for c in chunks:
+            rd, wr = ctx.Pipe(duplex=False)
+            p = ctx.Process(target=_oracle_proc, args=(workload, c, steps, barrier, wr), daemon=True)
+            p.start()
+            wr.close()
+            pipes.append(rd)
+            ps.append(p)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    times = []
+    for _ in range(steps):
+        times.append(max(rd.recv() for rd in pipes))
+    for p in ps:
+        p.join(timeout=60)
+    return times, procs, cores, ntok
+
+
+def cpu_baseline(workload, steps=1):
+    """The oracle on the host cores, whole layer steps of `workload`."""
+    from bit_moe_expert_top_gb300 import synth
+    w = synth.get_workload(workload)
+    max_tok = w.T if _decode_like(w) else 16   # prefill steps: a bounded token sample
+    try:
+        times, procs, cores, ntok = oracle_steps(workload, steps, max_tok)
+    except Exception as e:  # reported, not fatal to the GPU line
+        return {"value": None, "unit": "tokens/s", "cores": 0, "kind": "oracle", "sample": f"failed: {e}"}
+    t = statistics.median(times)
+    return {"value": round(ntok / t, 4), "unit": "tokens/s", "cores": procs, "host_cores": cores, "kind": "oracle",
+            "sample": (f"{'all ' if ntok == w.T else ''}{ntok} of {w.T} tokens of one {workload} layer per step, "
+                       f"split over {procs} processes (numpy fp64, 1 BLAS thread each), median of {steps} "
+                       f"step(s), {t:.2f} s per step")}
 
 
 def run_reference(args):
@@ -431,42 +588,41 @@ def run_reference(args):
         return
     from bit_moe_expert_top_gb300 import synth
     w = synth.get_workload(args.workload)
-    vals = []
-    for _ in range(args.warmup + args.steps):
-        vals.append(cpu_baseline(args.workload, args.cpu_sample))
-    timed = [v for v in vals[args.warmup:] if v.get("value")]
-    value = statistics.median([v["value"] for v in timed]) if timed else None
-    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(1e3 * w.T / value, 3) if value else None, "higher_is_better": True,
+    max_tok = w.T if _decode_like(w) else 16
+    times, procs, cores, ntok = oracle_steps(args.workload, args.warmup + args.steps, max_tok)
+    timed = times[args.warmup:]
+    t = statistics.median(timed)
+    value = ntok / t
+    sample = (f"{'all ' if ntok == w.T else ''}{ntok} of {w.T} tokens of one {args.workload} layer per step, "
+              f"split over {procs} processes (numpy fp64, 1 BLAS thread each)")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": args.workload, "E": w.E, "H": w.H, "I": w.I, "k": w.k, "T": w.T,
-                      "weights": w.weights},
-           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                            "sample": timed[0]["sample"] if timed else "failed"},
-           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                      "weights": w.weights, "tokens_per_step": ntok},
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": procs, "host_cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8"])
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,mixed_decode",
+                    help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")
-    ap.add_argument("--e2e-steps", type=int, default=500)
-    ap.add_argument("--cpu-sample", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
-    if args.oracle_sample:
-        print(json.dumps(oracle_sample(args.oracle_sample, args.cpu_sample)))
-        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -18,13 +18,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_WS_SMALL, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3, 4
-DEVERR_BAD_ID, DEVERR_NAN_LOGIT, DEVERR_NAN_SCALE, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 1, 2, 4, 8, 16
+DEVERR_BAD_ID, DEVERR_NAN_LOGIT, DEVERR_NAN_SCALE, DEVERR_TIMEOUT, DEVERR_OVERFLOW, DEVERR_LAUNCH = 1, 2, 4, 8, 16, 32
 FMT_NONE, FMT_BF16, FMT_F32, FMT_MXFP8, FMT_MXFP8_BF16 = 0, 1, 2, 3, 4
 STAGE_FC1_SWIGLU, STAGE_FC2 = 1, 2
 MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
 
 # every entry point declared in include/moe.h
-EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_route", "moe_permute_workspace_size",
+EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wait_limit",
+           "moe_check_bounded_wait", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
            "moe_combine"]
@@ -42,6 +43,8 @@ _SIGS = {
     "moe_version": (_I, []),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_error": (_I, [_P, _P, _P]),
+    "moe_set_wait_limit": (_L, [_L]),
+    "moe_check_bounded_wait": (_I, [_L, _P, _P]),
     "moe_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_permute_workspace_size": (_S, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _S, _P, _P]),
@@ -107,6 +110,14 @@ def moe_get_error(dev_err: torch.Tensor, stream=None) -> int:
     bits = ctypes.c_uint32(0)
     _check(lib().moe_get_error(_ptr(dev_err), _stream(stream), ctypes.addressof(bits)))
     return int(bits.value)
+
+
+def moe_set_wait_limit(cycles: int) -> int:
+    return int(lib().moe_set_wait_limit(cycles))
+
+
+def moe_check_bounded_wait(cycles, dev_err, stream=None):
+    _check(lib().moe_check_bounded_wait(cycles, _ptr(dev_err), _stream(stream)))
 
 
 def moe_route(logits, k, ids, w, dev_err=None, stream=None):

@@ -2,9 +2,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/moe.h"
 #include "internal.cuh"
@@ -56,6 +58,32 @@ const DeviceInfo& device_info() {
   return d;
 }
 
+namespace {
+struct SmemLimit {
+  int device;
+  const void* kernel;
+  int bytes;
+};
+std::mutex g_smem_mu;
+std::vector<SmemLimit> g_smem;
+std::atomic<long long> g_wait{kWaitCycles};
+}  // namespace
+
+cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_smem_mu);
+  for (const SmemLimit& l : g_smem)
+    if (l.device == dev && l.kernel == kernel && l.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  g_smem.push_back({dev, kernel, bytes});
+  return cudaSuccess;
+}
+
+long long wait_limit() { return g_wait.load(std::memory_order_relaxed); }
+
 static int check_device() {
   const DeviceInfo& d = device_info();
   if (d.device < 0) return fail(MOE_ERR_CUDA, "no CUDA device");
@@ -80,6 +108,18 @@ int moe_get_error(const uint32_t* dev_err, void* stream, uint32_t* bits) {
   if (e != cudaSuccess) return cuda_status(e, "moe_get_error(sync)");
   e = cudaMemcpy(bits, dev_err, sizeof(uint32_t), cudaMemcpyDeviceToHost);
   return cuda_status(e, "moe_get_error(copy)");
+}
+
+long long moe_set_wait_limit(long long cycles) {
+  if (cycles <= 0) cycles = kWaitCycles;
+  return g_wait.exchange(cycles);
+}
+
+int moe_check_bounded_wait(long long cycles, uint32_t* dev_err, void* stream) {
+  if (cycles < 1 || cycles > kWaitCycles || !dev_err) return fail(MOE_ERR_ARG, "moe_check_bounded_wait: bad args");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_bounded_wait_check(cycles, dev_err, static_cast<cudaStream_t>(stream)),
+                     "moe_check_bounded_wait");
 }
 
 int moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err, void* stream) {
@@ -243,6 +283,7 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
   a.out_fmt = out_fmt;
   a.out_scale = out_scale;
   a.dev_err = dev_err;
+  a.wait = wait_limit();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return cuda_status(launch_gemv(a, s), "moe_w2_mm");
 }
@@ -260,14 +301,6 @@ int moe_w2_mm_noalloc(int stage, const void* act, int act_rows, const int32_t* a
   if (act_rows < 0 || rows < 0) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: act_rows or rows < 0");
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: act_row_div < 1");
   if (rows == 0) return MOE_OK;
-  const size_t need = lut_workspace_bytes(stage, rows, N, K);
-  if (need > MOE_W2_NOALLOC_SCRATCH_BYTES) {
-    std::snprintf(g_err, sizeof(g_err),
-                  "moe_w2_mm_noalloc: %d rows need %zu bytes of scratch, above the fixed %u bytes; use moe_w2_mm "
-                  "with a workspace",
-                  rows, need, MOE_W2_NOALLOC_SCRATCH_BYTES);
-    return MOE_ERR_WS_SMALL;
-  }
   MMArgs a{};
   a.stage = stage;
   a.act = act;
@@ -290,8 +323,19 @@ int moe_w2_mm_noalloc(int stage, const void* act, int act_rows, const int32_t* a
   a.out = out;
   a.out_fmt = out_fmt;
   a.dev_err = dev_err;
+  a.wait = wait_limit();
+  // the shape first: a shape the table GEMV does not take is unsupported
+  // whatever its size
   if (!lut_supported(a))
     return fail(MOE_ERR_UNSUPPORTED, "moe_w2_mm_noalloc: K is not a multiple of the table GEMV's slice width");
+  const size_t need = lut_workspace_bytes(stage, rows, N, K);
+  if (need > MOE_W2_NOALLOC_SCRATCH_BYTES) {
+    std::snprintf(g_err, sizeof(g_err),
+                  "moe_w2_mm_noalloc: %d rows need %zu bytes of scratch, above the fixed %u bytes; use moe_w2_mm "
+                  "with a workspace",
+                  rows, need, MOE_W2_NOALLOC_SCRATCH_BYTES);
+    return MOE_ERR_WS_SMALL;
+  }
   return cuda_status(launch_lut_gemv_noalloc(a, rows, static_cast<cudaStream_t>(stream)), "moe_w2_mm_noalloc");
 }
 
@@ -346,6 +390,7 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
   a.out_fmt = out_fmt;
   a.out_scale = out_scale;
   a.dev_err = dev_err;
+  a.wait = wait_limit();
   return cuda_status(launch_gemv(a, static_cast<cudaStream_t>(stream)), "moe_mxfp4_mm");
 }
 

@@ -13,8 +13,9 @@
 
 namespace moe {
 
-// A bounded wait gives up after this many SM clock cycles (~1-2 s); the
-// waiter then reports MOE_DEVERR_TIMEOUT instead of hanging the GPU.
+// A bounded wait gives up after a limit of SM clock cycles and the waiter
+// then reports MOE_DEVERR_TIMEOUT instead of hanging the GPU.  The limit is a
+// kernel parameter (moe_set_wait_limit); this is its default (~1.5 s).
 constexpr long long kWaitCycles = 3000000000LL;
 
 MOE_D uint32_t smem_u32(const void* p) {
@@ -51,12 +52,12 @@ MOE_D bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false if it did not complete within kWaitCycles.
-MOE_D bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// false if it did not complete within `limit` SM clock cycles.
+MOE_D bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }

@@ -50,6 +50,7 @@ struct TcParams {
   void* out;
   int out_fmt;
   uint32_t* dev_err;
+  long long wait;  // bounded-wait limit (SM clock cycles)
 };
 
 // ------------------------------------------------------------------ PTX
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) w2_gemm_kernel(const __grid_c
         const int row0 = P.offsets[e] + mt * kBM;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kStagesTC;
-          if (L >= kStagesTC && !mbar_wait(&empty[s], ((L / kStagesTC) - 1) & 1)) {
+          if (L >= kStagesTC && !mbar_wait(&empty[s], ((L / kStagesTC) - 1) & 1, P.wait)) {
             abort_all();
             break;
           }
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) w2_gemm_kernel(const __grid_c
       decode_tile(i, e, blk, mt);
       for (int kb = 0; kb < KB; ++kb, ++L) {
         const int s = L % kStagesTC;
-        if (L >= kStagesTC && !mbar_wait(&empty[s], ((L / kStagesTC) - 1) & 1)) {
+        if (L >= kStagesTC && !mbar_wait(&empty[s], ((L / kStagesTC) - 1) & 1, P.wait)) {
           abort_all();
           break;
         }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) w2_gemm_kernel(const __grid_c
       int t = 0;
       for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
         const int a = t & 1;
-        if (t >= 2 && !mbar_wait(&acc_empty[a], ((t >> 1) - 1) & 1)) {
+        if (t >= 2 && !mbar_wait(&acc_empty[a], ((t >> 1) - 1) & 1, P.wait)) {
           abort_all();
           break;
         }
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) w2_gemm_kernel(const __grid_c
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kStagesTC;
           const uint32_t par = (L / kStagesTC) & 1;
-          if (!mbar_wait(&full_a[s], par) || !mbar_wait(&full_b[s], par)) {
+          if (!mbar_wait(&full_a[s], par, P.wait) || !mbar_wait(&full_b[s], par, P.wait)) {
             ok = false;
             break;
           }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) w2_gemm_kernel(const __grid_c
       int e, blk, mt;
       decode_tile(i, e, blk, mt);
       const int a = t & 1;
-      if (!mbar_wait(&acc_full[a], (t >> 1) & 1)) {
+      if (!mbar_wait(&acc_full[a], (t >> 1) & 1, P.wait)) {
         abort_all();
         break;
       }
@@ -474,6 +475,7 @@ cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
+  P.wait = a.wait;
   // A: [rows_total][K] bf16, box 64 x 128 with the 128-byte swizzle
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1)};
@@ -489,11 +491,11 @@ cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   cudaError_t e;
   if (bn256) {
-    e = cudaFuncSetAttribute(w2_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = set_smem_limit(w2_gemm_kernel<256>, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     w2_gemm_kernel<256><<<di.sms, kGemmThreads, smem, s>>>(map, P);
   } else {
-    e = cudaFuncSetAttribute(w2_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = set_smem_limit(w2_gemm_kernel<128>, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     w2_gemm_kernel<128><<<di.sms, kGemmThreads, smem, s>>>(map, P);
   }

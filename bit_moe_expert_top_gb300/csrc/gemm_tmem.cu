@@ -94,6 +94,7 @@ struct TmParams {
   void* out;
   int out_fmt;
   uint32_t* dev_err;
+  long long wait;           // bounded-wait limit (SM clock cycles)
 };
 
 // ------------------------------------------------------------------ PTX
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     uint32_t dyn;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
     if (tiles_off + static_cast<uint32_t>(kTS * kBTile + ring_bytes<WF, NT>()) > dyn) {  // refuse
-      if (tid == 0) set_err(P.dev_err, MOE_DEVERR_TIMEOUT);
+      if (tid == 0) set_err(P.dev_err, MOE_DEVERR_LAUNCH);
       return;
     }
   }
@@ -375,8 +376,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kTS;
-          if (L >= kTS && (!mbar_wait(&empty[s], ((L / kTS) - 1) & 1) ||
-                           !mbar_wait(&empty[kTS + s], ((L / kTS) - 1) & 1))) {
+          if (L >= kTS && (!mbar_wait(&empty[s], ((L / kTS) - 1) & 1, P.wait) ||
+                           !mbar_wait(&empty[kTS + s], ((L / kTS) - 1) & 1, P.wait))) {
             ok = false;
             break;
           }
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int c = L % kCS;
-          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1)) {
+          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1, P.wait)) {
             ok = false;
             break;
           }
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int c = L % RD;
-          if (L >= RD && !mbar_wait(&code_empty[c], ((L / RD) - 1) & 1)) {
+          if (L >= RD && !mbar_wait(&code_empty[c], ((L / RD) - 1) & 1, P.wait)) {
             ok = false;
             break;
           }
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int c = L % kCS;
-          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1)) {
+          if (L >= kCS && !mbar_wait(&code_empty[c], ((L / kCS) - 1) & 1, P.wait)) {
             ok = false;
             break;
           }
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         decode_tile(i, e, blk, mt);
         const int nvalid = min(NT, P.offsets[e + 1] - P.offsets[e] - mt * NT);
         const uint32_t idesc = idesc_bf16_mn(128, min(NT, (nvalid + 15) & ~15));
-        if (t >= 1 && !mbar_wait(&acc_empty[bs], (t - 1) & 1)) {
+        if (t >= 1 && !mbar_wait(&acc_empty[bs], (t - 1) & 1, P.wait)) {
           abort_all();
           break;
         }
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         for (int kb = 0; kb < KB; ++kb, ++L) {
           const int s = L % kTS;
           const uint32_t par = (L / kTS) & 1;
-          if (!mbar_wait(&full_b[s], par) || !mbar_wait(&full_a[bs * kTS + s], par)) {
+          if (!mbar_wait(&full_b[s], par, P.wait) || !mbar_wait(&full_a[bs * kTS + s], par, P.wait)) {
             ok = false;
             break;
           }
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const uint32_t sbase = smem_u32(codes_s) + static_cast<uint32_t>(4096 + bsel * 512 + (m >> 2) * 16 + (m & 3) * 2);
       for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
         const int s = L % kTS, c = L % kCS;
-        if (!mbar_wait(&code_full[c], (L / kCS) & 1)) {
+        if (!mbar_wait(&code_full[c], (L / kCS) & 1, P.wait)) {
           ok = false;
           break;
         }
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[3]) : "r"(co + cw3) : "memory");
         asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc0) : "r"(so) : "memory");
         asm volatile("ld.shared.u16 %0, [%1+8];" : "=r"(sc1) : "r"(so) : "memory");
-        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
+        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1, P.wait)) {
           ok = false;
           break;
         }
@@ -630,7 +631,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
           const uint32_t L = L0 + d0;
           if (L < Ltot && ok) {
             const int s = L % kTS, c = L % RD;
-            if (!mbar_wait(&code_full[c], (L / RD) & 1)) {
+            if (!mbar_wait(&code_full[c], (L / RD) & 1, P.wait)) {
               ok = false;
               break;
             }
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                            : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
                            : "r"(qo + ((static_cast<uint32_t>(h) ^ qx) << 4))
                            : "memory");
-            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
+            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1, P.wait)) {
               ok = false;
             } else {
               tm_fence_after();
@@ -690,7 +691,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       const uint32_t rx = static_cast<uint32_t>((m >> 1) & 3);
       for (uint32_t L = 0; L < Ltot && ok && !aborted(); ++L) {
         const int s = L % kTS, c = L % kCS;
-        if (!mbar_wait(&code_full[c], (L / kCS) & 1)) {
+        if (!mbar_wait(&code_full[c], (L / kCS) & 1, P.wait)) {
           ok = false;
           break;
         }
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                        : "=r"(vb[j].x), "=r"(vb[j].y), "=r"(vb[j].z), "=r"(vb[j].w)
                        : "r"(ro + ((static_cast<uint32_t>(j) ^ rx) << 4))
                        : "memory");
-        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1)) {
+        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1, P.wait)) {
           ok = false;
           break;
         }
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
       int e, blk, mt;
       decode_tile(i, e, blk, mt);
-      if (!mbar_wait(acc_full, t & 1)) {
+      if (!mbar_wait(acc_full, t & 1, P.wait)) {
         abort_all();
         break;
       }
@@ -880,13 +881,8 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
   const size_t pre = lut ? ((1024 + static_cast<size_t>(kPre) + 65535) & ~size_t(65535)) - 1024 + 65536
                          : static_cast<size_t>(kPre) + 1024;
   const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + ring_bytes<WF, NT>() + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(tmem_mm_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = set_smem_limit(tmem_mm_kernel<WF, NT>, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   return launch_pdl(tmem_mm_kernel<WF, NT>, dim3(device_info().sms), dim3(kTmThreads), smem, s, map, cmap, smap, P);
 }
 
@@ -925,6 +921,7 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
+  P.wait = a.wait;
   // token tile: 128 rows for prefill-sized groups, 32 for decode-sized ones
   // (the decode of each weight block repeats per token tile, so 32-row tiles
   // only pay off when groups are small)

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams P) {
         else row0 = nb * kOutBlk + st * RS;
         const int s = L % P.stages;
         if (L >= static_cast<uint32_t>(P.stages)) {
-          if (!mbar_wait(&empty[s], ((L / P.stages) - 1) & 1)) {
+          if (!mbar_wait(&empty[s], ((L / P.stages) - 1) & 1, a.wait)) {
             set_err(a.dev_err, MOE_DEVERR_TIMEOUT);
             return;
           }
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams P) {
     const int ntok = min(kTR, a.offsets[e + 1] - p0);
     for (int st = 0; st < nst; ++st, ++L) {
       const int s = L % P.stages;
-      const bool ok = mbar_wait(&full[s], (L / P.stages) & 1);
+      const bool ok = mbar_wait(&full[s], (L / P.stages) & 1, a.wait);
       const uint8_t* sq = ring + static_cast<size_t>(s) * P.stage_bytes;
       const uint8_t* ss = sq + P.sq_bytes;
       bool abort_now = !ok;
@@ -428,7 +428,7 @@ cudaError_t launch_t(const GemvParams& P0, cudaStream_t s) {
   if (stages < 2) return cudaErrorInvalidConfiguration;
   P.stages = stages;
   const SmemLayout lay = smem_layout(stages, P.stage_bytes, G, V, P.a.E);
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<WK, AF>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  cudaError_t e = set_smem_limit(gemv_kernel<WK, AF>, lay.total);
   if (e != cudaSuccess) return e;
   gemv_kernel<WK, AF><<<di.sms, kThreads, lay.total, s>>>(P);
   return cudaGetLastError();

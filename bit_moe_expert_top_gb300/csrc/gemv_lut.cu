@@ -489,9 +489,10 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
 // sums [rows][NB][NSL][kBR] (fp32).  Everything is written before it is read;
 // no initial contents needed.  NB = N/8 batches for FC1 (8 gate + 8 up rows
 // each), N/16 for FC2.
+// nsl = 0 (no table GEMV, no workspace) unless K is a multiple of the slice.
 static void lut_geometry(int stage, int N, int K, int& nb, int& nsl) {
   nb = stage == MOE_STAGE_FC1_SWIGLU ? N / 8 : N / 16;
-  nsl = K / kSW;
+  nsl = K % kSW == 0 ? K / kSW : 0;
 }
 
 static size_t lut_header_bytes(int rows) { return (static_cast<size_t>(rows + 1) * sizeof(int) + 255) & ~size_t(255); }
@@ -544,13 +545,9 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(w2_lut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLutSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  cudaError_t e = launch_pdl(w2_lut_kernel, dim3(device_info().sms), dim3(kLutThreads), kLutSmem, s, P);
+  cudaError_t e = set_smem_limit(w2_lut_kernel, kLutSmem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(w2_lut_kernel, dim3(device_info().sms), dim3(kLutThreads), kLutSmem, s, P);
   if (e != cudaSuccess) return e;
   // the finishing kernel as a programmatic dependent: its launch overlaps the
   // main kernel's tail; its pdl_wait orders the scratch reads

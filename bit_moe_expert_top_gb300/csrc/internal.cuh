@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace moe {
 
 // Launch `kernel` as a programmatic dependent of the preceding work in `s`:
@@ -34,6 +36,18 @@ struct DeviceInfo {
 };
 // Cached properties of the current device.
 const DeviceInfo& device_info();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (device, kernel, size); thread-safe.
+cudaError_t set_smem_limit(const void* kernel, int bytes);
+template <typename K>
+cudaError_t set_smem_limit(K* kernel, int bytes) {
+  return set_smem_limit(reinterpret_cast<const void*>(kernel), bytes);
+}
+
+// The bounded-wait limit (SM clock cycles) that launches pass to their
+// kernels (moe_set_wait_limit).
+long long wait_limit();
 
 // ---- route / permute / combine (route_permute.cu)
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
@@ -87,6 +101,7 @@ struct MMArgs {
   int out_fmt;
   uint8_t* out_scale;
   uint32_t* dev_err;
+  long long wait;             // bounded-wait limit in SM clock cycles
 };
 // Dispatch: the shared-memory LUT GEMV for 2-bit weights when the shape allows,
 // else the generic CUDA-core kernel.
@@ -101,6 +116,11 @@ cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 // tensor-core grouped matmul with the dequantised weights in TMEM (gemm_tmem.cu)
 bool tmem_mm_supported(const MMArgs& a);
 cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s);
+
+// ---- diagnostics (diag.cu)
+// One warp waits with the pipelines' bounded wait, limit `cycles`, on a
+// shared-memory mbarrier nobody arrives on; sets MOE_DEVERR_TIMEOUT.
+cudaError_t launch_bounded_wait_check(long long cycles, uint32_t* dev_err, cudaStream_t s);
 
 // ---- the table GEMV on the library's own fixed scratch (noalloc.cu)
 // Device address of the scratch array on the current device (looked up on the

@@ -237,13 +237,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
                            uint32_t* dev_err, cudaStream_t s) {
   const int A = T * k;
   const size_t smem = static_cast<size_t>(kPermWarps + 1) * E * sizeof(int);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_smem_limit(permute_kernel, static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int)));
+  if (e != cudaSuccess) return e;
   return launch_pdl(permute_kernel, dim3(1), dim3(1024), smem, s, ids, A, E, offsets, perm, inv, dev_err);
 }
 

@@ -33,7 +33,12 @@
  *    caller zeroes; may be NULL to ignore) and carry on.  Read with
  *    moe_get_error.
  *  - Thread-safe: the only host-side global state is a per-device property
- *    cache and the per-device address of moe_w2_mm_noalloc's scratch.
+ *    cache, a per-device record of the kernels whose shared-memory limit was
+ *    raised, the bounded-wait limit (moe_set_wait_limit) and the per-device
+ *    address of moe_w2_mm_noalloc's scratch.
+ *  - Every on-chip wait of a pipeline (mbarrier phases) is bounded: a wait
+ *    that runs past the limit makes its kernel stop, set MOE_DEVERR_TIMEOUT and
+ *    return, so a fault in the pipeline never hangs the GPU.
  *
  * Canonical weight layout (what callers store; parity is stated against it)
  * ---------------------------------------------------------------------------
@@ -85,6 +90,8 @@ extern "C" {
 #define MOE_DEVERR_NAN_SCALE 0x4u    /* E8M0 scale byte 255 (NaN) in MXFP4 weights      */
 #define MOE_DEVERR_TIMEOUT 0x8u      /* a bounded on-chip wait gave up; outputs invalid */
 #define MOE_DEVERR_OVERFLOW 0x10u    /* an expert group exceeded a kernel's row limit   */
+#define MOE_DEVERR_LAUNCH 0x20u      /* a kernel found its launch short of what its layout
+                                        needs (dynamic shared memory) and did nothing   */
 
 /* activation / output formats */
 #define MOE_FMT_NONE 0
@@ -115,6 +122,19 @@ MOE_API const char* moe_last_error_string(void);
 /* Synchronises `stream`, then copies the device word *dev_err to the host
  * word *bits (host pointer).  The device word is left unchanged. */
 MOE_API int moe_get_error(const uint32_t* dev_err, void* stream, uint32_t* bits);
+
+/* Sets the bounded-wait limit, in SM clock cycles, that expert-matmul
+ * launches made after this call pass to their kernels (cycles <= 0 restores
+ * the default, 3e9 cycles, about 1.5 s at 2 GHz).  Returns the previous
+ * limit.  Process-wide; host only. */
+MOE_API long long moe_set_wait_limit(long long cycles);
+
+/* Self-test of the bounded wait (no counterpart in the pages): launches one
+ * warp that waits, with limit `cycles` (1 .. 3e9), on a shared-memory
+ * mbarrier that nothing ever arrives on, using the pipelines' wait.  When the
+ * limit runs out the kernel ORs MOE_DEVERR_TIMEOUT into *dev_err and returns;
+ * the context stays usable.  No copy or MMA is in flight in that kernel. */
+MOE_API int moe_check_bounded_wait(long long cycles, uint32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------ routing
  * Top-k softmax routing (vLLM-Moet README line table: 384 routed experts per
@@ -265,7 +285,9 @@ MOE_API int moe_w2_mm(int stage, int mode,
  * take (K not a multiple of its slice width) give MOE_ERR_UNSUPPORTED.
  * Set-up: the first call on a device, with that device current, looks up the
  * scratch's device address (cudaGetSymbolAddress, which may load the module);
- * make that first call before any stream capture.  Nothing in the scratch
+ * make that first call before any stream capture.  The address is cached per
+ * device until the process exits: after cudaDeviceReset on a device the
+ * cached address is stale, so do not call this entry point there again.  Nothing in the scratch
  * needs to start at zero, so a call issues no copy or memset.
  * One scratch per device: calls that overlap on the GPU (other streams or
  * threads) race on it and give wrong results; serialise them. */

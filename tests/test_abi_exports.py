@@ -52,6 +52,13 @@ def test_host_only_calls(lib_path):
     b = lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 128, 2048, 4096)
     assert 0 < a < b
     assert lib.moe_w2_mm_workspace_size(7, 64, 2048, 4096) == 0
+    # K not a multiple of the table GEMV's 512-element slice: no workspace
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 64, 256, 640) == 0
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 64, 4096, 1152) == 0
+    assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 64, 4096, 1536) > 0
+    # the bounded-wait limit is host state: set, read back, restore
+    prev = lib.moe_set_wait_limit(777)
+    assert lib.moe_set_wait_limit(prev) == 777
 
 
 def test_noalloc_limit_matches_header(lib_path):

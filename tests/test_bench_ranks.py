@@ -68,8 +68,8 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("RANK", "1")
     called = []
-    monkeypatch.setattr(bench, "cpu_baseline", lambda *a, **k: called.append(a) or {})
-    args = bench.argparse.Namespace(workload="tiny", warmup=0, steps=1, cpu_sample=1)
+    monkeypatch.setattr(bench, "oracle_steps", lambda *a, **k: called.append(a) or ([1.0], 1, 1, 16))
+    args = bench.argparse.Namespace(workload="tiny", warmup=0, steps=1)
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.run_reference(args)
@@ -79,9 +79,9 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
 def test_reference_arm_line_on_rank_zero(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("RANK", "0")
-    sample = {"value": 4.0, "unit": "tokens/s", "sample": "fake sample"}
-    monkeypatch.setattr(bench, "cpu_baseline", lambda *a, **k: dict(sample))
-    args = bench.argparse.Namespace(workload="tiny", warmup=1, steps=2, cpu_sample=1)
+    # one warm-up step, then two timed whole steps of 16 tokens in 4 s each
+    monkeypatch.setattr(bench, "oracle_steps", lambda *a, **k: ([0.5, 4.0, 4.0], 4, 16, 16))
+    args = bench.argparse.Namespace(workload="tiny", warmup=1, steps=2)
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.run_reference(args)
@@ -89,4 +89,14 @@ def test_reference_arm_line_on_rank_zero(monkeypatch):
     assert len(lines) == 1
     res = json.loads(lines[0])
     assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["value"] == 4.0
+    assert res["ms_per_step"] == 4000.0          # the measured whole-step time, not an extrapolation
+    assert res["cpu_baseline"]["cores"] == 4 and res["cpu_baseline"]["value"] == 4.0
     assert res["e2e"] == {"value": 4.0, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_steps_split_tokens_over_processes():
+    """The CPU arms' runner: whole steps of the tiny layer, its 16 tokens split
+    over up to one spawned process per host core; one time per step."""
+    times, procs, cores, ntok = bench.oracle_steps("tiny", 2)
+    assert ntok == 16 and len(times) == 2 and all(t > 0 for t in times)
+    assert procs == min(cores, 16) and cores == len(os.sched_getaffinity(0))

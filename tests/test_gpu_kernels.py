@@ -229,3 +229,40 @@ def test_combine_matches_oracle(yfmt):
     L.moe_combine(yd, yfmt, dev(wt), dev(inv), T, k, H, outb, L.FMT_BF16)
     ob = C.bf16_bits_to_f64(host(outb).view(np.uint16))
     assert np.max(np.abs(ob - C.rne_bf16(want))) <= 2 ** -7 * np.max(np.abs(want))
+
+
+# ----------------------------------------------------------------- error paths
+
+def test_bounded_wait_expires_and_reports_timeout():
+    """A wait that nothing ends gives up after its limit, reports
+    MOE_DEVERR_TIMEOUT and returns; the context stays usable (a routing call
+    afterwards is still exact)."""
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_check_bounded_wait(2_000_000, err)          # ~1 ms of SM clocks
+    assert L.moe_get_error(err) == L.DEVERR_TIMEOUT
+    w = synth.get_workload("tiny")
+    lg = synth.make_logits(w)
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
+    wt = torch.empty((w.T, w.k), dtype=torch.float32, device=DEV)
+    err2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_route(dev(lg), w.k, ids, wt, err2)
+    assert L.moe_get_error(err2) == 0
+    assert np.array_equal(host(ids), M.route(lg, w.k)[0])
+
+
+def test_wait_limit_setting_round_trips():
+    """moe_set_wait_limit returns the previous limit; <= 0 restores the default."""
+    prev = L.moe_set_wait_limit(12345)
+    try:
+        assert L.moe_set_wait_limit(0) == 12345
+        assert L.moe_set_wait_limit(0) == 3_000_000_000
+    finally:
+        L.moe_set_wait_limit(prev)
+
+
+def test_bounded_wait_check_rejects_bad_limits():
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for cyc in (0, -5, 3_000_000_001):
+        with pytest.raises(L.MoEError) as ei:
+            L.moe_check_bounded_wait(cyc, err)
+        assert ei.value.code == L.MOE_ERR_ARG

@@ -87,3 +87,42 @@ def test_noalloc_rejects_rows_beyond_the_fixed_scratch():
                             act_row=b.perm, act_row_div=w.k, dev_err=b.dev_err)
     assert ei.value.code == L.MOE_ERR_WS_SMALL
     assert "scratch" in str(ei.value)
+
+
+def test_k_not_a_multiple_of_the_slice_width():
+    """K = 640 (a multiple of 128, not of the table GEMV's 512-element slice):
+    the workspace query answers 0, moe_w2_mm runs the register-decode GEMV
+    (a workspace passed anyway is ignored) and matches the oracle's exact
+    sums, and moe_w2_mm_noalloc refuses the shape as unsupported (not as a
+    small scratch), whatever the row count."""
+    from oracle import codecs as C
+    from oracle import moe as M
+    w = synth.get_workload("tiny").replace(E=4, H=640, I=256, k=2, T=9, logits="uniform")
+    assert L.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 64, w.I, w.H) == 0
+    assert L.moe_w2_mm_workspace_size(L.STAGE_FC2, 64, w.H, 640) == 0
+    ml, acc, _ = make_layer(w, seed=1, out_fmt=L.FMT_F32, mode=L.MODE_GEMV)
+    x = synth.make_x(w, 1)
+    lg = synth.make_logits(w, 1)
+    ids, _, _ = M.route(lg, w.k)
+    off, perm, _ = M.permute(ids, w.E)
+    A = w.T * w.k
+    h = torch.empty((A, w.I), dtype=torch.float32, device="cuda")
+    junk_ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    L.moe_w2_mm(L.STAGE_FC1_SWIGLU, dev(x.view(np.int16)), L.FMT_BF16, ml.c1k, ml.s1k, dev(off), w.E, w.I, w.H, h,
+                L.FMT_F32, act_row=dev(perm), act_row_div=w.k, mode=L.MODE_GEMV, ws=junk_ws)
+    torch.cuda.synchronize()
+    xp = C.bf16_bits_to_f64(x)[perm // w.k]
+    want = np.zeros((A, w.I))
+    for e in range(w.E):
+        r = slice(off[e], off[e + 1])
+        if off[e] != off[e + 1]:
+            W1 = acc(e)[0]
+            want[r] = M.silu(C.to_f32(xp[r] @ W1[:w.I].T)) * C.to_f32(xp[r] @ W1[w.I:].T)
+    rms = np.sqrt(np.mean(want ** 2))
+    assert np.max(np.abs(h.double().cpu().numpy() - want)) <= 1e-4 * rms
+    out = torch.empty((100000, w.I), dtype=torch.int16, device="cuda")
+    for rows in (A, 100000):
+        with pytest.raises(L.MoEError) as ei:
+            L.moe_w2_mm_noalloc(L.STAGE_FC1_SWIGLU, dev(x.view(np.int16)), ml.c1k, ml.s1k, dev(off), w.E, w.I, w.H,
+                                rows, out, L.FMT_BF16, act_row=dev(perm), act_row_div=w.k)
+        assert ei.value.code == L.MOE_ERR_UNSUPPORTED
