@@ -12,8 +12,9 @@ the previous step's weights in the 129 MB L2.
 The same run also times the other workloads of the metric, each on its own
 layer of weights, as sub-records of the line (``workloads``): prefill_bf16
 (8192 tokens, 2-bit experts on the tensor cores), prefill_fp8 (16384 tokens,
-MXFP4 experts through the FP8 workspace) and mixed_decode (64 tokens, 2-bit
-experts plus 64 MXFP4 delta-cache entries).
+MXFP4 experts through the FP8 workspace), prefill_fp8_direct (the same
+workload with the MXFP4 experts multiplied as stored, no workspace) and
+mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache entries).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead: whole layer steps of the same workload, its tokens split over one
@@ -148,12 +149,16 @@ def build_workload(name, layers, batches, device, tokens=None):
     from bit_moe_expert_top_gb300 import synth
     from bit_moe_expert_top_gb300.layer import MoELayer
 
-    w = synth.get_workload(name)
+    direct = name.endswith("_direct")  # MXFP4 experts multiplied as stored, no FP8 workspace
+    w = synth.get_workload(name[:-len("_direct")] if direct else name)
     if tokens:
         w = w.replace(T=tokens)
     mls = []
     for l in range(layers):
-        if w.weights == "w2":
+        if direct:
+            ml = MoELayer("mxfp4", w.E, w.H, w.I, w.k, device, mx=synth.make_mxfp4_layer(w, seed=0, layer=l),
+                          out_fmt=L.FMT_BF16)
+        elif w.weights == "w2":
             ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16)
         elif w.weights == "mixed":
             ml = MoELayer("mixed", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l),
@@ -317,7 +322,7 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None):
                 "flops_per_step": A * flops_per_assignment(w), "launch_us": round(mm_ms / n_mm * 1e3, 2),
                 "step_frac": round(tot_flops / (t_max / 1e3) / 1e12 / peak, 4)}
     rec = {"value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(t_max / steps, 5),
-           "config": {"workload": name, "E": w.E, "H": w.H, "I": w.I, "k": w.k, "T": w.T, "weights": w.weights,
+           "config": {"workload": name, "weight_path": mls[0].fmt, "E": w.E, "H": w.H, "I": w.I, "k": w.k, "T": w.T, "weights": w.weights,
                       "l2": (f"inputs larger than L2: {layers} distinct layers of weights rotated per step"
                              if layers > 1 else "inputs larger than L2: one layer of weights "
                              f"({_layer_gb(mls[0]):.1f} GB) and 4 token batches rotated per step"),
@@ -408,6 +413,8 @@ def launches_per_step(ml, T):
     if ml.fmt == "mixed":
         mx_tc = ml.mx_tensor_path()
         return 3 + (1 if mx_tc else 0) + 2 * 2 + 2 * 1
+    if ml.fmt == "mxfp4":
+        return 6
     nb = (ml.E + ml.batch - 1) // ml.batch
     return 4 + 4 * nb
 
@@ -613,9 +620,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8"])
+                    choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct"])
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,mixed_decode",
+    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

@@ -223,7 +223,8 @@ static int check_mm(const char* who, int stage, int mode, const void* act, int a
   if (E < 1 || E > 1024 || N <= 0 || K <= 0 || N % 128 || K % 128 || K > 8192)
     return fail(MOE_ERR_ARG, "%s: bad shape (N, K multiples of 128, K <= 8192, 1 <= E <= 1024)", who);
   if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "%s: act_fmt", who);
-  if (act_fmt == MOE_FMT_MXFP8 && !act_scale) return fail(MOE_ERR_ARG, "%s: act_scale is NULL", who);
+  if (act_fmt == MOE_FMT_MXFP8 && (!act_scale || !aligned(act_scale, 4)))
+    return fail(MOE_ERR_ARG, "%s: act_scale NULL or not 4-byte aligned", who);
   if (!act || !offsets || !out || !aligned(act, 16)) return fail(MOE_ERR_ARG, "%s: NULL or misaligned pointer", who);
   if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32 && out_fmt != MOE_FMT_MXFP8 && out_fmt != MOE_FMT_MXFP8_BF16)
     return fail(MOE_ERR_ARG, "%s: out_fmt", who);

@@ -441,6 +441,7 @@ cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s) {
   // GEMV for decode-sized ones (one 128-row tile per expert would be mostly idle)
   const bool want_gemm =
       a.mode == MOE_MODE_GEMM || (a.mode == MOE_MODE_AUTO && a.act_row == nullptr && a.act_rows >= 2048);
+  if (want_gemm && mx_mm_supported(a)) return launch_mx_mm(a, a.act_rows, s);
   if (want_gemm && tmem_mm_supported(a)) return launch_tmem_mm(a, a.act_rows, s);
   if (a.out_fmt == MOE_FMT_MXFP8_BF16) return cudaErrorNotSupported;  // tensor-core path only
   if (want_gemm && gemm_supported(a)) return launch_gemm_tc(a, a.act_rows, s);

@@ -115,6 +115,9 @@ bool gemm_supported(const MMArgs& a);
 cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 // tensor-core grouped matmul with the dequantised weights in TMEM (gemm_tmem.cu)
 bool tmem_mm_supported(const MMArgs& a);
+// block-scaled FP8 tensor-core matmul on MXFP8 activations (gemm_mx.cu)
+bool mx_mm_supported(const MMArgs& a);
+cudaError_t launch_mx_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 
 // ---- diagnostics (diag.cu)

@@ -14,7 +14,13 @@ with the weight path chosen by the layer's format:
             workspace ring (``mxfp4_to_fp8_ws`` on a side stream) ahead of the
             FP8 matmuls on the main stream, the conversion of the next batch
             overlapping the matmuls of the current one ("国产GPU完成MoE大模型
-            Day-0适配" §四).
+            Day-0适配" §四);
+* ``mxfp4`` the same MXFP4 experts multiplied as they are stored (E2M1
+            codes and E8M0 scales straight into the block-scaled tensor core),
+            no workspace.
+
+The FP8 formats quantise the token rows to MXFP8 in the gather, and FC1
+writes h as MXFP8 for FC2 ("FC1 + SwiGLU + MXFP8 quant, FC2").
 
 No arithmetic happens here: every step runs in the library's kernels.
 """
@@ -74,7 +80,7 @@ class MoELayer:
                 ts = _dev(src_s.view(np.int16), dev)
                 L.moe_w2_repack(tc, ts, src_c.shape[0], src_c.shape[1], K, dc, ds)
                 del tc, ts
-        if fmt in ("mixed", "fp8"):
+        if fmt in ("mixed", "fp8", "mxfp4"):
             q1, s1, q2, s2 = mx
             self.q1, self.e1 = _dev(q1, dev), _dev(s1, dev)
             self.q2, self.e2 = _dev(q2, dev), _dev(s2, dev)
@@ -100,7 +106,10 @@ class MoELayer:
     def use_gemm(self, T: int) -> bool:
         """Prefill-sized 2-bit and FP8-workspace steps run FC1/FC2 on the
         tensor cores over permuted (gathered) activation rows; decode-sized
-        ones on the CUDA-core kernels."""
+        ones on the CUDA-core kernels.  Direct MXFP4 steps always use the
+        block-scaled tensor core."""
+        if self.fmt == "mxfp4":
+            return True
         if self.fmt not in ("w2", "fp8") or self.mode == L.MODE_GEMV:
             return False
         return self.mode == L.MODE_GEMM or T * self.k >= self.gemm_min_rows
@@ -116,7 +125,7 @@ class MoELayer:
         dev, E, H, I, k = self.device, self.E, self.H, self.I, self.k
         A = T * k
         gather = self.use_gemm(T)
-        fp8 = self.fmt == "fp8" and not gather  # MXFP8 bytes + scales (the tensor path keeps bf16 values)
+        fp8 = self.fmt in ("fp8", "mxfp4")  # MXFP8 codes + scales for x_perm and h
         return StepBuffers(
             ids=torch.empty((T, k), dtype=torch.int32, device=dev),
             w=torch.empty((T, k), dtype=torch.float32, device=dev),
@@ -157,10 +166,20 @@ class MoELayer:
         L.moe_route(logits, k, b.ids, b.w, b.dev_err)
         if self.fmt == "fp8":
             tc = self.use_gemm(T)
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x,
-                          act_fmt=L.FMT_MXFP8_BF16 if tc else L.FMT_MXFP8, x_perm=b.x_perm,
-                          x_perm_scale=None if tc else b.x_perm_scale, dev_err=b.dev_err)
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
+                          x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
             self._fp8_experts(b, tc)
+        elif self.fmt == "mxfp4":
+            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
+                          x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
+            with self._timed("mx4_fc1_gemm"):
+                L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h, L.FMT_MXFP8,
+                               e2m1=self.q1, e8m0=self.e1, act_scale=b.x_perm_scale, out_scale=b.h_scale,
+                               mode=L.MODE_GEMM, dev_err=b.dev_err)
+            with self._timed("mx4_fc2_gemm"):
+                L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                               e2m1=self.q2, e8m0=self.e2, act_scale=b.h_scale, mode=L.MODE_GEMM,
+                               dev_err=b.dev_err)
         elif self.use_gemm(T):
             L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                           dev_err=b.dev_err)
@@ -233,8 +252,8 @@ class MoELayer:
     def _fp8_experts(self, b: StepBuffers, tc: bool = False):
         """Expert batches: MXFP4 -> FP8 workspace conversion on a side stream,
         ring of `fp8_ring` batches, matmuls of batch i after its conversion.
-        tc: the tensor-core matmuls on bf16 activation rows holding the MXFP8
-        values (FC1 writes h MXFP8-rounded the same way)."""
+        tc: the block-scaled FP8 tensor-core matmuls (MXFP8 token rows, E4M3
+        workspace weights; FC1 writes h as MXFP8), else the CUDA-core GEMV."""
         E, H, I = self.E, self.H, self.I
         main = torch.cuda.current_stream(self.device)
         conv = self.conv_stream
@@ -260,12 +279,13 @@ class MoELayer:
             main.wait_event(converted[i])
             if tc:
                 with self._timed("fp8_fc1_gemm"):
-                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, b.offsets, E, I, H, b.h,
-                                   L.FMT_MXFP8_BF16, fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot,
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h,
+                                   L.FMT_MXFP8, fp8_ws=self.ws1, ws_slot_of_expert=self.ws_slot,
+                                   act_scale=b.x_perm_scale, out_scale=b.h_scale,
                                    expert_begin=e0, expert_end=e1, mode=L.MODE_GEMM, dev_err=b.dev_err)
                 with self._timed("fp8_fc2_gemm"):
-                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
-                                   fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot,
+                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                                   fp8_ws=self.ws2, ws_slot_of_expert=self.ws_slot, act_scale=b.h_scale,
                                    expert_begin=e0, expert_end=e1, mode=L.MODE_GEMM, dev_err=b.dev_err)
             else:
                 with self._timed("fp8_fc1"):

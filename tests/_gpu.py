@@ -35,8 +35,9 @@ def bf16_to_f64(t):
     return C.bf16_bits_to_f64(host(t).view(np.uint16))
 
 
-def make_layer(w, seed=0, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, layer=0):
-    """(MoELayer, oracle expert accessor, profile)."""
+def make_layer(w, seed=0, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, layer=0, direct=False):
+    """(MoELayer, oracle expert accessor, profile).  direct: MXFP4 experts
+    multiplied as stored (no FP8 workspace)."""
     if w.weights == "w2":
         raw = synth.make_w2_layer(w, seed, layer)
         ml = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=out_fmt, mode=mode)
@@ -49,6 +50,9 @@ def make_layer(w, seed=0, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, layer=0):
         acc = M.mixed_expert_weights(M.w2_expert_weights(*raw), M.mxfp4_expert_weights(*mx), slot)
         return ml, acc, "bf16"
     mx = synth.make_mxfp4_layer(w, seed=seed, layer=layer)
+    if direct:
+        ml = MoELayer("mxfp4", w.E, w.H, w.I, w.k, mx=mx, out_fmt=out_fmt, mode=mode)
+        return ml, M.mxfp4_expert_weights(*mx), "fp8"
     ml = MoELayer("fp8", w.E, w.H, w.I, w.k, mx=mx, out_fmt=out_fmt, mode=mode,
                   fp8_batch=max(1, min(16, w.E // 4)))
     return ml, M.fp8_expert_weights(*mx), "fp8"

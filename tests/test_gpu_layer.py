@@ -17,8 +17,8 @@ from tests._gpu import TOL_BF16, TOL_FP8, bf16_to_f64, dev, host, make_layer, re
 pytestmark = pytest.mark.gpu
 
 
-def _check_full(w, seed=0, mode=L.MODE_GEMV):
-    ml, acc, prof = make_layer(w, seed, mode=mode)
+def _check_full(w, seed=0, mode=L.MODE_GEMV, direct=False):
+    ml, acc, prof = make_layer(w, seed, mode=mode, direct=direct)
     x = synth.make_x(w, seed)
     logits = synth.make_logits(w, seed, x_bits=x)
     out, b = run_layer(ml, x, logits)
@@ -73,9 +73,9 @@ def test_fp8_layer_nan_scale_flagged():
     assert L.moe_get_error(b.dev_err) & L.DEVERR_NAN_SCALE
 
 
-def _check_sampled(name, tokens, seed=0, mode=L.MODE_GEMV):
+def _check_sampled(name, tokens, seed=0, mode=L.MODE_GEMV, direct=False):
     w = synth.get_workload(name)
-    ml, acc, prof = make_layer(w, seed, mode=mode)
+    ml, acc, prof = make_layer(w, seed, mode=mode, direct=direct)
     x = synth.make_x(w, seed)
     logits = synth.make_logits(w, seed, x_bits=x)
     out, b = run_layer(ml, x, logits)
