@@ -140,9 +140,9 @@ def flops_per_assignment(w):
     return 6 * w.H * w.I
 
 
-def build_workload(name, layers, batches, device, tokens=None):
+def build_workload(name, layers, batches, device, tokens=None, experts=None):
     """Device weights (MoELayer per distinct layer) and token batches
-    (tokens: a smaller token count for profiling captures)."""
+    (tokens / experts: a smaller case for profiling captures)."""
     import torch
 
     from bit_moe_expert_top_gb300 import _lib as L
@@ -153,6 +153,8 @@ def build_workload(name, layers, batches, device, tokens=None):
     w = synth.get_workload(name[:-len("_direct")] if direct else name)
     if tokens:
         w = w.replace(T=tokens)
+    if experts:
+        w = w.replace(E=experts, n_hot=min(w.n_hot, experts))
     mls = []
     for l in range(layers):
         if direct:
@@ -202,7 +204,7 @@ def _decode_like(w):
     return w.T * w.k < 4096
 
 
-def measure(name, args, device, world, layers, *, clocks=None, tokens=None):
+def measure(name, args, device, world, layers, *, clocks=None, tokens=None, experts=None):
     """Time `steps` layer steps of workload `name` from a CUDA graph.
 
     Returns the record of the workload (tokens/s, ms per step, the roofline
@@ -214,7 +216,7 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None):
     from bit_moe_expert_top_gb300 import _lib as L
 
     batches = max(layers, 4)
-    w, mls, xs_h, lgs_h = build_workload(name, layers, batches, device, tokens)
+    w, mls, xs_h, lgs_h = build_workload(name, layers, batches, device, tokens, experts)
     xs = [torch.from_numpy(x.view(np.int16)).to(device) for x in xs_h]
     lgs = [torch.from_numpy(lg).to(device) for lg in lgs_h]
     bufs = [ml.buffers(w.T) for ml in mls]
@@ -302,7 +304,7 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None):
 
     peaks = _peaks()
     decode = _decode_like(w)
-    traffic = _traffic(w) if tokens is None else None
+    traffic = _traffic(w) if tokens is None and experts is None else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -372,9 +374,9 @@ def run_gpu(args):
     L.lib()
 
     head, _ = measure(args.workload, args, device, world, args.layers, clocks=ClockSampler(local),
-                      tokens=args.tokens)
+                      tokens=args.tokens, experts=args.experts)
     subs = {}
-    if args.sub and args.tokens is None:
+    if args.sub and args.tokens is None and args.experts is None:
         for name in args.sub.split(","):
             if name and name != args.workload:
                 torch.cuda.empty_cache()
@@ -626,6 +628,8 @@ def main():
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the workload's expert count (small cases for profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -28,7 +28,7 @@ EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wai
            "moe_check_bounded_wait", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
-           "moe_combine"]
+           "moe_combine", "moe_cache_select", "moe_cache_fill"]
 W2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -59,6 +59,8 @@ _SIGS = {
     "moe_mxfp4_mm": (_I, [_I, _I, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
                           _P, _P, _S, _P, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _I, _P]),
+    "moe_cache_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_cache_fill": (_I, [_P, _I, _I, _P, _P, _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -197,3 +199,21 @@ def moe_mxfp4_mm(stage, act, act_fmt, offsets, E, N, K, out, out_fmt, e2m1=None,
 
 def moe_combine(y, y_fmt, w, inv, T, k, H, out, out_fmt, stream=None):
     _check(lib().moe_combine(_ptr(y), y_fmt, _ptr(w), _ptr(inv), T, k, H, _ptr(out), out_fmt, _stream(stream)))
+
+
+def moe_cache_select(offsets, counts, decay_shift, expert_slot, slot_expert, promoted, dev_err=None, stream=None):
+    E = counts.numel()
+    S = slot_expert.numel()
+    _check(lib().moe_cache_select(_ptr(offsets), E, _ptr(counts), decay_shift, S, _ptr(expert_slot),
+                                  _ptr(slot_expert), _ptr(promoted), _ptr(dev_err), _stream(stream)))
+
+
+def moe_cache_fill(promoted, srcs, dsts, nbytes, stream=None):
+    """srcs / dsts: device-accessible base addresses (tensors or ints); nbytes:
+    bytes per expert / slot of each array."""
+    n = len(srcs)
+    S = promoted.numel()
+    src_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in srcs])
+    dst_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in dsts])
+    by_arr = (ctypes.c_size_t * n)(*[int(b) for b in nbytes])
+    _check(lib().moe_cache_fill(_ptr(promoted), S, n, src_arr, dst_arr, by_arr, _stream(stream)))

@@ -395,6 +395,30 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
   return cuda_status(launch_gemv(a, static_cast<cudaStream_t>(stream)), "moe_mxfp4_mm");
 }
 
+int moe_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_shift, int S, int32_t* expert_slot,
+                     int32_t* slot_expert, int32_t* promoted, uint32_t* dev_err, void* stream) {
+  if (E < 1 || E > 1024 || S < 1 || S > E || decay_shift < 0) return fail(MOE_ERR_ARG, "moe_cache_select: bad shape");
+  if (!offsets || !counts || !expert_slot || !slot_expert || !promoted)
+    return fail(MOE_ERR_ARG, "moe_cache_select: NULL pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_cache_select(offsets, E, counts, decay_shift, S, expert_slot, slot_expert, promoted,
+                                         dev_err, static_cast<cudaStream_t>(stream)),
+                     "moe_cache_select");
+}
+
+int moe_cache_fill(const int32_t* promoted, int S, int n_arrays, const void* const* src, void* const* dst,
+                   const size_t* bytes, void* stream) {
+  if (S < 1 || n_arrays < 1 || n_arrays > 4 || !promoted || !src || !dst || !bytes)
+    return fail(MOE_ERR_ARG, "moe_cache_fill: bad arguments");
+  for (int a = 0; a < n_arrays; ++a) {
+    if (!src[a] || !dst[a] || !aligned(src[a], 16) || !aligned(dst[a], 16) || bytes[a] == 0 || bytes[a] % 16)
+      return fail(MOE_ERR_ARG, "moe_cache_fill: array pointers must be 16-byte aligned, sizes multiples of 16");
+  }
+  if (int r = check_device()) return r;
+  return cuda_status(launch_cache_fill(promoted, S, n_arrays, src, dst, bytes, static_cast<cudaStream_t>(stream)),
+                     "moe_cache_fill");
+}
+
 int moe_combine(const void* y, int y_fmt, const float* w, const int32_t* inv, int T, int k, int H, void* out,
                 int out_fmt, void* stream) {
   if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 128) return fail(MOE_ERR_ARG, "moe_combine: bad shape");

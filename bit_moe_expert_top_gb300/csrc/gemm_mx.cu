@@ -284,54 +284,79 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
     }
   } else if (warp >= 4 && warp < 8) {
     // ================= scale factors into TMEM =================
+    // The words of a stage are loaded kPF stages ahead (a register ring), so
+    // the L2 round trip of the scale loads overlaps the MMAs of the stages
+    // in between; a warp can run at most kMS stages ahead of the MMAs anyway.
+    constexpr int kPF = kMS;
     const int q = warp & 3;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     if (AF == kAE4M3) tm_st1(tl + kSFU + q, 0x7F7F7F7Fu);  // 2^0 for every weight row and k-block
-    uint32_t L = 0;
-    bool ok = true;
-    uint32_t nan = 0;
-    for (int i = blockIdx.x; i < total && ok && !aborted(); i += gridDim.x) {
+    const int ntile = static_cast<int>(blockIdx.x) < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const uint32_t Ltot = static_cast<uint32_t>(ntile) * static_cast<uint32_t>(KB);
+    // prefetch cursor: tile pi, k-stage pkb
+    int pi = blockIdx.x, pkb = 0, p0 = 0;
+    const uint8_t* wsa0 = nullptr;
+    const uint8_t* wsa1 = nullptr;
+    auto rebase = [&]() {
       int e, blk, mt;
-      decode_tile(i, e, blk, mt);
-      const int p0 = P.offsets[e] + mt * NT;
-      const uint8_t* wsa[2] = {nullptr, nullptr};
+      decode_tile(pi, e, blk, mt);
+      p0 = P.offsets[e] + mt * NT;
       if (AF == kAE2M1) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-          wsa[b] = P.wscale + (static_cast<size_t>(wslot[e]) * P.R + brow(blk, b) + 32 * q + lane) * KSB;
+        const size_t r = static_cast<size_t>(wslot[e]) * P.R + 32 * q + lane;
+        wsa0 = P.wscale + (r + brow(blk, 0)) * KSB;
+        wsa1 = P.wscale + (r + brow(blk, 1)) * KSB;
       }
-      for (int kb = 0; kb < KB; ++kb, ++L) {
-        const int s = L % kMS;
-        // token n = lane + 32 j of the tile: its 4 E8M0 bytes of this stage
-        uint32_t w[4];
+    };
+    if (pi < total) rebase();
+    uint32_t w[kPF][4], wa[kPF][2];
+    uint32_t nan = 0;
+    auto load = [&](uint32_t (&wd)[4], uint32_t (&wad)[2]) {
+      if (pi >= total) return;
+      // token n = lane + 32 j of the tile: its 4 E8M0 bytes of this stage
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int p = p0 + lane + 32 * j;
-          w[j] = (j < NT / 32 && p < P.rows_total) ? ld_u32(P.act_scale + static_cast<size_t>(p) * KSB + 4 * kb)
-                                                   : 0x7F7F7F7Fu;
-        }
-        uint32_t wa[2] = {0, 0};
-        if (AF == kAE2M1) {
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + lane + 32 * j;
+        wd[j] = (j < NT / 32 && p < P.rows_total) ? ld_u32(P.act_scale + static_cast<size_t>(p) * KSB + 4 * pkb)
+                                                  : 0x7F7F7F7Fu;
+      }
+      if (AF == kAE2M1) {
+        wad[0] = ld_u32(wsa0 + 4 * pkb);
+        wad[1] = ld_u32(wsa1 + 4 * pkb);
+      }
+      if (++pkb == KB) {
+        pkb = 0;
+        pi += gridDim.x;
+        if (pi < total) rebase();
+      }
+    };
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            wa[b] = ld_u32(wsa[b] + 4 * kb);
-            nan |= has_ff_byte(wa[b]) ? 1u : 0u;
+    for (int d = 0; d < kPF; ++d) load(w[d], wa[d]);
+    bool ok = true;
+    for (uint32_t L0 = 0; L0 < Ltot && ok; L0 += kPF) {
+      if (__any_sync(0xffffffffu, aborted())) break;  // warp-uniform
+#pragma unroll
+      for (int d = 0; d < kPF; ++d) {
+        const uint32_t L = L0 + d;
+        if (L < Ltot && ok) {
+          const int s = L % kMS;
+          // one decision per warp (the tcgen05.st below are warp-collective)
+          ok = __all_sync(0xffffffffu, L < kMS || mbar_wait(&empty[s], ((L / kMS) - 1) & 1, P.wait));
+          if (ok) {
+            tm_fence_after();  // the MMAs that read these columns are complete
+            const uint32_t c0 = tl + kSF0 + s * kSFCols;
+            tm_st4(c0 + 8, w[d][0], w[d][1], w[d][2], w[d][3]);
+            if (AF == kAE2M1) {
+              nan |= (has_ff_byte(wa[d][0]) || has_ff_byte(wa[d][1])) ? 1u : 0u;
+              tm_st1(c0 + q, wa[d][0]);
+              tm_st1(c0 + 4 + q, wa[d][1]);
+            }
+            tm_st_wait();
+            tm_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sf_full[s]);
+            load(w[d], wa[d]);  // the stage kPF ahead
           }
         }
-        // one decision per warp (the tcgen05.st below are warp-collective)
-        ok = __all_sync(0xffffffffu, L < kMS || mbar_wait(&empty[s], ((L / kMS) - 1) & 1, P.wait));
-        if (!ok) break;
-        tm_fence_after();  // the MMAs that read these columns are complete
-        const uint32_t c0 = tl + kSF0 + s * kSFCols;
-        tm_st4(c0 + 8, w[0], w[1], w[2], w[3]);
-        if (AF == kAE2M1) {
-          tm_st1(c0 + q, wa[0]);
-          tm_st1(c0 + 4 + q, wa[1]);
-        }
-        tm_st_wait();
-        tm_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_full[s]);
       }
     }
     if (!ok) abort_all();
@@ -357,7 +382,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       named_bar_sync(1, 128);
     };
     int t = 0;
-    for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
+    for (int i = blockIdx.x; i < total; i += gridDim.x, ++t) {
+      if (__any_sync(0xffffffffu, aborted())) break;  // warp-uniform
       int e, blk, mt;
       decode_tile(i, e, blk, mt);
       // one decision per warp (the tcgen05.ld below are warp-collective)

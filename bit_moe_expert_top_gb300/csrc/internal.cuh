@@ -120,6 +120,13 @@ bool mx_mm_supported(const MMArgs& a);
 cudaError_t launch_mx_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 
+// ---- FP4 delta-cache management (cache.cu)
+cudaError_t launch_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_shift, int S,
+                                int32_t* expert_slot, int32_t* slot_expert, int32_t* promoted, uint32_t* dev_err,
+                                cudaStream_t s);
+cudaError_t launch_cache_fill(const int32_t* promoted, int S, int n, const void* const* src, void* const* dst,
+                              const size_t* bytes, cudaStream_t s);
+
 // ---- diagnostics (diag.cu)
 // One warp waits with the pipelines' bounded wait, limit `cycles`, on a
 // shared-memory mbarrier nobody arrives on; sets MOE_DEVERR_TIMEOUT.

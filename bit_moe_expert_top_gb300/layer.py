@@ -302,6 +302,34 @@ class MoELayer:
                 convert(i + self.ring)
         main.wait_stream(conv)
 
+    # ------------------------------------------------------------ delta cache
+    def attach_store(self, store, decay_shift: int = 31):
+        """Manage the FP4 delta cache of a mixed layer on the device: ``store``
+        holds the MXFP4 weights of every expert (q1, s1, q2, s2 stacked over
+        E; device tensors, or pinned host tensors read over the CPU-GPU
+        link).  ``update_cache`` then re-selects the cached experts from the
+        running routing counts and copies newly promoted experts into their
+        slots (moe_cache_select + moe_cache_fill), with no host sync."""
+        assert self.fmt == "mixed"
+        E, S = self.E, self.q1.shape[0]
+        self.store = list(store)
+        self.store_bytes = [t[0].numel() * t.element_size() for t in self.store]
+        self.decay_shift = decay_shift
+        self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
+        es = self.expert_slot.cpu().numpy()
+        se = np.full(S, -1, dtype=np.int32)
+        for e in np.nonzero(es >= 0)[0]:
+            se[es[e]] = e
+        self.slot_expert = _dev(se, self.device)
+        self.promoted = torch.empty(S, dtype=torch.int32, device=self.device)
+
+    def update_cache(self, b: StepBuffers):
+        """After a step: counts from the step's grouping, new cached set and
+        slot maps, copies of the promoted experts (stream-ordered)."""
+        L.moe_cache_select(b.offsets, self.counts, self.decay_shift, self.expert_slot, self.slot_expert,
+                           self.promoted, dev_err=b.dev_err)
+        L.moe_cache_fill(self.promoted, self.store, [self.q1, self.e1, self.q2, self.e2], self.store_bytes)
+
     def touched_weight_bytes(self, offsets: np.ndarray) -> int:
         """Bytes of packed weights (codes/nibbles + scales) of the experts the
         step touches: the decode roofline's algorithmic traffic."""

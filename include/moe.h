@@ -324,6 +324,46 @@ MOE_API int moe_mxfp4_mm(int stage, int mode,
                  void* out, int out_fmt, uint8_t* out_scale,
                  void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------ FP4 delta cache
+ * Which experts hold an MXFP4 slot of the delta cache, kept on the device and
+ * updated between steps from the routing, with no host sync (blog
+ * "这个项目我们能学到什么?" on vLLM-Moet: the hottest experts are kept at FP4
+ * precision over the 2-bit base; "GPU作为专家缓存": the GPU holds the hot
+ * experts).  The policy is this library's reading (the pages fix it nowhere):
+ *   counts   uint32 [E] (in/out): per-expert hotness, an integer moving
+ *            average of routed assignments: c <- c - (c >> decay_shift) + n_e,
+ *            n_e = offsets[e+1] - offsets[e] of this step; decay_shift >= 31
+ *            keeps the cumulative count; saturates at 2^32 - 1.  Zero them
+ *            once before the first call.
+ *   the cached set is the S experts of largest count, ties to the lowest id;
+ *   slot_expert int32 [S] (in/out): expert held by slot s, -1 = empty; a
+ *            cached expert that stays in the set keeps its slot, experts that
+ *            leave free theirs, experts that enter take the free slots in
+ *            ascending order, hottest first.  (Entries >= E set BAD_ID and are
+ *            treated as empty.)
+ *   expert_slot int32 [E] (out): the inverse map, -1 = not cached: the map
+ *            moe_w2_mm / moe_mxfp4_mm take as expert_slot.
+ *   promoted int32 [S] (out): the expert that entered slot s in this call, -1
+ *            where the slot kept its expert or stays empty; moe_cache_fill
+ *            copies exactly these.
+ * 1 <= S <= E <= 1024.  One small kernel; stream-ordered with the steps. */
+MOE_API int moe_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_shift, int S,
+                     int32_t* expert_slot, int32_t* slot_expert, int32_t* promoted,
+                     uint32_t* dev_err, void* stream);
+
+/* Copies the stored weights of each promoted expert into its slot: for every
+ * slot s with promoted[s] = e >= 0 and every array a < n_arrays (at most 4,
+ * e.g. W1 nibbles, W1 scales, W2 nibbles, W2 scales):
+ *   dst[a] + s * bytes[a]  <-  src[a] + e * bytes[a]        (bytes[a] bytes)
+ * src, dst and bytes are HOST arrays of n_arrays entries; src[a] and dst[a]
+ * point to device-accessible memory: device memory, or pinned host memory
+ * mapped into the device's address space (the expert store may stay in host
+ * memory and be read over the CPU-GPU link).  Pointers 16-byte aligned,
+ * bytes[a] a multiple of 16.  Slots that were not promoted are not touched,
+ * so steps that use other slots may follow on the same stream. */
+MOE_API int moe_cache_fill(const int32_t* promoted, int S, int n_arrays, const void* const* src, void* const* dst,
+                   const size_t* bytes, void* stream);
+
 /* ------------------------------------------------------------------ combine
  * out[t][n] = sum_{j=0..k-1} w[t][j] * y[inv[t*k+j]][n], accumulated in fp32 in
  * ascending j, then rounded to out_fmt (BF16 or F32).  One owner per output
