@@ -221,6 +221,13 @@ class MoELayer:
         L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
         return b.out
 
+    def capture(self, T: int) -> "LayerGraph":
+        """The whole layer step for T tokens captured once into a CUDA graph
+        (route, permute, the expert matmuls, combine: one graph launch per
+        step, with the library's programmatic launch edges kept); see
+        LayerGraph."""
+        return LayerGraph(self, T)
+
     class _Timer:
         """Event pair around one library call; recorded as timing nodes when
         the step is being captured into a CUDA graph (external events)."""
@@ -345,3 +352,34 @@ class MoELayer:
             else:
                 tot += mx_bytes
         return tot
+
+
+class LayerGraph:
+    """A captured layer step: ``run(x, logits)`` copies the step's inputs into
+    the graph's own input buffers (stream-ordered device copies) and replays
+    the graph; the output is ``out`` (overwritten by every run).  Inputs may
+    be device tensors or pinned host tensors.  The buffers and weights the
+    step uses stay owned by the graph and its layer."""
+
+    def __init__(self, layer: MoELayer, T: int):
+        dev = layer.device
+        self.layer = layer
+        self.x = torch.zeros((T, layer.H), dtype=torch.int16, device=dev)
+        self.logits = torch.zeros((T, layer.E), dtype=torch.float32, device=dev)
+        self.bufs = layer.buffers(T)
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):   # warm once outside the capture (library set-up, smem limits)
+            layer.step(self.x, self.logits, self.bufs)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.out = layer.step(self.x, self.logits, self.bufs)
+        torch.cuda.synchronize(dev)
+
+    def run(self, x: torch.Tensor, logits: torch.Tensor) -> torch.Tensor:
+        self.x.copy_(x, non_blocking=True)
+        self.logits.copy_(logits, non_blocking=True)
+        self.graph.replay()
+        return self.out

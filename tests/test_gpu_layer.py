@@ -136,3 +136,26 @@ def test_prefill_bf16_full_size_sampled():
 
 def test_prefill_fp8_full_size_sampled():
     _check_sampled("prefill_fp8", [5, 16383])
+
+
+@pytest.mark.parametrize("name,mode", [("decode", L.MODE_GEMV), ("tiny", L.MODE_GEMM)])
+def test_captured_layer_graph_matches_the_eager_step(name, mode):
+    """MoELayer.capture: the whole step replayed from one CUDA graph gives the
+    eager step's bits, for a second batch copied into the graph's inputs
+    too, and matches the oracle."""
+    w = synth.get_workload(name)
+    ml, acc, prof = make_layer(w, 0, mode=mode)
+    g = ml.capture(w.T)
+    for bi in range(2):
+        x = synth.make_x(w, 0, tid_offset=bi)
+        lg = synth.make_logits(w, 0, x_bits=x, tid_offset=bi)
+        xd, ld = dev(x.view(np.int16)), dev(lg)
+        out_g = g.run(xd, ld).clone()
+        b = ml.buffers(w.T)
+        out_e = ml.step(xd, ld, b)
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out_e)
+        tok = [0, w.T - 1]
+        ref = M.layer(x, lg, w.k, acc, profile=prof, tokens=tok)
+        err, _ = rel_err(host(out_g)[tok], ref["out"])
+        assert err <= TOL_BF16
