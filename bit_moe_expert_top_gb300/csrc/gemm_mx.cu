@@ -28,10 +28,14 @@
 //               (token n at lane n mod 32 of every lane quarter, column n/32),
 //               and for MXFP4 the weight rows' E8M0 words (row m at lane m,
 //               column m/32)
-//   warps 8-11  epilogue: tcgen05.ld of D_0 / D_1, SwiGLU for FC1, output
-//               rounding (fp32, bf16, or MXFP8: E4M3 codes + E8M0 per 32
-//               outputs, the FP8 path's h), shared staging and 16-byte row
-//               stores
+//   warps 8-15  epilogue, two warps per TMEM lane quarter on alternate
+//               32-token chunks: tcgen05.ld of D_0 / D_1, SwiGLU for FC1,
+//               output rounding (fp32, bf16, or MXFP8: E4M3 codes + E8M0 per
+//               32 outputs, the FP8 path's h; block maxima by a butterfly
+//               reduce-scatter across the warp), shared staging and 16-byte
+//               row stores.  Measured (per-role clock counts): with four
+//               epilogue warps and one shuffle reduction per token the
+//               epilogue, not the MMAs, set the pace
 //   warp 3      allocates and frees TMEM
 //
 // Tiles are walked round-robin by a persistent grid (one CTA per SM) in the
@@ -50,7 +54,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kMxWarps = 12;
+constexpr int kMxWarps = 16;
 constexpr int kMxThreads = kMxWarps * 32;
 constexpr int kKS = 128;        // K elements per stage: 4 MMAs of K = 32, one E8M0 word per row
 constexpr int kMS = 4;          // pipeline stages
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
   uint64_t* empty = full + kMS;                         // [kMS] both blocks' MMAs of the stage done
   uint64_t* sf_full = empty + kMS;                      // [kMS] the stage's scale columns written
   uint64_t* acc_full = sf_full + kMS;
-  uint64_t* acc_empty = acc_full + 1;                   // [2] weight block b's accumulator read
+  uint64_t* acc_empty = acc_full + 1;                   // [2] weight block b's accumulator read (8 warps)
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_empty + 2);
   int* flags = reinterpret_cast<int*>(tmem_base_s + 2);
   int* tile_start = flags + 8;          // [E+1]
@@ -176,8 +180,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       mbar_init(&sf_full[s], 4);
     }
     mbar_init(acc_full, 2);
-    mbar_init(&acc_empty[0], 4);
-    mbar_init(&acc_empty[1], 4);
+    mbar_init(&acc_empty[0], 8);
+    mbar_init(&acc_empty[1], 8);
     flags[0] = 0;
     fence_barrier_init();
   }
@@ -362,24 +366,27 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
     if (!ok) abort_all();
     if (__any_sync(0xffffffffu, nan != 0) && lane == 0) set_err(P.dev_err, MOE_DEVERR_NAN_SCALE);
   } else if (warp >= 8) {
-    // ================= epilogue =================
+    // ================= epilogue (8 warps: two per TMEM lane quarter) =================
+    // Warps q and q + 4 of the group read lanes 32q..32q+31 (outputs) and
+    // take alternate 32-token chunks; a 64-token window of the staging tile is
+    // flushed to global memory with 16-byte row stores by all eight.
     const int q = warp & 3;
-    const int et = tid - 8 * 32;  // 0..127
+    const int eh = (warp - 8) >> 2;  // chunk parity
+    const int et = tid - 8 * 32;     // 0..255
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     const bool f32_out = P.out_fmt == MOE_FMT_F32;
     const bool mx_out = P.out_fmt == MOE_FMT_MXFP8;
     const int ob = mx_out ? 1 : 2;  // staged bytes per output
-    // rows [j0, j1) of the staging tile ([64 tokens][128 outputs]) to global
-    auto flush = [&](int prow0, int j0, int j1, int nbase) {
-      named_bar_sync(1, 128);
+    auto flush = [&](int prow0, int j0, int j1, int nbase) {  // rows [j0, j1) of the window
+      named_bar_sync(1, 256);
       const int pieces = 128 * ob / 16;  // 16-byte pieces per row
-      for (int idx = et; idx < (j1 - j0) * pieces; idx += 128) {
+      for (int idx = et; idx < (j1 - j0) * pieces; idx += 256) {
         const int j = idx / pieces, pc = idx - j * pieces;
         const uint4 v = *reinterpret_cast<const uint4*>(stg + ((j0 + j) & 63) * 128 * ob + pc * 16);
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(P.out) +
                                   (static_cast<size_t>(prow0 + j0 + j) * P.N + nbase) * ob + pc * 16) = v;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
     };
     int t = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++t) {
@@ -394,6 +401,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       tm_fence_after();
       const int p0 = P.offsets[e] + mt * NT;
       const int nvalid = min(NT, P.offsets[e + 1] - p0);
+      // this warp's last chunk: its accumulator reads end there
+      const int nch = (nvalid + 31) / 32;
+      const int last_c = (nch - 1 - eh) >= 0 ? 32 * (((nch - 1 - eh) & ~1) + eh) : -1;
       auto release = [&](int which) {  // 0 / 1: that block, 2: both
         tm_fence_before();
         __syncwarp();
@@ -402,53 +412,74 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
           if (which != 0) mbar_arrive(&acc_empty[1]);
         }
       };
+      if (last_c < 0) release(2);  // no chunk for this warp in this tile
       for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
         const int nbase = fc1 ? blk * 128 : blk * 256 + half * 128;
         const int n = nbase + 32 * q + lane;  // this lane's output
 #pragma unroll 1
-        for (int c = 0; c < nvalid; c += 32) {
-          uint32_t r0[32], r1[32];
-          if (fc1) {
-            tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
-            tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
-          } else {
-            tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
-          }
-          tm_ld_wait();
-          if (c + 32 >= nvalid) release(fc1 ? 2 : half);
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] = fc1 ? silu_fast(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
-          if (f32_out) {
-            float* o = static_cast<float*>(P.out);
+        for (int w0 = 0; w0 < nvalid; w0 += 64) {
+          const int c = w0 + 32 * eh;
+          if (c < nvalid) {
+            uint32_t r0[32], r1[32];
+            if (fc1) {
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
+            } else {
+              tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
+            }
+            tm_ld_wait();
+            if (c == last_c) release(fc1 ? 2 : half);
+            float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c + j < nvalid) o[static_cast<size_t>(p0 + c + j) * P.N + n] = v[j];
-            continue;
-          }
-          if (mx_out) {
-            // MXFP8: token j's block of 32 outputs is this warp's 32 lanes
-            uint32_t myx = 0;
+              v[j] = fc1 ? silu_fast(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
+            if (f32_out) {
+              float* o = static_cast<float*>(P.out);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float m = fabsf(v[j]);
+              for (int j = 0; j < 32; ++j)
+                if (c + j < nvalid) o[static_cast<size_t>(p0 + c + j) * P.N + n] = v[j];
+            } else if (mx_out) {
+              // MXFP8: token j's block of 32 outputs is this warp's 32 lanes.
+              // Block maxima by a butterfly reduce-scatter: afterwards lane L
+              // holds the maximum of token L (31 shuffles for 32 tokens).
+              float a[32];
 #pragma unroll
-              for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-              const int X = mx_scale_exp(m);
-              if (lane == j) myx = static_cast<uint32_t>(X + 127);
-              const uint16_t two = f32x2_to_e4m3x2(v[j] * exp2i(-X), 0.f);
-              stg[((c + j) & 63) * 128 + 32 * q + lane] = static_cast<uint8_t>(two & 0xffu);
+              for (int j = 0; j < 32; ++j) a[j] = fabsf(v[j]);
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) {
+                const bool up = (lane & m) != 0;
+#pragma unroll
+                for (int j = 0; j < m; ++j) {
+                  const float keep = up ? a[j + m] : a[j];
+                  const float send = up ? a[j] : a[j + m];
+                  a[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
+                }
+              }
+              const int X = mx_scale_exp(a[0]);  // token c + lane
+              if (c + lane < nvalid)
+                P.out_scale[static_cast<size_t>(p0 + c + lane) * (P.N / 32) + nbase / 32 + q] =
+                    static_cast<uint8_t>(X + 127);
+              const float inv = exp2i(-X);
+              uint8_t* row = stg + (c & 63) * 128 + 32 * q + lane;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float i0 = __shfl_sync(0xffffffffu, inv, j), i1 = __shfl_sync(0xffffffffu, inv, j + 1);
+                const uint16_t two = f32x2_to_e4m3x2(v[j] * i0, v[j + 1] * i1);
+                row[j * 128] = static_cast<uint8_t>(two & 0xffu);
+                row[(j + 1) * 128] = static_cast<uint8_t>(two >> 8);
+              }
+            } else {
+              uint16_t* row = reinterpret_cast<uint16_t*>(stg) + (c & 63) * 128 + 32 * q + lane;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                uint32_t b2;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(v[j + 1]), "f"(v[j]));
+                row[j * 128] = static_cast<uint16_t>(b2 & 0xffffu);
+                row[(j + 1) * 128] = static_cast<uint16_t>(b2 >> 16);
+              }
             }
-            if (c + lane < nvalid)
-              P.out_scale[static_cast<size_t>(p0 + c + lane) * (P.N / 32) + nbase / 32 + q] = static_cast<uint8_t>(myx);
-          } else {
-            uint16_t* s16 = reinterpret_cast<uint16_t*>(stg);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s16[((c + j) & 63) * 128 + 32 * q + lane] = f32_to_bf16_rne(v[j]);
           }
-          const int cend = min(c + 32, nvalid);
-          if ((c & 63) == 32 || cend == nvalid) flush(p0, c & ~63, cend, nbase);
+          if (!f32_out) flush(p0, w0, min(w0 + 64, nvalid), nbase);
         }
       }
     }
