@@ -13,8 +13,11 @@ The same run also times the other workloads of the metric, each on its own
 layer of weights, as sub-records of the line (``workloads``): prefill_bf16
 (8192 tokens, 2-bit experts on the tensor cores), prefill_fp8 (16384 tokens,
 MXFP4 experts through the FP8 workspace), prefill_fp8_direct (the same
-workload with the MXFP4 experts multiplied as stored, no workspace) and
-mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache entries).
+workload with the MXFP4 experts multiplied as stored, no workspace),
+mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache entries)
+and decode_host (the decode workload with every expert in pinned host memory
+and half of them resident on the device: the routed others are copied over
+the CPU-GPU link each step).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead: whole layer steps of the same workload, its tokens split over one
@@ -150,7 +153,9 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
     from bit_moe_expert_top_gb300.layer import MoELayer
 
     direct = name.endswith("_direct")  # MXFP4 experts multiplied as stored, no FP8 workspace
-    w = synth.get_workload(name[:-len("_direct")] if direct else name)
+    hosted = name.endswith("_host")    # 2-bit experts in host memory, half of them resident on the device
+    base = name[:-len("_direct")] if direct else (name[:-len("_host")] if hosted else name)
+    w = synth.get_workload(base)
     if tokens:
         w = w.replace(T=tokens)
     if experts:
@@ -160,6 +165,9 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
         if direct:
             ml = MoELayer("mxfp4", w.E, w.H, w.I, w.k, device, mx=synth.make_mxfp4_layer(w, seed=0, layer=l),
                           out_fmt=L.FMT_BF16)
+        elif hosted:
+            ml = MoELayer("w2host", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16,
+                          resident=range(0, w.E, 2), stage_slots=w.T * w.k)
         elif w.weights == "w2":
             ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16)
         elif w.weights == "mixed":
@@ -226,13 +234,14 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
         return mls[li].step(xs[i % batches], lgs[i % batches], bufs[li], ev)
 
     # algorithmic work of every (layer, batch) pairing used by the timed steps
-    work_bytes = {}
+    work_bytes, staged = {}, {}
     for i in range(batches):
         li = i % layers
         step(i)
         torch.cuda.synchronize()
         off = bufs[li].offsets.cpu().numpy()
         work_bytes[i] = mls[li].touched_weight_bytes(off)
+        staged[i] = mls[li].staged_bytes(off) if mls[li].fmt == "w2host" else 0
         if L.moe_get_error(bufs[li].dev_err) != 0:
             raise RuntimeError(f"{name}: device error flags set during warm-up")
 
@@ -333,6 +342,13 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
            "tflops": round(tot_flops / (t_max / 1e3) / 1e12, 2),
            "roofline": roof, "kernels_us": kernels_us,
            "gpu_launches": steps * launches_per_step(mls[0], w.T)}
+    if mls[0].fmt == "w2host":
+        sb = sum(staged[i % batches] for i in range(steps))
+        rec["host_resident"] = {"resident_experts": mls[0].R, "staging_slots": mls[0].S,
+                                "staged_bytes_per_step": round(sb / steps),
+                                "link_gbs": round(sb / (t_max / 1e3) / 1e9, 1),
+                                "note": "weights of the routed experts without a device slot, copied from pinned "
+                                        "host memory each step"}
     if clk is not None:
         rec["clocks"] = clk
     if not args.no_e2e:
@@ -417,6 +433,8 @@ def launches_per_step(ml, T):
         return 3 + (1 if mx_tc else 0) + 2 * 2 + 2 * 1
     if ml.fmt == "mxfp4":
         return 6
+    if ml.fmt == "w2host":  # route, permute, stage select, fill, 3 x (table GEMV + summing kernel), combine
+        return 11
     nb = (ml.E + ml.batch - 1) // ml.batch
     return 4 + 4 * nb
 
@@ -622,9 +640,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct"])
+                    choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct",
+                             "decode_host"])
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode",
+    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode,decode_host",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

@@ -28,7 +28,7 @@ EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wai
            "moe_check_bounded_wait", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
-           "moe_combine", "moe_cache_select", "moe_cache_fill"]
+           "moe_combine", "moe_cache_select", "moe_cache_fill", "moe_stage_select", "moe_w2_mm_slots"]
 W2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -61,6 +61,8 @@ _SIGS = {
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _I, _P]),
     "moe_cache_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_cache_fill": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "moe_stage_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
+    "moe_w2_mm_slots": (_I, [_I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _S, _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -217,3 +219,17 @@ def moe_cache_fill(promoted, srcs, dsts, nbytes, stream=None):
     dst_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in dsts])
     by_arr = (ctypes.c_size_t * n)(*[int(b) for b in nbytes])
     _check(lib().moe_cache_fill(_ptr(promoted), S, n, src_arr, dst_arr, by_arr, _stream(stream)))
+
+
+def moe_stage_select(offsets, res_slot, R, weight_slot, staged, dev_err=None, stream=None):
+    E = res_slot.numel()
+    _check(lib().moe_stage_select(_ptr(offsets), E, _ptr(res_slot), R, staged.numel(), _ptr(weight_slot),
+                                  _ptr(staged), _ptr(dev_err), _stream(stream)))
+
+
+def moe_w2_mm_slots(stage, act, codes_k, scales_k, offsets, weight_slot, slot_lo, slot_hi, E, N, K, out, out_fmt,
+                    ws, act_row=None, act_row_div=1, dev_err=None, stream=None):
+    nbytes = ws.numel() * ws.element_size()
+    _check(lib().moe_w2_mm_slots(stage, _ptr(act), act.shape[0], _ptr(act_row), act_row_div, _ptr(codes_k),
+                                 _ptr(scales_k), _ptr(offsets), _ptr(weight_slot), slot_lo, slot_hi, E, N, K,
+                                 _ptr(out), out_fmt, _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))

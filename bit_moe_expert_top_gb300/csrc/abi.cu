@@ -406,6 +406,62 @@ int moe_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_
                      "moe_cache_select");
 }
 
+int moe_stage_select(const int32_t* offsets, int E, const int32_t* res_slot, int R, int S, int32_t* weight_slot,
+                     int32_t* staged, uint32_t* dev_err, void* stream) {
+  if (E < 1 || E > 1024 || R < 0 || S < 1 || S > 1024) return fail(MOE_ERR_ARG, "moe_stage_select: bad shape");
+  if (!offsets || !res_slot || !weight_slot || !staged) return fail(MOE_ERR_ARG, "moe_stage_select: NULL pointer");
+  if (int r = check_device()) return r;
+  return cuda_status(launch_stage_select(offsets, E, res_slot, R, S, weight_slot, staged, dev_err,
+                                         static_cast<cudaStream_t>(stream)),
+                     "moe_stage_select");
+}
+
+int moe_w2_mm_slots(int stage, const void* act, int act_rows, const int32_t* act_row, int act_row_div,
+                    const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
+                    const int32_t* weight_slot, int slot_lo, int slot_hi, int E, int N, int K, void* out, int out_fmt,
+                    void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  if (int r = check_mm("moe_w2_mm_slots", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, offsets, E, N, K, out,
+                       out_fmt, nullptr))
+    return r;
+  if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32) return fail(MOE_ERR_ARG, "moe_w2_mm_slots: out_fmt");
+  if (!codes_k || !scales_k || !weight_slot || !aligned(codes_k, 16) || !aligned(scales_k, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_mm_slots: weights / slot map NULL or misaligned");
+  if (act_rows < 0 || slot_lo < 0 || slot_hi < slot_lo) return fail(MOE_ERR_ARG, "moe_w2_mm_slots: bad rows / slots");
+  if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm_slots: act_row_div < 1");
+  if (!ws || !aligned(ws, 256)) return fail(MOE_ERR_ARG, "moe_w2_mm_slots: needs a 256-byte aligned workspace");
+  MMArgs a{};
+  a.stage = stage;
+  a.act = act;
+  a.act_fmt = MOE_FMT_BF16;
+  a.act_rows = act_rows;
+  a.mode = MOE_MODE_GEMV;
+  a.act_row = act_row;
+  a.act_row_div = act_row ? act_row_div : 1;
+  a.wkind = kW2;
+  a.wq = codes_k;
+  a.wscale = scales_k;
+  a.wslot_of = weight_slot;
+  a.slot_lo = slot_lo;
+  a.slot_hi = slot_hi;
+  a.offsets = offsets;
+  a.expert_begin = 0;
+  a.expert_end = E;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.out_fmt = out_fmt;
+  a.dev_err = dev_err;
+  a.wait = wait_limit();
+  if (!lut_supported(a))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_w2_mm_slots: K is not a multiple of the table GEMV's slice width");
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.ws_rows = lut_workspace_rows(stage, ws_bytes, N, K);
+  if (a.ws_rows < 1) return fail(MOE_ERR_WS_SMALL, "moe_w2_mm_slots: workspace below one row");
+  return cuda_status(launch_lut_gemv(a, ws, static_cast<cudaStream_t>(stream)), "moe_w2_mm_slots");
+}
+
 int moe_cache_fill(const int32_t* promoted, int S, int n_arrays, const void* const* src, void* const* dst,
                    const size_t* bytes, void* stream) {
   if (S < 1 || n_arrays < 1 || n_arrays > 4 || !promoted || !src || !dst || !bytes)

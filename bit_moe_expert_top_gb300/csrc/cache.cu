@@ -108,6 +108,56 @@ __global__ void __launch_bounds__(kSelThreads) cache_select_kernel(const int32_t
   }
 }
 
+// Host-resident experts staged per step: every expert routed in this step
+// that has no resident slot gets a staging slot (R + j, j in ascending
+// expert order); its weights are then copied in (cache_fill_kernel) while the
+// resident experts' matmuls run.
+__global__ void __launch_bounds__(kSelThreads) stage_select_kernel(const int32_t* __restrict__ offsets, int E,
+                                                                   const int32_t* __restrict__ res_slot, int R,
+                                                                   int S, int32_t* __restrict__ weight_slot,
+                                                                   int32_t* __restrict__ staged, uint32_t* dev_err) {
+  __shared__ int warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int cold = 0, rs = -1;
+  if (tid < E) {
+    rs = res_slot[tid];
+    if (rs >= R) {
+      set_err(dev_err, MOE_DEVERR_BAD_ID);
+      rs = -1;
+    }
+    cold = (offsets[tid + 1] > offsets[tid] && rs < 0) ? 1 : 0;
+  }
+  // exclusive prefix of the cold flags over the block (ascending expert id)
+  int incl = cold;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  const int j = before + incl - cold;
+  if (tid < S) staged[tid] = -1;
+  __syncthreads();
+  if (tid < E) {
+    int ws = rs;
+    if (cold) {
+      if (j < S) {
+        ws = R + j;
+        staged[j] = tid;
+      } else {
+        set_err(dev_err, MOE_DEVERR_OVERFLOW);  // more routed cold experts than staging slots: skipped
+        ws = -1;
+      }
+    }
+    weight_slot[tid] = ws;
+  }
+}
+
 struct FillArgs {
   const uint8_t* src[4];
   uint8_t* dst[4];
@@ -138,6 +188,12 @@ cudaError_t launch_cache_select(const int32_t* offsets, int E, uint32_t* counts,
                                 cudaStream_t s) {
   return launch_pdl(cache_select_kernel, dim3(1), dim3(kSelThreads), 0, s, offsets, E, counts, decay_shift, S,
                     expert_slot, slot_expert, promoted, dev_err);
+}
+
+cudaError_t launch_stage_select(const int32_t* offsets, int E, const int32_t* res_slot, int R, int S,
+                                int32_t* weight_slot, int32_t* staged, uint32_t* dev_err, cudaStream_t s) {
+  return launch_pdl(stage_select_kernel, dim3(1), dim3(kSelThreads), 0, s, offsets, E, res_slot, R, S, weight_slot,
+                    staged, dev_err);
 }
 
 cudaError_t launch_cache_fill(const int32_t* promoted, int S, int n, const void* const* src, void* const* dst,

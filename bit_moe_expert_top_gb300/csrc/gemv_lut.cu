@@ -48,7 +48,7 @@ constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kBuildWarps = 16;               // warps that build a segment's tables
 constexpr int kBR = 16;                       // weight rows per batch (4 row quads; 32-row batches measured slower)
 constexpr int kSW = 512;                      // K elements per slice
-constexpr int kPrologue = 8192;               // shared bytes below the table window
+constexpr int kPrologue = 12288;              // shared bytes below the table window
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
@@ -59,6 +59,8 @@ constexpr int kSegCap = 128;
 constexpr int kXBufOff = kSegTabOff + 8 * kSegCap;  // bf16 [2][kSW]
 static_assert(kXBufOff + 2 * kSW * 2 <= kPrologue, "prologue overflow");
 static_assert(4 * (kMaxE + 1) <= kSegTabOff, "prologue overflow");
+constexpr int kSlotTabOff = 8192;             // int [E]: weight slot of each expert
+static_assert(kXBufOff + 2 * kSW * 2 <= kSlotTabOff && kSlotTabOff + 4 * kMaxE <= kPrologue, "prologue overflow");
 
 struct LutParams {
   const uint16_t* act;
@@ -69,6 +71,8 @@ struct LutParams {
   const uint16_t* scales;   // w2l bf16 scales
   const int32_t* select_map;
   int select;
+  const int32_t* wslot;     // expert -> slot of the weight arrays (NULL: slot = expert)
+  int slot_lo, slot_hi;     // with wslot: only experts whose slot lies in [slot_lo, slot_hi)
   const int32_t* offsets;
   int E, N, K, R;           // R = weight rows per expert
   int NSL;                  // K slices
@@ -166,6 +170,7 @@ MOE_D void rs_level2(float2* v, int lane, int m) {
 __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   int* pref = reinterpret_cast<int*>(smem);  // [E+1] selected permuted rows before expert e
+  int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);  // [E] weight slot of expert e
 
   pdl_wait();  // offsets, activations and the scratch belong to earlier kernels
   pdl_trigger();
@@ -190,6 +195,12 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
         bool sel = c > 0;
         if (sel && P.select == 1) sel = P.select_map[e] < 0;
         if (sel && P.select == 2) sel = P.select_map[e] >= 0;
+        int ws = e;
+        if (P.wslot) {
+          ws = P.wslot[e];
+          sel = sel && ws >= P.slot_lo && ws < P.slot_hi;
+        }
+        slot_tab[e] = ws;
         if (sel) n[h] = c;
       }
     }
@@ -263,9 +274,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
     return static_cast<uint32_t>(rb * 4 + q);
   };
   // this lane's code / scale addresses in slice s of expert e
-  auto codes_at = [&](int e, int sl) { return P.codes + e * mat_codes + sl * slice_codes + lane * 16; };
+  auto codes_at = [&](int e, int sl) { return P.codes + slot_tab[e] * mat_codes + sl * slice_codes + lane * 16; };
   auto scales_at = [&](int e, int sl) {
-    return reinterpret_cast<const uint8_t*>(P.scales + e * mat_scales + sl * slice_scales) + (lane >> 1) * 8;
+    return reinterpret_cast<const uint8_t*>(P.scales + slot_tab[e] * mat_scales + sl * slice_scales) + (lane >> 1) * 8;
   };
   auto issue = [&](const uint8_t* gc, const uint8_t* gs, int rb) {
 #pragma unroll
@@ -532,6 +543,9 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   P.scales = static_cast<const uint16_t*>(a.wscale);
   P.select_map = a.select_map;
   P.select = a.select;
+  P.wslot = a.wslot_of;
+  P.slot_lo = a.slot_lo;
+  P.slot_hi = a.slot_hi;
   P.offsets = a.offsets;
   P.E = a.E;
   P.N = a.N;

@@ -91,6 +91,7 @@ struct MMArgs {
   const uint8_t* wq;          // codes / nibbles / e4m3 bytes, [slots][rows][K*bits/8]
   const void* wscale;         // bf16 (w2k) or E8M0 [slots][rows][K/32]; NULL for FP8
   const int32_t* wslot_of;    // expert -> weight slot (nullable: slot = e)
+  int slot_lo, slot_hi;       // 2-bit table GEMV with wslot_of: experts whose slot is in [slot_lo, slot_hi)
   const int32_t* select_map;  // per-expert map read by `select`
   int select;                 // 0: all experts; 1: experts with select_map[e] < 0 (the
                               // 2-bit pass skips delta-cached experts); 2: select_map[e] >= 0
@@ -124,6 +125,8 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s);
 cudaError_t launch_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_shift, int S,
                                 int32_t* expert_slot, int32_t* slot_expert, int32_t* promoted, uint32_t* dev_err,
                                 cudaStream_t s);
+cudaError_t launch_stage_select(const int32_t* offsets, int E, const int32_t* res_slot, int R, int S,
+                                int32_t* weight_slot, int32_t* staged, uint32_t* dev_err, cudaStream_t s);
 cudaError_t launch_cache_fill(const int32_t* promoted, int S, int n, const void* const* src, void* const* dst,
                               const size_t* bytes, cudaStream_t s);
 

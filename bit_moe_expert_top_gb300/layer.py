@@ -17,7 +17,12 @@ with the weight path chosen by the layer's format:
             Day-0适配" §四);
 * ``mxfp4`` the same MXFP4 experts multiplied as they are stored (E2M1
             codes and E8M0 scales straight into the block-scaled tensor core),
-            no workspace.
+            no workspace;
+* ``w2host`` 2-bit experts kept in pinned host memory with a device pool of
+            resident slots plus staging slots: every step the routed experts
+            that are not resident are copied over the CPU-GPU link into the
+            staging slots (moe_stage_select + moe_cache_fill on a side
+            stream) while the resident experts' FC1 runs (moe_w2_mm_slots).
 
 The FP8 formats quantise the token rows to MXFP8 in the gather, and FC1
 writes h as MXFP8 for FC2 ("FC1 + SwiGLU + MXFP8 quant, FC2").
@@ -59,17 +64,20 @@ class StepBuffers:
 class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
-                 out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048):
+                 out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
+                 resident=None, stage_slots: int = 64):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
-        expert_slot int32 [E] (mixed): cache slot of each expert, -1 if none."""
+        expert_slot int32 [E] (mixed): cache slot of each expert, -1 if none.
+        resident (w2host): the expert ids kept in device memory; stage_slots:
+        staging slots for the routed host-resident experts of one step."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
         self.gemm_min_rows = gemm_min_rows
         dev = self.device
-        if fmt in ("w2", "mixed"):
+        if fmt in ("w2", "mixed", "w2host"):
             c1, s1, c2, s2 = w2
             self.c1k = torch.empty(c1.shape, dtype=torch.uint8, device=dev)
             self.s1k = torch.empty(s1.shape, dtype=torch.int16, device=dev)
@@ -80,6 +88,8 @@ class MoELayer:
                 ts = _dev(src_s.view(np.int16), dev)
                 L.moe_w2_repack(tc, ts, src_c.shape[0], src_c.shape[1], K, dc, ds)
                 del tc, ts
+        if fmt == "w2host":
+            self._host_pool(resident, stage_slots)
         if fmt in ("mixed", "fp8", "mxfp4"):
             q1, s1, q2, s2 = mx
             self.q1, self.e1 = _dev(q1, dev), _dev(s1, dev)
@@ -101,6 +111,38 @@ class MoELayer:
             self.batch_slots = [self.ws_slot[b:min(E, b + fp8_batch)].contiguous() for b in range(0, E, fp8_batch)]
             self.conv_stream = torch.cuda.Stream(device=dev)
         torch.cuda.synchronize(dev)
+
+    def _host_pool(self, resident, stage_slots):
+        """w2l weights of every expert to pinned host memory; the device keeps
+        a pool of R resident slots + S staging slots."""
+        E, dev = self.E, self.device
+        full = [self.c1k, self.s1k, self.c2k, self.s2k]
+        self.store = [t.cpu().pin_memory() for t in full]
+        res = np.asarray(sorted(set(int(e) for e in (resident if resident is not None else []))), dtype=np.int64)
+        self.R, self.S = int(res.size), int(stage_slots)
+        self.pool = []
+        for t in full:
+            p = torch.empty((self.R + self.S,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+            if self.R:
+                p[:self.R].copy_(t[torch.from_numpy(res).to(dev)])
+            self.pool.append(p)
+        self.c1k, self.s1k, self.c2k, self.s2k = self.pool
+        self.pool_bytes = [t[0].numel() * t.element_size() for t in self.pool]
+        rs = np.full(E, -1, dtype=np.int32)
+        rs[res] = np.arange(self.R, dtype=np.int32)
+        self.res_slot = _dev(rs, dev)
+        self.weight_slot = torch.empty(E, dtype=torch.int32, device=dev)
+        self.staged = torch.empty(self.S, dtype=torch.int32, device=dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        del full
+
+    def staged_bytes(self, offsets: np.ndarray) -> int:
+        """Bytes the step copies over the CPU-GPU link (w2host): the routed
+        experts without a resident slot."""
+        cnt = np.diff(np.asarray(offsets))
+        rs = self.res_slot.cpu().numpy()
+        n = int(np.sum((cnt > 0) & (rs < 0)))
+        return min(n, self.S) * sum(self.pool_bytes)
 
     # ------------------------------------------------------------ buffers
     def use_gemm(self, T: int) -> bool:
@@ -141,7 +183,7 @@ class MoELayer:
                     if gather or self.fmt == "fp8" or self.mx_tensor_path() else None),
             x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
-            ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed") and not gather else None,
+            ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed", "w2host") and not gather else None,
         )
 
     def _gemv_ws(self, A: int, cap_bytes: int = 1 << 30) -> Optional[torch.Tensor]:
@@ -180,6 +222,8 @@ class MoELayer:
                 L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
                                e2m1=self.q2, e8m0=self.e2, act_scale=b.h_scale, mode=L.MODE_GEMM,
                                dev_err=b.dev_err)
+        elif self.fmt == "w2host":
+            self._host_step(x, b)
         elif self.use_gemm(T):
             L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                           dev_err=b.dev_err)
@@ -220,6 +264,30 @@ class MoELayer:
                                    mode=L.MODE_GEMM if mx_tc else self.mode, dev_err=b.dev_err)
         L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
         return b.out
+
+    def _host_step(self, x, b: StepBuffers):
+        """Grouping, staging of the routed host-resident experts on a side
+        stream, FC1 over the resident experts meanwhile, FC1 over the staged
+        ones once their copy has landed, then FC2 over all (table GEMV)."""
+        E, H, I, k, R, S = self.E, self.H, self.I, self.k, self.R, self.S
+        L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+        L.moe_stage_select(b.offsets, self.res_slot, R, self.weight_slot, self.staged, dev_err=b.dev_err)
+        main = torch.cuda.current_stream(self.device)
+        cs = self.copy_stream
+        cs.wait_stream(main)
+        L.moe_cache_fill(self.staged, self.store, [p[R:] for p in self.pool], self.pool_bytes, stream=cs)
+        landed = torch.cuda.Event()
+        landed.record(cs)
+        with self._timed("w2_fc1"):
+            if R:
+                L.moe_w2_mm_slots(L.STAGE_FC1_SWIGLU, x, self.c1k, self.s1k, b.offsets, self.weight_slot, 0, R, E, I,
+                                  H, b.h, L.FMT_BF16, b.ws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
+            main.wait_event(landed)
+            L.moe_w2_mm_slots(L.STAGE_FC1_SWIGLU, x, self.c1k, self.s1k, b.offsets, self.weight_slot, R, R + S, E,
+                              I, H, b.h, L.FMT_BF16, b.ws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
+        with self._timed("w2_fc2"):
+            L.moe_w2_mm_slots(L.STAGE_FC2, b.h, self.c2k, self.s2k, b.offsets, self.weight_slot, 0, R + S, E, H, I,
+                              b.y, L.FMT_BF16, b.ws, dev_err=b.dev_err)
 
     def capture(self, T: int) -> "LayerGraph":
         """The whole layer step for T tokens captured once into a CUDA graph

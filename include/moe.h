@@ -351,6 +351,39 @@ MOE_API int moe_cache_select(const int32_t* offsets, int E, uint32_t* counts, in
                      int32_t* expert_slot, int32_t* slot_expert, int32_t* promoted,
                      uint32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------ host-resident experts
+ * Experts kept in host memory, staged into device memory per step (blog
+ * "这个项目我们能学到什么?" on vLLM-Moet: the GPU as a cache of hot experts,
+ * the rest fetched as needed; vLLM-Moet README, "MoET hybrid"): a pool of
+ * R + S weight slots in device memory, slots [0, R) hold resident experts,
+ * slots [R, R + S) are staging slots refilled every step.
+ *   res_slot    int32 [E]: resident slot of each expert, -1 = host-resident
+ *               (an entry >= R sets BAD_ID and counts as host-resident)
+ *   weight_slot int32 [E] (out): the slot each routed expert is read from
+ *               this step: its resident slot, or R + j for the j-th routed
+ *               host-resident expert (ascending expert id); -1 when more than
+ *               S host-resident experts are routed (OVERFLOW; skipped)
+ *   staged      int32 [S] (out): the expert to copy into staging slot R + j,
+ *               -1 = unused; pass it to moe_cache_fill with the store's
+ *               arrays as src and the pool's slot-R addresses as dst
+ * 1 <= E <= 1024, 1 <= S <= 1024.  One small kernel. */
+MOE_API int moe_stage_select(const int32_t* offsets, int E, const int32_t* res_slot, int R, int S,
+                     int32_t* weight_slot, int32_t* staged, uint32_t* dev_err, void* stream);
+
+/* The 2-bit table GEMV of moe_w2_mm (stage FC1 or FC2, bf16 activations,
+ * BF16 or F32 output) with the weights addressed through a slot map: expert
+ * e is read from slot weight_slot[e] of the w2l arrays codes_k / scales_k
+ * (slot-major, the per-expert sizes of moe_w2_repack), and only experts whose
+ * slot lies in [slot_lo, slot_hi) are computed (rows of the others are left
+ * untouched), so the resident and the staged experts of a step can run as two
+ * calls around the staging copy.  Outputs are bit-identical to moe_w2_mm's
+ * for the same rows.  Needs the table GEMV's shapes (K a multiple of 512,
+ * else MOE_ERR_UNSUPPORTED) and its workspace (ws, ws_bytes as moe_w2_mm). */
+MOE_API int moe_w2_mm_slots(int stage, const void* act, int act_rows, const int32_t* act_row, int act_row_div,
+                    const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
+                    const int32_t* weight_slot, int slot_lo, int slot_hi, int E, int N, int K,
+                    void* out, int out_fmt, void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
+
 /* Copies the stored weights of each promoted expert into its slot: for every
  * slot s with promoted[s] = e >= 0 and every array a < n_arrays (at most 4,
  * e.g. W1 nibbles, W1 scales, W2 nibbles, W2 scales):
