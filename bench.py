@@ -410,6 +410,8 @@ def run_gpu(args):
         "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values()),
         "clocks": head.get("clocks"),
     }
+    if "host_resident" in head:
+        res["host_resident"] = head["host_resident"]
     if subs:
         res["workloads"] = subs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

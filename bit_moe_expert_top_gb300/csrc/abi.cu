@@ -131,17 +131,13 @@ int moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, 
 }
 
 size_t moe_permute_workspace_size(int T, int k, int E) {
-  (void)T;
-  (void)k;
-  (void)E;
-  return 0;
+  if (T <= 0 || k < 1 || E < 1 || E > 1024 || static_cast<int64_t>(T) * k >= (1LL << 31)) return 0;
+  return permute_workspace_bytes(T * k, E);
 }
 
 int moe_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
                 const uint16_t* x, int H, int act_fmt, void* x_perm, uint8_t* x_perm_scale, void* ws,
                 size_t ws_bytes, uint32_t* dev_err, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || static_cast<int64_t>(T) * k >= (1LL << 31))
     return fail(MOE_ERR_ARG, "moe_permute: bad shape");
   if (!offsets || (T > 0 && (!ids || !perm || !inv))) return fail(MOE_ERR_ARG, "moe_permute: NULL pointer");
@@ -155,8 +151,9 @@ int moe_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32
   }
   if (int r = check_device()) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_permute(ids, T, k, E, offsets, perm, inv, dev_err, s);
-  if (e == cudaSuccess && act_fmt != MOE_FMT_NONE) e = launch_gather(x, perm, T * k, k, H, act_fmt, x_perm, x_perm_scale, s);
+  if (ws && !aligned(ws, 16)) return fail(MOE_ERR_ARG, "moe_permute: ws not 16-byte aligned");
+  cudaError_t e = launch_permute(ids, T, k, E, offsets, perm, inv, ws, ws_bytes, dev_err, s);
+  if (e == cudaSuccess && act_fmt != MOE_FMT_NONE) e = launch_gather(x, inv, T, k, H, act_fmt, x_perm, x_perm_scale, s);
   return cuda_status(e, "moe_permute");
 }
 

@@ -171,13 +171,22 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const int32_t* __restri
   const int s = blockIdx.y;
   const int e = promoted[s];
   if (e < 0) return;
+  // four independent 16-byte loads in flight per thread: the source may be
+  // host memory behind the CPU-GPU link, where latency is long
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (int a = 0; a < F.n; ++a) {
     const size_t n16 = F.bytes[a] / 16;
     const uint4* src = reinterpret_cast<const uint4*>(F.src[a] + static_cast<size_t>(e) * F.bytes[a]);
     uint4* dst = reinterpret_cast<uint4*>(F.dst[a] + static_cast<size_t>(s) * F.bytes[a]);
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x)
-      dst[i] = __ldcs(src + i);
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[i + u * stride] = v[u];
+    }
+    for (; i < n16; i += stride) dst[i] = __ldcs(src + i);
   }
 }
 

@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
   } else if (warp >= 4 && warp < 8) {
     // ================= scale factors into TMEM =================
     // The words of a stage are loaded kPF stages ahead (a register ring), so
-    // the L2 round trip of the scale loads overlaps the MMAs of the stages
-    // in between; a warp can run at most kMS stages ahead of the MMAs anyway.
-    constexpr int kPF = kMS;
+    // the round trip of the scale loads (strided rows, from HBM on a weight
+    // block's first tile) overlaps the MMAs of the stages in between.
+    constexpr int kPF = 8;
     const int q = warp & 3;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     if (AF == kAE4M3) tm_st1(tl + kSFU + q, 0x7F7F7F7Fu);  // 2^0 for every weight row and k-block

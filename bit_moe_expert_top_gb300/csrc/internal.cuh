@@ -53,8 +53,10 @@ long long wait_limit();
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
                          cudaStream_t s);
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
-                           uint32_t* dev_err, cudaStream_t s);
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, int H, int act_fmt, void* x_perm,
+                           void* ws, size_t ws_bytes, uint32_t* dev_err, cudaStream_t s);
+// workspace of the multi-CTA grouping (0: the single-CTA kernel does it)
+size_t permute_workspace_bytes(int A, int E);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int T, int k, int H, int act_fmt, void* x_perm,
                           uint8_t* x_perm_scale, cudaStream_t s);
 cudaError_t launch_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols, void* rows,
                              cudaStream_t s);

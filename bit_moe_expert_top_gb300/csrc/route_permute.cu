@@ -233,9 +233,179 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   }
 }
 
+// Multi-CTA grouping for large A (prefill): block b owns the contiguous
+// assignments [b*CB, (b+1)*CB).  permute_count: per-block expert counts
+// (each warp counts its 32-id tiles as above, the block adds its warps);
+// permute_scan (one CTA): per expert, the exclusive prefix over blocks plus
+// the expert's group start; permute_place: each block recounts per warp,
+// takes its warps' exclusive prefix on top of the block's base and writes
+// perm/inv in increasing assignment order within each expert (stable, the
+// same result as the single-CTA kernel).
+constexpr int kPermCB = 4096;  // assignments per block
+
+// per-warp counts of the warp's slice [beg, end) into h (this warp's row)
+MOE_D bool perm_count_warp(const int32_t* __restrict__ ids, int beg, int end, int E, int* h, int lane) {
+  const unsigned lt_mask = (1u << lane) - 1u;
+  bool bad = false;
+  for (int base0 = beg; base0 < end; base0 += 32 * kPermU) {
+    int ev[kPermU];
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      const int a = base0 + 32 * u + lane;
+      ev[u] = (a < end) ? ids[a] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      if (base0 + 32 * u >= end) break;  // warp-uniform
+      const int a = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (a < end && (e < 0 || e >= E)) {
+        bad = true;
+        e = -1;
+      }
+      const int key = (e >= 0) ? e : (E + lane);
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      if (e >= 0 && (m & lt_mask) == 0) h[e] += __popc(m);
+      __syncwarp();
+    }
+  }
+  return bad;
+}
+
+// positions of the warp's slice from the running bases in h (this warp's row)
+MOE_D void perm_place_warp(const int32_t* __restrict__ ids, int beg, int end, int E, int* h, int lane,
+                           int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base0 = beg; base0 < end; base0 += 32 * kPermU) {
+    int ev[kPermU];
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      const int a = base0 + 32 * u + lane;
+      ev[u] = (a < end) ? ids[a] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPermU; ++u) {
+      if (base0 + 32 * u >= end) break;
+      const int a = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (a < end && (e < 0 || e >= E)) e = -1;
+      const int key = (e >= 0) ? e : (E + lane);
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      int pos = -1;
+      if (e >= 0) pos = h[e] + __popc(m & lt_mask);
+      __syncwarp();
+      if (e >= 0 && (m & lt_mask) == 0) h[e] += __popc(m);
+      __syncwarp();
+      if (a < end) {
+        inv[a] = pos;
+        if (pos >= 0) perm[pos] = a;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ ids, int A, int E,
+                                                             int32_t* __restrict__ blk, uint32_t* dev_err) {
+  extern __shared__ int s_perm[];  // [32][E]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b0 = blockIdx.x * kPermCB, b1 = min(A, b0 + kPermCB);
+  const int wc = kPermCB / kPermWarps;
+  for (int i = tid; i < kPermWarps * E; i += blockDim.x) s_perm[i] = 0;
+  __syncthreads();
+  const bool bad = perm_count_warp(ids, b0 + warp * wc, min(b1, b0 + (warp + 1) * wc), E, s_perm + warp * E, lane);
+  if (bad) set_err(dev_err, MOE_DEVERR_BAD_ID);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < kPermWarps; ++w) c += s_perm[w * E + e];
+    blk[static_cast<size_t>(blockIdx.x) * E + e] = c;
+  }
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ blk, int nb, int E,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int warp_sums[32];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int run = 0;
+  if (tid < E)
+    for (int b = 0; b < nb; ++b) {
+      const int c = blk[static_cast<size_t>(b) * E + tid];
+      blk[static_cast<size_t>(b) * E + tid] = run;
+      run += c;
+    }
+  const int v = tid < E ? run : 0;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sums[w];
+  const int excl = before + incl - v;
+  if (tid < E) {
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+    for (int b = 0; b < nb; ++b) blk[static_cast<size_t>(b) * E + tid] += excl;
+  }
+}
+
+__global__ void __launch_bounds__(1024) permute_place_kernel(const int32_t* __restrict__ ids, int A, int E,
+                                                             const int32_t* __restrict__ blk,
+                                                             int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int s_perm[];  // [32][E]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b0 = blockIdx.x * kPermCB, b1 = min(A, b0 + kPermCB);
+  const int wc = kPermCB / kPermWarps;
+  const int beg = b0 + warp * wc, end = min(b1, b0 + (warp + 1) * wc);
+  for (int i = tid; i < kPermWarps * E; i += blockDim.x) s_perm[i] = 0;
+  __syncthreads();
+  perm_count_warp(ids, beg, end, E, s_perm + warp * E, lane);
+  __syncthreads();
+  // per expert: exclusive prefix over the block's warps on top of the block's base
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = blk[static_cast<size_t>(blockIdx.x) * E + e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = s_perm[w * E + e];
+      s_perm[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  perm_place_warp(ids, beg, end, E, s_perm + warp * E, lane, perm, inv);
+}
+
+size_t permute_workspace_bytes(int A, int E) {
+  if (A < 2 * kPermCB) return 0;  // one CTA does it
+  const size_t nb = (static_cast<size_t>(A) + kPermCB - 1) / kPermCB;
+  return nb * static_cast<size_t>(E) * sizeof(int32_t);
+}
+
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* perm, int32_t* inv,
-                           uint32_t* dev_err, cudaStream_t s) {
+                           void* ws, size_t ws_bytes, uint32_t* dev_err, cudaStream_t s) {
   const int A = T * k;
+  const size_t need = permute_workspace_bytes(A, E);
+  if (need > 0 && ws != nullptr && ws_bytes >= need) {
+    const int nb = (A + kPermCB - 1) / kPermCB;
+    const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int);
+    int32_t* blk = static_cast<int32_t*>(ws);
+    cudaError_t e = set_smem_limit(permute_count_kernel, static_cast<int>(kPermWarps * 1024 * sizeof(int)));
+    if (e == cudaSuccess) e = set_smem_limit(permute_place_kernel, static_cast<int>(kPermWarps * 1024 * sizeof(int)));
+    if (e == cudaSuccess) e = launch_pdl(permute_count_kernel, dim3(nb), dim3(1024), smem, s, ids, A, E, blk, dev_err);
+    if (e == cudaSuccess) e = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, blk, nb, E, offsets);
+    if (e == cudaSuccess)
+      e = launch_pdl(permute_place_kernel, dim3(nb), dim3(1024), smem, s, ids, A, E,
+                     static_cast<const int32_t*>(blk), perm, inv);
+    return e;
+  }
   const size_t smem = static_cast<size_t>(kPermWarps + 1) * E * sizeof(int);
   cudaError_t e = set_smem_limit(permute_kernel, static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int)));
   if (e != cudaSuccess) return e;
@@ -243,16 +413,36 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
 }
 
 // ------------------------------------------------------------------ gather
-__global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
-                                   int H, uint16_t* __restrict__ xp) {
+// Token-major: a warp takes one (token, 1024-element chunk) unit, reads the
+// token's activations once and writes them to the k permuted rows of that
+// token (inv of its k assignments), so each token row is read from HBM once
+// and, for MXFP8, quantised once.
+__global__ void scatter_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv, int T, int k,
+                                    int H, uint16_t* __restrict__ xp) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
-  const int vec = H / 8;  // uint4 per row
-  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(perm[p] / k) * H);
-    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(p) * H);
-    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+  const int nch = (H + 1023) / 1024;
+  const int64_t units = static_cast<int64_t>(T) * nch;
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); u0 < units;
+       u0 += static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5)) {
+    const int t = static_cast<int>(u0 / nch), base0 = static_cast<int>(u0 - static_cast<int64_t>(t) * nch) * 1024;
+    const uint16_t* src = x + static_cast<size_t>(t) * H;
+    uint4 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e0 = base0 + 256 * u + lane * 8;
+      if (e0 < H) raw[u] = __ldg(reinterpret_cast<const uint4*>(src + e0));
+    }
+    for (int j = 0; j < k; ++j) {
+      const int p = inv[static_cast<size_t>(t) * k + j];
+      if (p < 0) continue;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e0 = base0 + 256 * u + lane * 8;
+        if (e0 < H) *reinterpret_cast<uint4*>(xp + static_cast<size_t>(p) * H + e0) = raw[u];
+      }
+    }
   }
 }
 
@@ -260,80 +450,95 @@ __global__ void gather_bf16_kernel(const uint16_t* __restrict__ x, const int32_t
 // elements, 4 lanes form one block of 32 (block max by two shuffles).
 // AS_BF16: write each element's MXFP8 value q * 2^X as bf16 instead of q + X.
 template <bool AS_BF16>
-__global__ void gather_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int A, int k,
-                                    int H, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+__global__ void scatter_mxfp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv, int T, int k,
+                                     int H, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
-  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < A; p += gridDim.x * (blockDim.x >> 5)) {
-    const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
-    // four 256-element chunks per round: their loads are in flight together
-    for (int base0 = 0; base0 < H; base0 += 1024) {
-      uint4 raw[4];
+  const int nch = (H + 1023) / 1024;
+  const int64_t units = static_cast<int64_t>(T) * nch;
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); u0 < units;
+       u0 += static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5)) {
+    const int t = static_cast<int>(u0 / nch), base0 = static_cast<int>(u0 - static_cast<int64_t>(t) * nch) * 1024;
+    const uint16_t* src = x + static_cast<size_t>(t) * H;
+    uint4 raw[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e0 = base0 + 256 * u + lane * 8;
-        if (e0 < H) raw[u] = __ldg(reinterpret_cast<const uint4*>(src + e0));
+    for (int u = 0; u < 4; ++u) {
+      const int e0 = base0 + 256 * u + lane * 8;
+      if (e0 < H) raw[u] = __ldg(reinterpret_cast<const uint4*>(src + e0));
+    }
+    // quantise the chunk once: per lane 4 x 8 elements -> 4 x (8 codes, or 8 bf16 values) + the block scales
+    uint2 codes[4];
+    uint4 vals[4];
+    uint32_t xs[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e0 = base0 + 256 * u + lane * 8;
+      const bool ok = e0 < H;
+      float f[8];
+      float amax = 0.f;
+      const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = ok ? __uint_as_float(wv[i] << 16) : 0.f;
+        f[2 * i + 1] = ok ? __uint_as_float(wv[i] & 0xffff0000u) : 0.f;
+        amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
       }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int X = mx_scale_exp(amax);
+      const float iv = exp2i(-X);
+      uint32_t packed[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t lo = f32x2_to_e4m3x2(f[4 * i] * iv, f[4 * i + 1] * iv);
+        uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * iv, f[4 * i + 3] * iv);
+        packed[i] = lo | (hi << 16);
+      }
+      codes[u] = make_uint2(packed[0], packed[1]);
+      xs[u] = static_cast<uint32_t>(X + 127);
+      if (AS_BF16) {
+        const float sc2 = exp2i(X);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 v = e4m3x2_to_f32x2(static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1))));
+          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(v.y * sc2), "f"(v.x * sc2));
+        }
+        vals[u] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      const int p = inv[static_cast<size_t>(t) * k + j];
+      if (p < 0) continue;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e0 = base0 + 256 * u + lane * 8;
-        if (base0 + 256 * u >= H) break;  // warp-uniform
-        const bool ok = e0 < H;
-        float f[8];
-        float amax = 0.f;
-        if (ok) {
-          const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(wv[i] << 16);
-            f[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
-            amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-          }
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        if (ok) {
-          const int X = mx_scale_exp(amax);
-          const float inv = exp2i(-X);
-          uint32_t packed[2];
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            uint32_t lo = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
-            uint32_t hi = f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-            packed[i] = lo | (hi << 16);
-          }
-          if (AS_BF16) {
-            const float sc2 = exp2i(X);
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 v = e4m3x2_to_f32x2(static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1))));
-              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(v.y * sc2), "f"(v.x * sc2));
-            }
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + static_cast<size_t>(p) * H + e0) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-          } else {
-            *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = make_uint2(packed[0], packed[1]);
-            if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(X + 127);
-          }
+        if (e0 >= H) continue;
+        if (AS_BF16) {
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + static_cast<size_t>(p) * H + e0) = vals[u];
+        } else {
+          *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * H + e0) = codes[u];
+          if ((lane & 3) == 0) sc[static_cast<size_t>(p) * (H / 32) + e0 / 32] = static_cast<uint8_t>(xs[u]);
         }
       }
     }
   }
 }
 
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int A, int k, int H, int act_fmt, void* x_perm,
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int T, int k, int H, int act_fmt, void* x_perm,
                           uint8_t* x_perm_scale, cudaStream_t s) {
-  if (A == 0) return cudaSuccess;
-  const int blocks = min((A + 7) / 8, device_info().sms * 8);
+  if (T == 0) return cudaSuccess;
+  const int64_t units = static_cast<int64_t>(T) * ((H + 1023) / 1024);
+  const int64_t cap = static_cast<int64_t>(device_info().sms) * 8;
+  const int blocks = static_cast<int>((units + 7) / 8 < cap ? (units + 7) / 8 : cap);
   if (act_fmt == MOE_FMT_BF16)
-    return launch_pdl(gather_bf16_kernel, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+    return launch_pdl(scatter_bf16_kernel, dim3(blocks), dim3(256), 0, s, x, inv, T, k, H,
                       static_cast<uint16_t*>(x_perm));
   if (act_fmt == MOE_FMT_MXFP8_BF16)
-    return launch_pdl(gather_mxfp8_kernel<true>, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+    return launch_pdl(scatter_mxfp8_kernel<true>, dim3(blocks), dim3(256), 0, s, x, inv, T, k, H,
                       static_cast<uint8_t*>(x_perm), static_cast<uint8_t*>(nullptr));
-  return launch_pdl(gather_mxfp8_kernel<false>, dim3(blocks), dim3(256), 0, s, x, perm, A, k, H,
+  return launch_pdl(scatter_mxfp8_kernel<false>, dim3(blocks), dim3(256), 0, s, x, inv, T, k, H,
                     static_cast<uint8_t*>(x_perm), x_perm_scale);
 }
 

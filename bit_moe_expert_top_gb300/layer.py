@@ -59,6 +59,7 @@ class StepBuffers:
     x_perm_scale: Optional[torch.Tensor]
     dev_err: torch.Tensor
     ws: Optional[torch.Tensor] = None
+    pws: Optional[torch.Tensor] = None   # grouping scratch of large steps (multi-CTA)
 
 
 class MoELayer:
@@ -184,7 +185,17 @@ class MoELayer:
             x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
             ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed", "w2host") and not gather else None,
+            pws=self._permute_ws(T),
         )
+
+    def _permute(self, b: StepBuffers, **kw):
+        """moe_permute with the step's grouping scratch (multi-CTA when large)."""
+        n = 0 if b.pws is None else b.pws.numel() * b.pws.element_size()
+        L.moe_permute(b.ids, self.E, b.offsets, b.perm, b.inv, ws=b.pws, ws_bytes=n, **kw)
+
+    def _permute_ws(self, T: int) -> Optional[torch.Tensor]:
+        n = L.moe_permute_workspace_size(T, self.k, self.E)
+        return torch.empty((n + 3) // 4, dtype=torch.int32, device=self.device) if n else None
 
     def _gemv_ws(self, A: int, cap_bytes: int = 1 << 30) -> Optional[torch.Tensor]:
         """Scratch of the 2-bit decode GEMV (FC1 and FC2 share it: the calls
@@ -208,11 +219,11 @@ class MoELayer:
         L.moe_route(logits, k, b.ids, b.w, b.dev_err)
         if self.fmt == "fp8":
             tc = self.use_gemm(T)
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
+            self._permute(b, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
                           x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
             self._fp8_experts(b, tc)
         elif self.fmt == "mxfp4":
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
+            self._permute(b, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm,
                           x_perm_scale=b.x_perm_scale, dev_err=b.dev_err)
             with self._timed("mx4_fc1_gemm"):
                 L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h, L.FMT_MXFP8,
@@ -225,7 +236,7 @@ class MoELayer:
         elif self.fmt == "w2host":
             self._host_step(x, b)
         elif self.use_gemm(T):
-            L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
+            self._permute(b, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                           dev_err=b.dev_err)
             with self._timed("w2_fc1_gemm"):
                 L.moe_w2_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
@@ -236,10 +247,10 @@ class MoELayer:
         else:
             mx_tc = self.mx_tensor_path()
             if mx_tc:  # the cache experts' matmuls read gathered rows
-                L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
+                self._permute(b, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                               dev_err=b.dev_err)
             else:
-                L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+                self._permute(b, dev_err=b.dev_err)
             with self._timed("w2_fc1"):
                 L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
                             L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
@@ -270,7 +281,7 @@ class MoELayer:
         stream, FC1 over the resident experts meanwhile, FC1 over the staged
         ones once their copy has landed, then FC2 over all (table GEMV)."""
         E, H, I, k, R, S = self.E, self.H, self.I, self.k, self.R, self.S
-        L.moe_permute(b.ids, E, b.offsets, b.perm, b.inv, dev_err=b.dev_err)
+        self._permute(b, dev_err=b.dev_err)
         L.moe_stage_select(b.offsets, self.res_slot, R, self.weight_slot, self.staged, dev_err=b.dev_err)
         main = torch.cuda.current_stream(self.device)
         cs = self.copy_stream

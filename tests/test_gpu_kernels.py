@@ -134,7 +134,7 @@ def test_route_zero_tokens_and_bad_args():
 # ----------------------------------------------------------------- grouping
 
 @pytest.mark.parametrize("E,T,k", [(8, 16, 2), (384, 8, 8), (384, 64, 8), (384, 8192, 8), (256, 16384, 8),
-                                   (5, 1, 5), (1024, 3, 32), (7, 1000, 1)])
+                                   (5, 1, 5), (1024, 3, 32), (7, 1000, 1), (1024, 9000, 4), (3, 4099, 2)])
 def test_permute_matches_oracle(E, T, k):
     g = np.random.default_rng(E * 7 + T)
     logits = g.random((T, E)).astype(np.float32)
@@ -142,13 +142,17 @@ def test_permute_matches_oracle(E, T, k):
     ids, _, _ = M.route(logits, k)
     off, perm, inv = M.permute(ids, E)
     A = T * k
-    go = torch.empty(E + 1, dtype=torch.int32, device=DEV)
-    gp = torch.empty(A, dtype=torch.int32, device=DEV)
-    gv = torch.empty(A, dtype=torch.int32, device=DEV)
-    L.moe_permute(dev(ids), E, go, gp, gv)
-    assert np.array_equal(host(go), off)
-    assert np.array_equal(host(gp), perm)
-    assert np.array_equal(host(gv), inv)
+    nws = L.moe_permute_workspace_size(T, k, E)
+    assert (nws > 0) == (A >= 8192)                   # large groupings run on many CTAs
+    for use_ws in ([False, True] if nws else [False]):
+        go = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+        gp = torch.full((A,), -7, dtype=torch.int32, device=DEV)
+        gv = torch.full((A,), -7, dtype=torch.int32, device=DEV)
+        ws = torch.full(((nws + 3) // 4,), -7, dtype=torch.int32, device=DEV) if use_ws else None
+        L.moe_permute(dev(ids), E, go, gp, gv, ws=ws, ws_bytes=nws if use_ws else 0)
+        assert np.array_equal(host(go), off)
+        assert np.array_equal(host(gp), perm)
+        assert np.array_equal(host(gv), inv)
 
 
 def test_permute_bad_ids_flagged():
