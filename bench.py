@@ -154,7 +154,11 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
 
     direct = name.endswith("_direct")  # MXFP4 experts multiplied as stored, no FP8 workspace
     hosted = name.endswith("_host")    # 2-bit experts in host memory, half of them resident on the device
-    base = name[:-len("_direct")] if direct else (name[:-len("_host")] if hosted else name)
+    fused = name.endswith("_fused")    # FC1 and FC2 of the 2-bit decode in one cooperative launch
+    base = name
+    for suf in ("_direct", "_host", "_fused"):
+        if name.endswith(suf):
+            base = name[:-len(suf)]
     w = synth.get_workload(base)
     if tokens:
         w = w.replace(T=tokens)
@@ -169,7 +173,8 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
             ml = MoELayer("w2host", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16,
                           resident=range(0, w.E, 2), stage_slots=w.T * w.k)
         elif w.weights == "w2":
-            ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16)
+            ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16,
+                          fused=fused)
         elif w.weights == "mixed":
             ml = MoELayer("mixed", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l),
                           mx=synth.make_mxfp4_layer(w, n=w.n_hot, seed=0, layer=l),
@@ -428,6 +433,8 @@ def launches_per_step(ml, T):
     table GEMV with its summing kernel (2-bit decode) or one tensor-core
     kernel, plus two workspace conversions per expert batch on the FP8 path."""
     tc = ml.use_gemm(T)
+    if ml.fmt == "w2" and ml.fused and not tc:  # route, permute, fused FC1+FC2 (+ its counter memset), combine
+        return 4
     if ml.fmt == "w2":
         return 6 if tc else 7
     if ml.fmt == "mixed":
@@ -643,9 +650,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct",
-                             "decode_host"])
+                             "decode_host", "decode_fused"])
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--sub", default="prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode,decode_host",
+    ap.add_argument("--sub", default="decode_fused,prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode,"
+                                     "decode_host",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

@@ -28,7 +28,8 @@ EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wai
            "moe_check_bounded_wait", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
-           "moe_combine", "moe_cache_select", "moe_cache_fill", "moe_stage_select", "moe_w2_mm_slots"]
+           "moe_combine", "moe_cache_select", "moe_cache_fill", "moe_stage_select", "moe_w2_mm_slots",
+           "moe_w2_decode_fused_workspace_size", "moe_w2_decode_fused"]
 W2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -62,6 +63,8 @@ _SIGS = {
     "moe_cache_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_cache_fill": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "moe_stage_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
+    "moe_w2_decode_fused_workspace_size": (_S, [_I, _I, _I]),
+    "moe_w2_decode_fused": (_I, [_P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _S, _P, _P]),
     "moe_w2_mm_slots": (_I, [_I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _S, _P, _P]),
 }
 
@@ -233,3 +236,15 @@ def moe_w2_mm_slots(stage, act, codes_k, scales_k, offsets, weight_slot, slot_lo
     _check(lib().moe_w2_mm_slots(stage, _ptr(act), act.shape[0], _ptr(act_row), act_row_div, _ptr(codes_k),
                                  _ptr(scales_k), _ptr(offsets), _ptr(weight_slot), slot_lo, slot_hi, E, N, K,
                                  _ptr(out), out_fmt, _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))
+
+
+def moe_w2_decode_fused_workspace_size(rows, H, I) -> int:
+    return int(lib().moe_w2_decode_fused_workspace_size(rows, H, I))
+
+
+def moe_w2_decode_fused(x, codes1, scales1, codes2, scales2, offsets, E, H, I, h, y, y_fmt, ws, act_row=None,
+                        act_row_div=1, expert_slot=None, dev_err=None, stream=None):
+    nbytes = ws.numel() * ws.element_size()
+    _check(lib().moe_w2_decode_fused(_ptr(x), x.shape[0], _ptr(act_row), act_row_div, _ptr(codes1), _ptr(scales1),
+                                     _ptr(codes2), _ptr(scales2), _ptr(offsets), _ptr(expert_slot), E, H, I,
+                                     _ptr(h), _ptr(y), y_fmt, _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))

@@ -337,6 +337,76 @@ int moe_w2_mm_noalloc(int stage, const void* act, int act_rows, const int32_t* a
   return cuda_status(launch_lut_gemv_noalloc(a, rows, static_cast<cudaStream_t>(stream)), "moe_w2_mm_noalloc");
 }
 
+size_t moe_w2_decode_fused_workspace_size(int rows, int H, int I) {
+  if (rows <= 0 || H <= 0 || I <= 0 || H % 128 || I % 128) return 0;
+  const size_t a = lut_workspace_bytes(MOE_STAGE_FC1_SWIGLU, rows, I, H);
+  const size_t b = lut_workspace_bytes(MOE_STAGE_FC2, rows, H, I);
+  if (a == 0 || b == 0) return 0;
+  return 256 + (a > b ? a : b);
+}
+
+int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_row, int act_row_div, const uint8_t* codes1,
+                        const uint16_t* scales1, const uint8_t* codes2, const uint16_t* scales2,
+                        const int32_t* offsets, const int32_t* expert_slot, int E, int H, int I, void* h, void* y,
+                        int y_fmt, void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  if (int r = check_mm("moe_w2_decode_fused", MOE_STAGE_FC1_SWIGLU, MOE_MODE_GEMV, x, MOE_FMT_BF16, nullptr, offsets,
+                       E, I, H, h, MOE_FMT_BF16, nullptr))
+    return r;
+  if (!y || !aligned(h, 16) || (y_fmt != MOE_FMT_BF16 && y_fmt != MOE_FMT_F32))
+    return fail(MOE_ERR_ARG, "moe_w2_decode_fused: h / y / y_fmt");
+  if (!codes1 || !scales1 || !codes2 || !scales2 || !aligned(codes1, 16) || !aligned(scales1, 16) ||
+      !aligned(codes2, 16) || !aligned(scales2, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_decode_fused: weights NULL or not 16-byte aligned");
+  if (act_rows < 0 || (act_row && act_row_div < 1)) return fail(MOE_ERR_ARG, "moe_w2_decode_fused: act rows");
+  if (!ws || !aligned(ws, 256) || ws_bytes <= 256) return fail(MOE_ERR_ARG, "moe_w2_decode_fused: workspace");
+  MMArgs a1{}, a2{};
+  for (MMArgs* a : {&a1, &a2}) {
+    a->act_fmt = MOE_FMT_BF16;
+    a->mode = MOE_MODE_GEMV;
+    a->wkind = kW2;
+    a->select_map = expert_slot;
+    a->select = expert_slot ? 1 : 0;
+    a->offsets = offsets;
+    a->expert_begin = 0;
+    a->expert_end = E;
+    a->E = E;
+    a->dev_err = dev_err;
+    a->wait = wait_limit();
+  }
+  a1.stage = MOE_STAGE_FC1_SWIGLU;
+  a1.act = x;
+  a1.act_rows = act_rows;
+  a1.act_row = act_row;
+  a1.act_row_div = act_row ? act_row_div : 1;
+  a1.wq = codes1;
+  a1.wscale = scales1;
+  a1.N = I;
+  a1.K = H;
+  a1.out = h;
+  a1.out_fmt = MOE_FMT_BF16;
+  a2.stage = MOE_STAGE_FC2;
+  a2.act = h;
+  a2.act_rows = 0x7fffffff;  // h rows are the permuted rows themselves
+  a2.act_row = nullptr;
+  a2.act_row_div = 1;
+  a2.wq = codes2;
+  a2.wscale = scales2;
+  a2.N = H;
+  a2.K = I;
+  a2.out = y;
+  a2.out_fmt = y_fmt;
+  if (!lut_supported(a1) || !lut_supported(a2))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_w2_decode_fused: H and I must be multiples of 512");
+  const size_t lws = ws_bytes - 256;
+  for (MMArgs* a : {&a1, &a2}) {
+    a->ws = static_cast<uint8_t*>(ws) + 256;
+    a->ws_bytes = lws;
+    a->ws_rows = lut_workspace_rows(a->stage, lws, a->N, a->K);
+    if (a->ws_rows < 1) return fail(MOE_ERR_WS_SMALL, "moe_w2_decode_fused: workspace below one row");
+  }
+  return cuda_status(launch_w2_decode_fused(a1, a2, ws, static_cast<cudaStream_t>(stream)), "moe_w2_decode_fused");
+}
+
 int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
                  const int32_t* act_row, int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
                  const int32_t* ws_slot_of_expert, const int32_t* offsets, const int32_t* expert_slot,

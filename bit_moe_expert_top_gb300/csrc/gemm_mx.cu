@@ -23,11 +23,11 @@
 //   warps 1, 2  MMA issue, one weight block each: 4 MMAs of K = 32 per stage,
 //               the scale byte of k-block ks picked by the instruction
 //               descriptor; tcgen05.commit frees the stage
-//   warps 4-7   scale factors: per stage, the tokens' E8M0 words and, for
-//               MXFP4, the weight rows' (4 k-blocks per 32-bit TMEM cell)
-//               written to TMEM with one tcgen05.st per warp (row / token n
-//               at lane n mod 32 of every lane quarter, column n / 32: the
-//               MMA reads row m at lane m, column m / 32)
+//   warps 4-7   scale factors: per stage, the tokens' E8M0 words (4 k-blocks
+//               per 32-bit TMEM cell) written to TMEM with tcgen05.st
+//               (token n at lane n mod 32 of every lane quarter, column n/32),
+//               and for MXFP4 the weight rows' E8M0 words (row m at lane m,
+//               column m/32)
 //   warps 8-15  epilogue, two warps per TMEM lane quarter on alternate
 //               32-token chunks: tcgen05.ld of D_0 / D_1, SwiGLU for FC1,
 //               output rounding (fp32, bf16, or MXFP8: E4M3 codes + E8M0 per
@@ -288,16 +288,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
     }
   } else if (warp >= 4 && warp < 8) {
     // ================= scale factors into TMEM =================
-    // Per stage one tcgen05.st per warp: 16 columns of the warp's lane
-    // quarter, the same values in every quarter (lane l, column j holds the
-    // word of row / token l + 32 j): the MMA reads row m's word at lane m,
-    // column base + m / 32, which this replicated layout holds for any m.
-    // Columns: weight block 0 (+0..3), block 1 (+4..7), tokens (+8..11).
     // The words of a stage are loaded kPF stages ahead (a register ring), so
     // the round trip of the scale loads (strided rows, from HBM on a weight
     // block's first tile) overlaps the MMAs of the stages in between.
-    constexpr int kPF = AF == kAE2M1 ? 4 : 8;
-    constexpr int kW = AF == kAE2M1 ? 12 : 4;  // words per lane per stage
+    constexpr int kPF = 8;
     const int q = warp & 3;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     if (AF == kAE4M3) tm_st1(tl + kSFU + q, 0x7F7F7F7Fu);  // 2^0 for every weight row and k-block
@@ -312,30 +306,26 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       decode_tile(pi, e, blk, mt);
       p0 = P.offsets[e] + mt * NT;
       if (AF == kAE2M1) {
-        const size_t r = static_cast<size_t>(wslot[e]) * P.R + lane;
+        const size_t r = static_cast<size_t>(wslot[e]) * P.R + 32 * q + lane;
         wsa0 = P.wscale + (r + brow(blk, 0)) * KSB;
         wsa1 = P.wscale + (r + brow(blk, 1)) * KSB;
       }
     };
     if (pi < total) rebase();
-    uint32_t w[kPF][kW];
+    uint32_t w[kPF][4], wa[kPF][2];
     uint32_t nan = 0;
-    auto load = [&](uint32_t (&wd)[kW]) {
+    auto load = [&](uint32_t (&wd)[4], uint32_t (&wad)[2]) {
       if (pi >= total) return;
       // token n = lane + 32 j of the tile: its 4 E8M0 bytes of this stage
-      uint32_t* tok = wd + (kW - 4);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int p = p0 + lane + 32 * j;
-        tok[j] = (j < NT / 32 && p < P.rows_total) ? ld_u32(P.act_scale + static_cast<size_t>(p) * KSB + 4 * pkb)
-                                                   : 0x7F7F7F7Fu;
+        wd[j] = (j < NT / 32 && p < P.rows_total) ? ld_u32(P.act_scale + static_cast<size_t>(p) * KSB + 4 * pkb)
+                                                  : 0x7F7F7F7Fu;
       }
-      if (AF == kAE2M1) {  // weight rows lane + 32 j of both blocks
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          wd[j] = ld_u32(wsa0 + static_cast<size_t>(32 * j) * KSB + 4 * pkb);
-          wd[4 + j] = ld_u32(wsa1 + static_cast<size_t>(32 * j) * KSB + 4 * pkb);
-        }
+      if (AF == kAE2M1) {
+        wad[0] = ld_u32(wsa0 + 4 * pkb);
+        wad[1] = ld_u32(wsa1 + 4 * pkb);
       }
       if (++pkb == KB) {
         pkb = 0;
@@ -344,7 +334,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       }
     };
 #pragma unroll
-    for (int d = 0; d < kPF; ++d) load(w[d]);
+    for (int d = 0; d < kPF; ++d) load(w[d], wa[d]);
     bool ok = true;
     for (uint32_t L0 = 0; L0 < Ltot && ok; L0 += kPF) {
       if (__any_sync(0xffffffffu, aborted())) break;  // warp-uniform
@@ -358,22 +348,17 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
           if (ok) {
             tm_fence_after();  // the MMAs that read these columns are complete
             const uint32_t c0 = tl + kSF0 + s * kSFCols;
+            tm_st4(c0 + 8, w[d][0], w[d][1], w[d][2], w[d][3]);
             if (AF == kAE2M1) {
-              uint32_t v[16];
-#pragma unroll
-              for (int i = 0; i < 12; ++i) v[i] = w[d][i];
-              v[12] = v[13] = v[14] = v[15] = 0u;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) nan |= has_ff_byte(w[d][i]) ? 1u : 0u;
-              tm_st16(c0, v);
-            } else {
-              tm_st4(c0 + 8, w[d][0], w[d][1], w[d][2], w[d][3]);
+              nan |= (has_ff_byte(wa[d][0]) || has_ff_byte(wa[d][1])) ? 1u : 0u;
+              tm_st1(c0 + q, wa[d][0]);
+              tm_st1(c0 + 4 + q, wa[d][1]);
             }
             tm_st_wait();
             tm_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sf_full[s]);
-            load(w[d]);  // the stage kPF ahead
+            load(w[d], wa[d]);  // the stage kPF ahead
           }
         }
       }

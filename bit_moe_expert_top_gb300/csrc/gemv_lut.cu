@@ -167,13 +167,11 @@ MOE_D void rs_level2(float2* v, int lane, int m) {
   }
 }
 
-__global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams P) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+// The table GEMV of one call (FC1 or FC2) by one CTA of the persistent grid.
+MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
   int* pref = reinterpret_cast<int*>(smem);  // [E+1] selected permuted rows before expert e
   int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);  // [E] weight slot of expert e
 
-  pdl_wait();  // offsets, activations and the scratch belong to earlier kernels
-  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
   const uint32_t table_win = (base + kPrologue + 65535u) & ~65535u;
@@ -457,6 +455,40 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   }
 }
 
+__global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();  // offsets, activations and the scratch belong to earlier kernels
+  pdl_trigger();
+  lut_run(P, smem);
+}
+
+// One output of the finishing step: the NSL slice sums of selected row i,
+// output n, added in slice order; SwiGLU for FC1; rounded and stored.
+MOE_D void finish_one(const LutParams& P, int i, int n) {
+  const int NSL = P.NSL, NB = P.NB;
+  const int p = __ldcg(P.rows_hdr + 1 + i);
+  if (p < 0) return;
+  float t;
+  if (P.fc1) {  // batch n/8: rows 0..7 gate rows, 8..15 the matching up rows
+    const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 3)) * NSL * kBR + (n & 7);
+    float g = 0.f, u = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < NSL; ++q) {
+      g += __ldcg(sp + q * kBR);
+      u += __ldcg(sp + q * kBR + 8);
+    }
+    t = silu_f32(g) * u;
+  } else {
+    const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * kBR + (n & 15);
+    t = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * kBR);
+  }
+  const size_t o = static_cast<size_t>(p) * P.N + n;
+  if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
+  else static_cast<uint16_t*>(P.out)[o] = f32_to_bf16_rne(t);
+}
+
 // Sums the NSL slice sums of every output in slice order, applies SwiGLU for
 // FC1, rounds and stores.  Block (i, j) takes selected rows i, i + gridDim.x,
 // ... and outputs [256 j, 256 j + 256); one thread per output.
@@ -464,33 +496,66 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
   // everything read here is written by the preceding (primary) grid
   pdl_wait();
   pdl_trigger();
-  const int NSL = P.NSL, NB = P.NB;
   const int n = blockIdx.y * 256 + threadIdx.x;
   if (n >= P.N) return;
   const int lim = min(__ldcg(P.rows_hdr), P.A);
-  for (int i = blockIdx.x; i < lim; i += gridDim.x) {
-    const int p = __ldcg(P.rows_hdr + 1 + i);
-    if (p < 0) continue;
-    float t;
-    if (P.fc1) {  // batch n/8: rows 0..7 gate rows, 8..15 the matching up rows
-      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 3)) * NSL * kBR + (n & 7);
-      float g = 0.f, u = 0.f;
-#pragma unroll 4
-      for (int q = 0; q < NSL; ++q) {
-        g += __ldcg(sp + q * kBR);
-        u += __ldcg(sp + q * kBR + 8);
+  for (int i = blockIdx.x; i < lim; i += gridDim.x) finish_one(P, i, n);
+}
+
+// ------------------------------------------------------------------ one launch for FC1 and FC2
+// All CTAs of a cooperative launch (every CTA resident: one per SM) meet
+// here.  The counter is zeroed before the launch; barrier k completes when it
+// reaches k * gridDim.x.  The wait is bounded: past the limit the CTA records
+// MOE_DEVERR_TIMEOUT and the kernel returns (the others then time out too).
+MOE_D bool grid_barrier(unsigned int* cnt, unsigned int target, long long limit, uint32_t* dev_err) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's results before its arrival
+    atomicAdd(cnt, 1u);
+    const long long t0 = clock64();
+    int ok = 1;
+    while (true) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > limit) {
+        ok = 0;
+        set_err(dev_err, MOE_DEVERR_TIMEOUT);
+        break;
       }
-      t = silu_f32(g) * u;
-    } else {
-      const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * kBR + (n & 15);
-      t = 0.f;
-#pragma unroll 4
-      for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * kBR);
+      __nanosleep(64);
     }
-    const size_t o = static_cast<size_t>(p) * P.N + n;
-    if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
-    else static_cast<uint16_t*>(P.out)[o] = f32_to_bf16_rne(t);
+    s_ok = ok;
   }
+  __syncthreads();
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the other CTAs' results are visible to every thread
+  return s_ok != 0;
+}
+
+MOE_D void finish_grid(const LutParams& P) {
+  const int lim = min(__ldcg(P.rows_hdr), P.A);
+  const int64_t total = static_cast<int64_t>(lim) * P.N;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    finish_one(P, static_cast<int>(idx / P.N), static_cast<int>(idx % P.N));
+}
+
+// FC1 + SwiGLU and FC2 of the 2-bit decode layer in one persistent launch:
+// FC1 tables, barrier, FC1 slice sums -> h, barrier, FC2 tables (on h),
+// barrier, FC2 slice sums -> y.  Same arithmetic and order as the two calls.
+__global__ void __launch_bounds__(kLutThreads, 1) w2_decode_fused_kernel(const LutParams P1, const LutParams P2,
+                                                                        unsigned int* bar, long long wait) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
+  lut_run(P1, smem);
+  if (!grid_barrier(bar, gridDim.x, wait, P1.dev_err)) return;
+  finish_grid(P1);
+  if (!grid_barrier(bar, 2 * gridDim.x, wait, P1.dev_err)) return;
+  lut_run(P2, smem);
+  if (!grid_barrier(bar, 3 * gridDim.x, wait, P1.dev_err)) return;
+  finish_grid(P2);
 }
 
 }  // namespace
@@ -533,7 +598,7 @@ bool lut_supported(const MMArgs& a) {
   return a.K % kSW == 0 && a.N % 32 == 0;
 }
 
-cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
+static LutParams lut_params(const MMArgs& a, void* ws) {
   LutParams P;
   P.act = static_cast<const uint16_t*>(a.act);
   P.act_row = a.act_row;
@@ -559,6 +624,11 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   P.out = a.out;
   P.out_fmt = a.out_fmt;
   P.dev_err = a.dev_err;
+  return P;
+}
+
+cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
+  const LutParams P = lut_params(a, ws);
   cudaError_t e = set_smem_limit(w2_lut_kernel, kLutSmem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(w2_lut_kernel, dim3(device_info().sms), dim3(kLutThreads), kLutSmem, s, P);
@@ -567,6 +637,29 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   // main kernel's tail; its pdl_wait orders the scratch reads
   const dim3 fgrid(static_cast<unsigned>(a.ws_rows < 4096 ? a.ws_rows : 4096), static_cast<unsigned>((a.N + 255) / 256));
   return launch_pdl(w2_lut_finish_kernel, fgrid, dim3(256), 0, s, P);
+}
+
+cudaError_t launch_w2_decode_fused(const MMArgs& fc1, const MMArgs& fc2, void* ws, cudaStream_t s) {
+  unsigned int* bar = static_cast<unsigned int*>(ws);
+  void* lws = static_cast<uint8_t*>(ws) + 256;
+  const LutParams P1 = lut_params(fc1, lws), P2 = lut_params(fc2, lws);
+  cudaError_t e = set_smem_limit(w2_decode_fused_kernel, kLutSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  // cooperative: every CTA is resident at once (one per SM), which the
+  // grid-wide barriers need
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_info().sms);
+  cfg.blockDim = dim3(kLutThreads);
+  cfg.dynamicSmemBytes = kLutSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w2_decode_fused_kernel, P1, P2, bar, fc1.wait);
 }
 
 }  // namespace moe

@@ -114,6 +114,9 @@ bool lut_supported(const MMArgs& a);
 size_t lut_workspace_bytes(int stage, int rows, int N, int K);
 int lut_workspace_rows(int stage, size_t bytes, int N, int K);
 cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s);
+// FC1 and FC2 of the table GEMV in one cooperative launch; ws = 256 bytes of
+// barrier counter, then the table GEMV's workspace (shared by both stages)
+cudaError_t launch_w2_decode_fused(const MMArgs& fc1, const MMArgs& fc2, void* ws, cudaStream_t s);
 bool gemm_supported(const MMArgs& a);
 cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 // tensor-core grouped matmul with the dequantised weights in TMEM (gemm_tmem.cu)

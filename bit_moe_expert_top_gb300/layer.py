@@ -60,22 +60,26 @@ class StepBuffers:
     dev_err: torch.Tensor
     ws: Optional[torch.Tensor] = None
     pws: Optional[torch.Tensor] = None   # grouping scratch of large steps (multi-CTA)
+    fws: Optional[torch.Tensor] = None   # scratch of the fused FC1+FC2 launch
 
 
 class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
-                 resident=None, stage_slots: int = 64):
+                 resident=None, stage_slots: int = 64, fused: bool = False):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
         expert_slot int32 [E] (mixed): cache slot of each expert, -1 if none.
         resident (w2host): the expert ids kept in device memory; stage_slots:
-        staging slots for the routed host-resident experts of one step."""
+        staging slots for the routed host-resident experts of one step.
+        fused (w2, decode-sized steps): FC1 and FC2 in one cooperative launch
+        (moe_w2_decode_fused) instead of two calls."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
+        self.fused = fused and fmt == "w2"
         self.gemm_min_rows = gemm_min_rows
         dev = self.device
         if fmt in ("w2", "mixed", "w2host"):
@@ -186,7 +190,12 @@ class MoELayer:
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
             ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed", "w2host") and not gather else None,
             pws=self._permute_ws(T),
+            fws=self._fused_ws(A) if self.fused and not gather else None,
         )
+
+    def _fused_ws(self, A: int) -> Optional[torch.Tensor]:
+        n = L.moe_w2_decode_fused_workspace_size(A, self.H, self.I)
+        return torch.empty((n + 3) // 4, dtype=torch.int32, device=self.device) if n else None
 
     def _permute(self, b: StepBuffers, **kw):
         """moe_permute with the step's grouping scratch (multi-CTA when large)."""
@@ -251,6 +260,12 @@ class MoELayer:
                               dev_err=b.dev_err)
             else:
                 self._permute(b, dev_err=b.dev_err)
+            if b.fws is not None:  # FC1 and FC2 in one cooperative launch
+                with self._timed("w2_fc1_fc2_fused"):
+                    L.moe_w2_decode_fused(x, self.c1k, self.s1k, self.c2k, self.s2k, b.offsets, E, H, I, b.h, b.y,
+                                          L.FMT_BF16, b.fws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
+                L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
+                return b.out
             with self._timed("w2_fc1"):
                 L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
                             L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,

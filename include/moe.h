@@ -300,6 +300,31 @@ MOE_API int moe_w2_mm_noalloc(int stage,
                       int E, int N, int K, int rows,
                       void* out, int out_fmt, uint32_t* dev_err, void* stream);
 
+/* FC1 + SwiGLU and FC2 of a 2-bit decode step in ONE kernel launch (vLLM-Moet
+ * README, "MoET hybrid": the decode MoE runs inside a captured CUDA graph;
+ * here the two expert matmuls and their summing steps are one persistent
+ * cooperative kernel, every CTA resident, with grid-wide barriers between
+ * FC1's tables, FC1's sums, FC2's tables and FC2's sums).  Computes exactly
+ * moe_w2_mm(FC1, GEMV, x via act_row -> h bf16) then moe_w2_mm(FC2, GEMV,
+ * h -> y): same kernels' arithmetic and summation order, bit-identical h and y.
+ *   x         bf16 [act_rows][H] token rows, read through act_row / act_row_div
+ *             (as moe_w2_mm); h bf16 [rows][I] out; y [rows][H] out in y_fmt
+ *             (BF16 or F32); rows = offsets[E]
+ *   codes1/scales1, codes2/scales2  w2l weights of W1 [E][2I][H/4] and W2
+ *   expert_slot  nullable: experts with expert_slot[e] >= 0 are skipped
+ *   ws        >= moe_w2_decode_fused_workspace_size(rows, H, I) bytes,
+ *             256-byte aligned; the first 256 bytes hold the barrier counter
+ *             (zeroed by the call, stream-ordered), the rest is the table
+ *             GEMV's scratch shared by both stages
+ * H and I multiples of 512, else MOE_ERR_UNSUPPORTED.  Every grid barrier is a
+ * bounded wait (MOE_DEVERR_TIMEOUT, then the kernel returns). */
+MOE_API size_t moe_w2_decode_fused_workspace_size(int rows, int H, int I);
+MOE_API int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_row, int act_row_div,
+                        const uint8_t* codes1, const uint16_t* scales1, const uint8_t* codes2,
+                        const uint16_t* scales2, const int32_t* offsets, const int32_t* expert_slot,
+                        int E, int H, int I, void* h, void* y, int y_fmt, void* ws, size_t ws_bytes,
+                        uint32_t* dev_err, void* stream);
+
 /* As moe_w2_mm for MXFP4 weights, or for FP8 workspace weights.
  * Weight source, exactly one of:
  *   e2m1/e8m0 non-NULL: MXFP4 slots [S][rows][K/2], [S][rows][K/32]; expert e
