@@ -95,7 +95,7 @@ MOE_D bool has_ff_byte(uint32_t w) {  // any E8M0 byte 255 (NaN)
   return ((x - 0x01010101u) & ~x & 0x80808080u) != 0;
 }
 
-template <int AF, int NT>
+template <int AF, int NT, bool kVec>
 __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_constant__ CUtensorMap tmap_b,
                                                               const __grid_constant__ CUtensorMap tmap_a,
                                                               const MxParams P) {
@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
     if (pi < total) rebase();
     uint32_t w[kPF][4], wa[kPF][2];
     uint32_t nan = 0;
+    // one stage's words (4-byte loads; any K)
     auto load = [&](uint32_t (&wd)[4], uint32_t (&wad)[2]) {
       if (pi >= total) return;
       // token n = lane + 32 j of the tile: its 4 E8M0 bytes of this stage
@@ -333,8 +334,42 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
         if (pi < total) rebase();
       }
     };
+    // four stages' words of ring entries d0..d0+3 with one 16-byte load per
+    // row (K a multiple of 512: a tile has a whole number of 4-stage groups
+    // and every row's scale bytes start 16-byte aligned)
+    auto load4 = [&](int d0) {
+      if (pi >= total) return;
 #pragma unroll
-    for (int d = 0; d < kPF; ++d) load(w[d], wa[d]);
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + lane + 32 * j;
+        uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        if (j < NT / 32 && p < P.rows_total)
+          v = __ldg(reinterpret_cast<const uint4*>(P.act_scale + static_cast<size_t>(p) * KSB + 4 * pkb));
+        w[d0][j] = v.x;
+        w[d0 + 1][j] = v.y;
+        w[d0 + 2][j] = v.z;
+        w[d0 + 3][j] = v.w;
+      }
+      if (AF == kAE2M1) {
+        const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(wsa0 + 4 * pkb));
+        const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(wsa1 + 4 * pkb));
+        wa[d0][0] = a0.x, wa[d0 + 1][0] = a0.y, wa[d0 + 2][0] = a0.z, wa[d0 + 3][0] = a0.w;
+        wa[d0][1] = a1.x, wa[d0 + 1][1] = a1.y, wa[d0 + 2][1] = a1.z, wa[d0 + 3][1] = a1.w;
+      }
+      pkb += 4;
+      if (pkb == KB) {
+        pkb = 0;
+        pi += gridDim.x;
+        if (pi < total) rebase();
+      }
+    };
+    if constexpr (kVec) {
+      load4(0);
+      load4(4);
+    } else {
+#pragma unroll
+      for (int d = 0; d < kPF; ++d) load(w[d], wa[d]);
+    }
     bool ok = true;
     for (uint32_t L0 = 0; L0 < Ltot && ok; L0 += kPF) {
       if (__any_sync(0xffffffffu, aborted())) break;  // warp-uniform
@@ -358,7 +393,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
             tm_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sf_full[s]);
-            load(w[d], wa[d]);  // the stage kPF ahead
+            if constexpr (kVec) {  // a group of four consumed: its entries take the group kPF ahead
+              if (d == 3) load4(0);
+              if (d == 7) load4(4);
+            } else {
+              load(w[d], wa[d]);  // the stage kPF ahead
+            }
           }
         }
       }
@@ -497,9 +537,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
 template <int AF, int NT>
 cudaError_t launch_mx_t(const CUtensorMap& mb, const CUtensorMap& ma, const MxParams& P, cudaStream_t s) {
   const size_t smem = mx_smem_bytes<NT>();
-  cudaError_t e = set_smem_limit(mx_mm_kernel<AF, NT>, static_cast<int>(smem));
+  if (P.K % 512 == 0 && reinterpret_cast<uintptr_t>(P.act_scale) % 16 == 0) {  // 16-byte scale loads
+    cudaError_t e = set_smem_limit(mx_mm_kernel<AF, NT, true>, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(mx_mm_kernel<AF, NT, true>, dim3(device_info().sms), dim3(kMxThreads), smem, s, mb, ma, P);
+  }
+  cudaError_t e = set_smem_limit(mx_mm_kernel<AF, NT, false>, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(mx_mm_kernel<AF, NT>, dim3(device_info().sms), dim3(kMxThreads), smem, s, mb, ma, P);
+  return launch_pdl(mx_mm_kernel<AF, NT, false>, dim3(device_info().sms), dim3(kMxThreads), smem, s, mb, ma, P);
 }
 
 }  // namespace

@@ -504,9 +504,10 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
 
 // ------------------------------------------------------------------ one launch for FC1 and FC2
 // All CTAs of a cooperative launch (every CTA resident: one per SM) meet
-// here.  The counter is zeroed before the launch; barrier k completes when it
-// reaches k * gridDim.x.  The wait is bounded: past the limit the CTA records
-// MOE_DEVERR_TIMEOUT and the kernel returns (the others then time out too).
+// here.  The counter is zero when the launch starts; barrier k completes when
+// it reaches k * gridDim.x.  The wait is bounded: past the limit the CTA
+// records MOE_DEVERR_TIMEOUT and the kernel returns (the others then time out
+// too).
 MOE_D bool grid_barrier(unsigned int* cnt, unsigned int target, long long limit, uint32_t* dev_err) {
   __shared__ int s_ok;
   __syncthreads();
@@ -556,6 +557,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_decode_fused_kernel(const L
   lut_run(P2, smem);
   if (!grid_barrier(bar, 3 * gridDim.x, wait, P1.dev_err)) return;
   finish_grid(P2);
+  // leave the counter at zero for the next launch: the last CTA to arrive
+  // here (every other CTA is past its last barrier wait) resets it
+  if (threadIdx.x == 0 && atomicAdd(bar, 1u) == 4 * gridDim.x - 1) atomicExch(bar, 0u);
 }
 
 }  // namespace
@@ -645,20 +649,21 @@ cudaError_t launch_w2_decode_fused(const MMArgs& fc1, const MMArgs& fc2, void* w
   const LutParams P1 = lut_params(fc1, lws), P2 = lut_params(fc2, lws);
   cudaError_t e = set_smem_limit(w2_decode_fused_kernel, kLutSmem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), s);
-  if (e != cudaSuccess) return e;
   // cooperative: every CTA is resident at once (one per SM), which the
-  // grid-wide barriers need
+  // grid-wide barriers need; programmatic: the launch overlaps the
+  // predecessor's tail (the kernel's griddepcontrol.wait orders its reads)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(device_info().sms);
   cfg.blockDim = dim3(kLutThreads);
   cfg.dynamicSmemBytes = kLutSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, w2_decode_fused_kernel, P1, P2, bar, fc1.wait);
 }
 

@@ -194,8 +194,10 @@ class MoELayer:
         )
 
     def _fused_ws(self, A: int) -> Optional[torch.Tensor]:
+        """The fused launch's workspace: a barrier counter that starts at
+        zero (the launch leaves it at zero), then the table GEMV's scratch."""
         n = L.moe_w2_decode_fused_workspace_size(A, self.H, self.I)
-        return torch.empty((n + 3) // 4, dtype=torch.int32, device=self.device) if n else None
+        return torch.zeros((n + 3) // 4, dtype=torch.int32, device=self.device) if n else None
 
     def _permute(self, b: StepBuffers, **kw):
         """moe_permute with the step's grouping scratch (multi-CTA when large)."""

@@ -313,11 +313,14 @@ MOE_API int moe_w2_mm_noalloc(int stage,
  *   codes1/scales1, codes2/scales2  w2l weights of W1 [E][2I][H/4] and W2
  *   expert_slot  nullable: experts with expert_slot[e] >= 0 are skipped
  *   ws        >= moe_w2_decode_fused_workspace_size(rows, H, I) bytes,
- *             256-byte aligned; the first 256 bytes hold the barrier counter
- *             (zeroed by the call, stream-ordered), the rest is the table
- *             GEMV's scratch shared by both stages
+ *             256-byte aligned; its first 4 bytes are the barrier counter,
+ *             which must be zero before the first call (e.g. a zero-filled
+ *             workspace) and which every call leaves at zero; the rest is the
+ *             table GEMV's scratch shared by both stages.  Calls that share
+ *             one workspace must not overlap on the GPU
  * H and I multiples of 512, else MOE_ERR_UNSUPPORTED.  Every grid barrier is a
- * bounded wait (MOE_DEVERR_TIMEOUT, then the kernel returns). */
+ * bounded wait (MOE_DEVERR_TIMEOUT, then the kernel returns); after a timeout
+ * the counter is left non-zero and must be zeroed again before the next call. */
 MOE_API size_t moe_w2_decode_fused_workspace_size(int rows, int H, int I);
 MOE_API int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_row, int act_row_div,
                         const uint8_t* codes1, const uint16_t* scales1, const uint8_t* codes2,
