@@ -14,6 +14,9 @@ layer of weights, as sub-records of the line (``workloads``): prefill_bf16
 (8192 tokens, 2-bit experts on the tensor cores), prefill_fp8 (16384 tokens,
 MXFP4 experts through the FP8 workspace), prefill_fp8_direct (the same
 workload with the MXFP4 experts multiplied as stored, no workspace),
+decode_unfused (the headline decode with FC1 and FC2 as two calls instead of
+one fused launch), decode_mxfp4 (the decode shapes with MXFP4 experts on the
+block-scaled FP8 tensor core, MXFP8 tokens),
 mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache entries)
 and decode_host (the decode workload with every expert in pinned host memory
 and half of them resident on the device: the routed others are copied over
@@ -154,9 +157,10 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
 
     direct = name.endswith("_direct")  # MXFP4 experts multiplied as stored, no FP8 workspace
     hosted = name.endswith("_host")    # 2-bit experts in host memory, half of them resident on the device
-    fused = name.endswith("_fused")    # FC1 and FC2 of the 2-bit decode in one cooperative launch
+    unfused = name.endswith("_unfused")  # the 2-bit decode's FC1 and FC2 as two calls (not one launch)
+    as_mx4 = name.endswith("_mxfp4")     # the workload with MXFP4 experts on the block-scaled tensor core
     base = name
-    for suf in ("_direct", "_host", "_fused"):
+    for suf in ("_direct", "_host", "_unfused", "_mxfp4"):
         if name.endswith(suf):
             base = name[:-len(suf)]
     w = synth.get_workload(base)
@@ -166,7 +170,7 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
         w = w.replace(E=experts, n_hot=min(w.n_hot, experts))
     mls = []
     for l in range(layers):
-        if direct:
+        if direct or as_mx4:
             ml = MoELayer("mxfp4", w.E, w.H, w.I, w.k, device, mx=synth.make_mxfp4_layer(w, seed=0, layer=l),
                           out_fmt=L.FMT_BF16)
         elif hosted:
@@ -174,7 +178,7 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
                           resident=range(0, w.E, 2), stage_slots=w.T * w.k)
         elif w.weights == "w2":
             ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16,
-                          fused=fused)
+                          fused=not unfused)
         elif w.weights == "mixed":
             ml = MoELayer("mixed", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l),
                           mx=synth.make_mxfp4_layer(w, n=w.n_hot, seed=0, layer=l),
@@ -433,7 +437,7 @@ def launches_per_step(ml, T):
     table GEMV with its summing kernel (2-bit decode) or one tensor-core
     kernel, plus two workspace conversions per expert batch on the FP8 path."""
     tc = ml.use_gemm(T)
-    if ml.fmt == "w2" and ml.fused and not tc:  # route, permute, fused FC1+FC2 (+ its counter memset), combine
+    if ml.fmt == "w2" and ml.fused and not tc:  # route, permute, fused FC1+FC2, combine
         return 4
     if ml.fmt == "w2":
         return 6 if tc else 7
@@ -650,10 +654,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct",
-                             "decode_host", "decode_fused"])
+                             "decode_host", "decode_unfused", "decode_mxfp4"])
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--sub", default="decode_fused,prefill_bf16,prefill_fp8,prefill_fp8_direct,mixed_decode,"
-                                     "decode_host",
+    ap.add_argument("--sub", default="decode_unfused,decode_mxfp4,prefill_bf16,prefill_fp8,prefill_fp8_direct,"
+                                     "mixed_decode,decode_host",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

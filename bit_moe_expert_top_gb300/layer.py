@@ -67,15 +67,16 @@ class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
-                 resident=None, stage_slots: int = 64, fused: bool = False):
+                 resident=None, stage_slots: int = 64, fused: bool = True):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
         expert_slot int32 [E] (mixed): cache slot of each expert, -1 if none.
         resident (w2host): the expert ids kept in device memory; stage_slots:
         staging slots for the routed host-resident experts of one step.
-        fused (w2, decode-sized steps): FC1 and FC2 in one cooperative launch
-        (moe_w2_decode_fused) instead of two calls."""
+        fused (w2, decode-sized steps on the table GEMV): FC1 and FC2 in one
+        cooperative launch (moe_w2_decode_fused) instead of two calls; the
+        default (measured ~1.5 % faster per decode step)."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode

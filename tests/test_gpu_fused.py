@@ -24,7 +24,7 @@ def test_fused_decode_bit_identical_to_two_calls(name):
     else:  # 64 tokens, Zipf routing: several rows per expert
         w = synth.get_workload("prefill_bf16").replace(T=64)
     raw = synth.make_w2_layer(w)
-    two = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV)
+    two = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, fused=False)
     one = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, fused=True)
     for bi in range(2):
         x = synth.make_x(w, 0, tid_offset=bi)
@@ -58,3 +58,19 @@ def test_fused_decode_repeats_and_captures():
     g = ml.capture(w.T)
     assert torch.equal(g.run(x, lg), first)
     assert L.moe_get_error(b.dev_err) == 0
+
+
+def test_mxfp4_decode_on_the_block_scaled_tensor_core():
+    """The decode shapes with MXFP4 experts multiplied as stored (MXFP8 tokens,
+    32-token tiles, one tile per expert): sampled tokens at the FP8 gate."""
+    from tests._gpu import TOL_FP8, make_layer, run_layer
+    w = synth.get_workload("decode").replace(weights="mxfp4")
+    ml, acc, prof = make_layer(w, direct=True)
+    x = synth.make_x(w)
+    lg = synth.make_logits(w, x_bits=x)
+    out, b = run_layer(ml, x, lg)
+    assert L.moe_get_error(b.dev_err) == 0
+    tok = [0, 3, 7]
+    ref = M.layer(x, lg, w.k, acc, profile=prof, tokens=tok)
+    err, _ = rel_err(host(out)[tok], ref["out"])
+    assert err <= TOL_FP8
