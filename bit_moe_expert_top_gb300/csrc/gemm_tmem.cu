@@ -724,10 +724,15 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float v =
+              for (int j = 0; j < 32; j += 2) {  // hardware RNE, two tokens per conversion
+                const float v0 =
                     fc1 ? silu_fast(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
-                stg[(c + j) * 128 + nl] = f32_to_bf16_rne(v);
+                const float v1 = fc1 ? silu_fast(__uint_as_float(r0[j + 1])) * __uint_as_float(r1[j + 1])
+                                     : __uint_as_float(r0[j + 1]);
+                uint32_t b2;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(v1), "f"(v0));
+                stg[(c + j) * 128 + nl] = static_cast<uint16_t>(b2 & 0xffffu);
+                stg[(c + j + 1) * 128 + nl] = static_cast<uint16_t>(b2 >> 16);
               }
             }
           }

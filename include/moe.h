@@ -149,7 +149,10 @@ MOE_API int moe_route(const float* logits, int T, int E, int k, int32_t* ids, fl
               uint32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------ grouping
- * Stable counting sort of the A = T*k assignments by expert id.
+ * Stable counting sort of the A = T*k assignments by expert id: the
+ * per-expert token groups the expert matmuls run on (vLLM-Moet README,
+ * release v2026.11.03-r23 notes: the prefill MoE step; the MXFP8 gather
+ * is its "MXFP8 quant" of the activations).
  *   ids      int32 [T][k]   expert of each assignment (ids outside [0,E) set
  *                           BAD_ID; such an assignment gets inv = -1 and no row)
  *   offsets  int32 [E+1]    out: group e occupies permuted rows
@@ -171,13 +174,16 @@ MOE_API int moe_permute(const int32_t* ids, int T, int k, int E,
                 const uint16_t* x, int H, int act_fmt, void* x_perm, uint8_t* x_perm_scale,
                 void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream);
 
-/* rows[a] = rows_perm[inv[a]] for a < A (the inverse of the gather).  fmt is
+/* rows[a] = rows_perm[inv[a]] for a < A (the inverse of the gather; no page
+ * has it: the identity unpermute(permute(x)) = x is a test of the grouping).  fmt is
  * MOE_FMT_BF16 or MOE_FMT_F32; cols elements per row.  A test helper. */
 MOE_API int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, int A, int cols,
                   void* rows, void* stream);
 
 /* ------------------------------------------------------------------ weights
- * Rewrite canonical 2-bit weights into the w2l kernel layout (run once, at load).
+ * Rewrite canonical 2-bit weights (blog "这个项目我们能学到什么?": codebook
+ * {-4,-1,1,4}, one fp16 scale per 32) into the w2l kernel layout (run once,
+ * at load).
  *   codes   uint8 [mats][R][K/4] canonical;   scales fp16 [mats][R][K/32]
  *   codes_k uint8 [mats][R][K/4] out;         scales_k bf16 [mats][R][K/32] out
  * w2l keeps the canonical code bytes but moves whole 32-bit words (16
@@ -193,12 +199,14 @@ MOE_API int moe_unpermute(const void* rows_perm, int fmt, const int32_t* inv, in
 MOE_API int moe_w2_repack(const uint8_t* codes, const uint16_t* scales, int64_t mats, int R, int K,
                   uint8_t* codes_k, uint16_t* scales_k, void* stream);
 
-/* Exact dequantised values (bf16 bit patterns [mats][R][K]) of w2l weights:
+/* Exact dequantised values (bf16 bit patterns [mats][R][K]) of w2l weights
+ * (the same blog's 2-bit codebook experts):
  * entry * RNE_bf16(scale), the values the expert matmuls compute with. */
 MOE_API int moe_dequant_w2(const uint8_t* codes_k, const uint16_t* scales_k, int64_t mats, int R, int K,
                    uint16_t* out_bf16, void* stream);
 
-/* Exact dequantised MXFP4 values as float [rows][K] (NaN where the scale is 255). */
+/* Exact dequantised MXFP4 values (OCP MX v1.0 E2M1 x E8M0; the vLLM-Moet
+ * README's MXFP4 experts) as float [rows][K] (NaN where the scale is 255). */
 MOE_API int moe_dequant_mxfp4(const uint8_t* e2m1, const uint8_t* e8m0, int64_t rows, int K,
                       float* out_f32, void* stream);
 
@@ -219,6 +227,9 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
                     uint32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------ expert matmuls
+ * The expert FFN (vLLM-Moet README, release v2026.11.03-r23 notes: "FC1 +
+ * SwiGLU + MXFP8 quant, FC2"; line table: 2-bit codebook experts, 384 per
+ * layer) on low-bit weights dequantised inside the matmul.
  * For every expert e whose group is non-empty and selected (see below), for
  * every permuted row p of the group (offsets[e] <= p < offsets[e+1]):
  *   activation row a_p = act row (act_row ? act_row[p] / act_row_div : p), K elements;
@@ -328,7 +339,14 @@ MOE_API int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_
                         int E, int H, int I, void* h, void* y, int y_fmt, void* ws, size_t ws_bytes,
                         uint32_t* dev_err, void* stream);
 
-/* As moe_w2_mm for MXFP4 weights, or for FP8 workspace weights.
+/* As moe_w2_mm for MXFP4 weights (blog "这个项目我们能学到什么?": the FP4
+ * delta cache of hot experts; OCP MX E2M1 + E8M0), or for FP8 workspace
+ * weights ("国产GPU完成MoE大模型Day-0适配" §四: the matmul reads the reused FP8
+ * workspace).  With MXFP8 activations on the tensor-core path (mode GEMM or
+ * AUTO at prefill sizes, act_row NULL, K a multiple of 128) both weight forms
+ * run on the block-scaled FP8 tensor core (tcgen05 kind::mxf8f6f4: E4M3 or
+ * E2M1 codes with their E8M0 block scales, MXFP8 tokens), and FC1 may write h
+ * as MXFP8 (out_scale E8M0 [rows][N/32]).
  * Weight source, exactly one of:
  *   e2m1/e8m0 non-NULL: MXFP4 slots [S][rows][K/2], [S][rows][K/32]; expert e
  *       uses slot expert_slot[e] (experts with expert_slot[e] < 0 are skipped;
@@ -426,6 +444,8 @@ MOE_API int moe_cache_fill(const int32_t* promoted, int S, int n_arrays, const v
                    const size_t* bytes, void* stream);
 
 /* ------------------------------------------------------------------ combine
+ * The weighted combine of the routed experts' outputs (the top-k softmax
+ * weights of moe_route; vLLM-Moet README line table, top-k routing):
  * out[t][n] = sum_{j=0..k-1} w[t][j] * y[inv[t*k+j]][n], accumulated in fp32 in
  * ascending j, then rounded to out_fmt (BF16 or F32).  One owner per output
  * row: deterministic, no atomics.  Assignments with inv < 0 contribute nothing.
