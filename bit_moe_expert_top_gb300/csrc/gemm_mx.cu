@@ -32,8 +32,8 @@
 //               32-token chunks: tcgen05.ld of D_0 / D_1, SwiGLU for FC1,
 //               output rounding (fp32, bf16, or MXFP8: E4M3 codes + E8M0 per
 //               32 outputs, the FP8 path's h; block maxima by a butterfly
-//               reduce-scatter across the warp), shared staging and 16-byte
-//               row stores.  Measured (per-role clock counts): with four
+//               reduce-scatter across the warp), a private shared tile per
+//               warp and 16-byte row pieces (no barrier across the warps).  Measured (per-role clock counts): with four
 //               epilogue warps and one shuffle reduction per token the
 //               epilogue, not the MMAs, set the pace
 //   warp 3      allocates and frees TMEM
@@ -59,7 +59,7 @@ constexpr int kMxThreads = kMxWarps * 32;
 constexpr int kKS = 128;        // K elements per stage: 4 MMAs of K = 32, one E8M0 word per row
 constexpr int kMS = 4;          // pipeline stages
 constexpr int kMTab = 12288;    // barriers, flags, tile tables (E <= 1024)
-constexpr int kMStg = 16384;    // epilogue staging: 64 tokens x 128 outputs x 2 bytes
+constexpr int kMStg = 16384;    // epilogue staging: 8 warps x [32 tokens][32 outputs] x 2 bytes
 constexpr uint32_t kSFCols = 16;  // TMEM scale columns per stage: SFA block 0 (+0), block 1 (+4), SFB (+8)
 
 enum { kAE4M3 = 0, kAE2M1 = 1 };
@@ -408,26 +408,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
   } else if (warp >= 8) {
     // ================= epilogue (8 warps: two per TMEM lane quarter) =================
     // Warps q and q + 4 of the group read lanes 32q..32q+31 (outputs) and
-    // take alternate 32-token chunks; a 64-token window of the staging tile is
-    // flushed to global memory with 16-byte row stores by all eight.
+    // take alternate 32-token chunks.  Each warp stages its chunk (32 tokens x
+    // its 32 outputs) in a private shared tile and writes it out itself with
+    // 16-byte row pieces: no barrier across the epilogue warps.
     const int q = warp & 3;
     const int eh = (warp - 8) >> 2;  // chunk parity
-    const int et = tid - 8 * 32;     // 0..255
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     const bool f32_out = P.out_fmt == MOE_FMT_F32;
     const bool mx_out = P.out_fmt == MOE_FMT_MXFP8;
-    const int ob = mx_out ? 1 : 2;  // staged bytes per output
-    auto flush = [&](int prow0, int j0, int j1, int nbase) {  // rows [j0, j1) of the window
-      named_bar_sync(1, 256);
-      const int pieces = 128 * ob / 16;  // 16-byte pieces per row
-      for (int idx = et; idx < (j1 - j0) * pieces; idx += 256) {
-        const int j = idx / pieces, pc = idx - j * pieces;
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + ((j0 + j) & 63) * 128 * ob + pc * 16);
-        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(P.out) +
-                                  (static_cast<size_t>(prow0 + j0 + j) * P.N + nbase) * ob + pc * 16) = v;
-      }
-      named_bar_sync(1, 256);
-    };
+    const int ob = mx_out ? 1 : 2;         // bytes per output
+    uint8_t* wst = stg + (warp - 8) * 2048;  // this warp's tile: [32 tokens][32 outputs]
     int t = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++t) {
       if (__any_sync(0xffffffffu, aborted())) break;  // warp-uniform
@@ -455,71 +445,88 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
       if (last_c < 0) release(2);  // no chunk for this warp in this tile
       for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
         const int nbase = fc1 ? blk * 128 : blk * 256 + half * 128;
-        const int n = nbase + 32 * q + lane;  // this lane's output
+        const int n0 = nbase + 32 * q;  // first output of this warp
+        const int n = n0 + lane;        // this lane's output
 #pragma unroll 1
-        for (int w0 = 0; w0 < nvalid; w0 += 64) {
-          const int c = w0 + 32 * eh;
-          if (c < nvalid) {
-            uint32_t r0[32], r1[32];
-            if (fc1) {
-              tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
-              tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
-            } else {
-              tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
-            }
-            tm_ld_wait();
-            if (c == last_c) release(fc1 ? 2 : half);
-            float v[32];
+        for (int c = 32 * eh; c < nvalid; c += 64) {
+          uint32_t r0[32], r1[32];
+          if (fc1) {
+            tm_ld32(tmem + tlane + static_cast<uint32_t>(c), r0);
+            tm_ld32(tmem + tlane + static_cast<uint32_t>(NT + c), r1);
+          } else {
+            tm_ld32(tmem + tlane + static_cast<uint32_t>(half * NT + c), r0);
+          }
+          tm_ld_wait();
+          if (c == last_c) release(fc1 ? 2 : half);
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = fc1 ? silu_fast(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
+          if (f32_out) {
+            float* o = static_cast<float*>(P.out);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              v[j] = fc1 ? silu_fast(__uint_as_float(r0[j])) * __uint_as_float(r1[j]) : __uint_as_float(r0[j]);
-            if (f32_out) {
-              float* o = static_cast<float*>(P.out);
+              if (c + j < nvalid) o[static_cast<size_t>(p0 + c + j) * P.N + n] = v[j];
+            continue;
+          }
+          if (mx_out) {
+            // MXFP8: token j's block of 32 outputs is this warp's 32 lanes.
+            // Block maxima by a butterfly reduce-scatter: afterwards lane L
+            // holds the maximum of token L (31 shuffles for 32 tokens).
+            float a[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c + j < nvalid) o[static_cast<size_t>(p0 + c + j) * P.N + n] = v[j];
-            } else if (mx_out) {
-              // MXFP8: token j's block of 32 outputs is this warp's 32 lanes.
-              // Block maxima by a butterfly reduce-scatter: afterwards lane L
-              // holds the maximum of token L (31 shuffles for 32 tokens).
-              float a[32];
+            for (int j = 0; j < 32; ++j) a[j] = fabsf(v[j]);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) a[j] = fabsf(v[j]);
+            for (int m = 16; m >= 1; m >>= 1) {
+              const bool up = (lane & m) != 0;
 #pragma unroll
-              for (int m = 16; m >= 1; m >>= 1) {
-                const bool up = (lane & m) != 0;
-#pragma unroll
-                for (int j = 0; j < m; ++j) {
-                  const float keep = up ? a[j + m] : a[j];
-                  const float send = up ? a[j] : a[j + m];
-                  a[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
-                }
-              }
-              const int X = mx_scale_exp(a[0]);  // token c + lane
-              if (c + lane < nvalid)
-                P.out_scale[static_cast<size_t>(p0 + c + lane) * (P.N / 32) + nbase / 32 + q] =
-                    static_cast<uint8_t>(X + 127);
-              const float inv = exp2i(-X);
-              uint8_t* row = stg + (c & 63) * 128 + 32 * q + lane;
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                const float i0 = __shfl_sync(0xffffffffu, inv, j), i1 = __shfl_sync(0xffffffffu, inv, j + 1);
-                const uint16_t two = f32x2_to_e4m3x2(v[j] * i0, v[j + 1] * i1);
-                row[j * 128] = static_cast<uint8_t>(two & 0xffu);
-                row[(j + 1) * 128] = static_cast<uint8_t>(two >> 8);
-              }
-            } else {
-              uint16_t* row = reinterpret_cast<uint16_t*>(stg) + (c & 63) * 128 + 32 * q + lane;
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                uint32_t b2;
-                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(v[j + 1]), "f"(v[j]));
-                row[j * 128] = static_cast<uint16_t>(b2 & 0xffffu);
-                row[(j + 1) * 128] = static_cast<uint16_t>(b2 >> 16);
+              for (int j = 0; j < m; ++j) {
+                const float keep = up ? a[j + m] : a[j];
+                const float send = up ? a[j] : a[j + m];
+                a[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
               }
             }
+            const int X = mx_scale_exp(a[0]);  // token c + lane
+            if (c + lane < nvalid)
+              P.out_scale[static_cast<size_t>(p0 + c + lane) * (P.N / 32) + n0 / 32] = static_cast<uint8_t>(X + 127);
+            const float inv = exp2i(-X);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float i0 = __shfl_sync(0xffffffffu, inv, j), i1 = __shfl_sync(0xffffffffu, inv, j + 1);
+              const uint16_t two = f32x2_to_e4m3x2(v[j] * i0, v[j + 1] * i1);
+              wst[j * 32 + lane] = static_cast<uint8_t>(two & 0xffu);
+              wst[(j + 1) * 32 + lane] = static_cast<uint8_t>(two >> 8);
+            }
+          } else {
+            uint16_t* w16 = reinterpret_cast<uint16_t*>(wst);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              uint32_t b2;
+              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(v[j + 1]), "f"(v[j]));
+              w16[j * 32 + lane] = static_cast<uint16_t>(b2 & 0xffffu);
+              w16[(j + 1) * 32 + lane] = static_cast<uint16_t>(b2 >> 16);
+            }
           }
-          if (!f32_out) flush(p0, w0, min(w0 + 64, nvalid), nbase);
+          __syncwarp();
+          // the tile's rows (tokens) as 16-byte pieces: 32 x ob bytes per row
+          if (mx_out) {
+#pragma unroll 1
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int row = (lane >> 1) + 16 * k2, pc = lane & 1;
+              if (c + row < nvalid)
+                *reinterpret_cast<uint4*>(static_cast<uint8_t*>(P.out) + static_cast<size_t>(p0 + c + row) * P.N +
+                                          n0 + pc * 16) = *reinterpret_cast<const uint4*>(wst + row * 32 + pc * 16);
+            }
+          } else {
+#pragma unroll 1
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int row = (lane >> 2) + 8 * k2, pc = lane & 3;
+              if (c + row < nvalid)
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + static_cast<size_t>(p0 + c + row) * P.N +
+                                          n0 + pc * 8) = *reinterpret_cast<const uint4*>(wst + row * 64 + pc * 16);
+            }
+          }
+          __syncwarp();  // the tile is free for the next chunk
         }
       }
     }
