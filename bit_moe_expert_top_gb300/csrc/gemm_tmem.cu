@@ -648,23 +648,14 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     if (!ok) abort_all();
   } else {
     // ================= epilogue =================
-    // bf16 outputs go through a shared staging tile [token][128 outputs] so
-    // that the global stores are whole 256-byte row pieces (16 bytes per
-    // lane); storing 2 bytes per lane straight from registers measured slower
+    // bf16 outputs: each warp stages a chunk (32 tokens x its 32 outputs) in
+    // a private shared tile and writes it out itself as 16-byte row pieces
+    // (storing 2 bytes per lane straight from registers measured slower; a
+    // tile shared by the four warps needs a barrier per flush)
     const int q = warp & 3;
-    const int et = tid - 10 * 32;  // 0..127
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
-    uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kTab);
+    uint16_t* wst = reinterpret_cast<uint16_t*>(smem + kTab) + q * 1024;  // [32 tokens][32 outputs]
     const int nl = 32 * q + lane;  // output within the 128-row block
-    auto store_stage = [&](int p0, int nvalid, int nbase) {
-      named_bar_sync(1, 128);  // staging complete
-      for (int idx = et; idx < nvalid * 16; idx += 128) {
-        const int j = idx >> 4, seg = idx & 15;
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + j * 128 + seg * 8);
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + static_cast<size_t>(p0 + j) * P.N + nbase + seg * 8) = v;
-      }
-      named_bar_sync(1, 128);  // staging free again
-    };
     int t = 0;
     for (int i = blockIdx.x; i < total && !aborted(); i += gridDim.x, ++t) {
       int e, blk, mt;
@@ -691,6 +682,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       if (bf16_out) {
         const int nb0 = fc1 ? blk * 128 : blk * 256;
         for (int half = 0; half < (fc1 ? 1 : 2); ++half) {
+          const int nw = nb0 + half * 128 + 32 * q;  // first output of this warp
 #pragma unroll 1
           for (int c = 0; c < nvalid; c += 32) {
             uint32_t r0[32], r1[32];
@@ -719,8 +711,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                 const float2 d = e4m3x2_to_f32x2(qq);
                 uint32_t b2;
                 asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(d.y * exp2i(X1)), "f"(d.x * exp2i(X0)));
-                stg[(c + j) * 128 + nl] = static_cast<uint16_t>(b2 & 0xffffu);
-                stg[(c + j + 1) * 128 + nl] = static_cast<uint16_t>(b2 >> 16);
+                wst[j * 32 + lane] = static_cast<uint16_t>(b2 & 0xffffu);
+                wst[(j + 1) * 32 + lane] = static_cast<uint16_t>(b2 >> 16);
               }
             } else {
 #pragma unroll
@@ -731,12 +723,20 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
                                      : __uint_as_float(r0[j + 1]);
                 uint32_t b2;
                 asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(v1), "f"(v0));
-                stg[(c + j) * 128 + nl] = static_cast<uint16_t>(b2 & 0xffffu);
-                stg[(c + j + 1) * 128 + nl] = static_cast<uint16_t>(b2 >> 16);
+                wst[j * 32 + lane] = static_cast<uint16_t>(b2 & 0xffffu);
+                wst[(j + 1) * 32 + lane] = static_cast<uint16_t>(b2 >> 16);
               }
             }
+            __syncwarp();
+#pragma unroll 1
+            for (int k2 = 0; k2 < 4; ++k2) {  // 32 rows x 64 bytes as 16-byte pieces
+              const int row = (lane >> 2) + 8 * k2, pc = lane & 3;
+              if (c + row < nvalid)
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + static_cast<size_t>(p0 + c + row) * P.N +
+                                          nw + pc * 8) = *reinterpret_cast<const uint4*>(wst + row * 32 + pc * 8);
+            }
+            __syncwarp();  // the tile is free for the next chunk
           }
-          store_stage(p0, nvalid, nb0 + half * 128);
         }
       } else {
         const int n0 = fc1 ? blk * 128 + nl : blk * 256 + nl;
