@@ -21,7 +21,7 @@ MOE_OK, MOE_ERR_ARG, MOE_ERR_WS_SMALL, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1,
 DEVERR_BAD_ID, DEVERR_NAN_LOGIT, DEVERR_NAN_SCALE, DEVERR_TIMEOUT, DEVERR_OVERFLOW, DEVERR_LAUNCH = 1, 2, 4, 8, 16, 32
 FMT_NONE, FMT_BF16, FMT_F32, FMT_MXFP8, FMT_MXFP8_BF16 = 0, 1, 2, 3, 4
 STAGE_FC1_SWIGLU, STAGE_FC2 = 1, 2
-MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
+MODE_AUTO, MODE_GEMV, MODE_GEMM, MODE_SPLIT = 0, 1, 2, 3
 
 # every entry point declared in include/moe.h
 EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wait_limit",

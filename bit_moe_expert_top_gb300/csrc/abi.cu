@@ -216,7 +216,7 @@ static int check_mm(const char* who, int stage, int mode, const void* act, int a
                     const int32_t* offsets, int E, int N, int K, const void* out, int out_fmt,
                     const uint8_t* out_scale) {
   if (stage != MOE_STAGE_FC1_SWIGLU && stage != MOE_STAGE_FC2) return fail(MOE_ERR_ARG, "%s: bad stage", who);
-  if (mode < MOE_MODE_AUTO || mode > MOE_MODE_GEMM) return fail(MOE_ERR_ARG, "%s: bad mode", who);
+  if (mode < MOE_MODE_AUTO || mode > MOE_MODE_SPLIT) return fail(MOE_ERR_ARG, "%s: bad mode", who);
   if (E < 1 || E > 1024 || N <= 0 || K <= 0 || N % 128 || K % 128 || K > 8192)
     return fail(MOE_ERR_ARG, "%s: bad shape (N, K multiples of 128, K <= 8192, 1 <= E <= 1024)", who);
   if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "%s: act_fmt", who);
@@ -249,6 +249,7 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
     return fail(MOE_ERR_ARG, "moe_w2_mm: weights NULL or not 16-byte aligned");
   if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_w2_mm: act_rows < 0");
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_w2_mm: act_row_div < 1");
+  if (mode == MOE_MODE_SPLIT && act_row) return fail(MOE_ERR_ARG, "moe_w2_mm: MOE_MODE_SPLIT reads permuted rows (act_row NULL)");
   MMArgs a{};
   a.stage = stage;
   a.act = act;
@@ -416,6 +417,7 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
   (void)ws_bytes;
   if (int r = check_mm("moe_mxfp4_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
     return r;
+  if (mode == MOE_MODE_SPLIT) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: MOE_MODE_SPLIT is for 2-bit weights");
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_row_div < 1");
   if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_rows < 0");
   if (expert_begin < 0 || expert_end > E || expert_begin > expert_end)

@@ -34,7 +34,10 @@
 //               then a shared staging tile and 16-byte row stores
 //
 // MXFP4 decode (delta-cache experts): a per-lane 256-entry byte -> 2 bf16
-// E2M1 table (same window), scaled by 2^(E8M0-127) as bf16 (exact).
+// E2M1 table (same window, lane l's copy in bank l: a 4-byte lookup per lane
+// is one wavefront; at an 8-byte stride lanes l and l + 16 collided and the
+// decode took 1.8x the MMA issue time per stage), scaled by 2^(E8M0-127) as
+// bf16 (exact).
 // 2-bit decode: a per-lane copy of the 256-entry byte -> 4 bf16 codebook
 // table (64 KB at a 64 KB-aligned shared address, lane l's copy in banks
 // 2l, 2l+1) is read with one PRMT-formed address per code byte, then scaled
@@ -88,6 +91,7 @@ struct TmParams {
   const int32_t* wslot_of;  // E4M3: expert -> workspace slot (< 0: skipped)
   const int32_t* select_map;
   int select;
+  int split;                 // 2: only groups of kSplitRows rows or more
   const int32_t* offsets;
   int ebeg, eend;           // experts processed: [ebeg, eend)
   int E, N, K, R;
@@ -178,12 +182,12 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
   const int KB = P.K / kKB;
 
   // ---- setup (shared memory only until pdl_wait: it overlaps the previous kernel)
-  if (WF == kFmtMX4) {  // per-lane E2M1 pair LUT: byte b -> bf16x2 (lo nibble first) at win + 256 b + 8 l
+  if (WF == kFmtMX4) {  // per-lane E2M1 pair LUT: byte b -> bf16x2 (lo nibble first) at win + 256 b + 4 l
     const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
     for (int i = tid; i < 256 * 32; i += kTmThreads) {
       const uint32_t b = static_cast<uint32_t>(i >> 5);
       const uint32_t lo = mag[b & 7] | ((b & 8u) << 12), hi = mag[(b >> 4) & 7] | ((b & 0x80u) << 8);
-      *reinterpret_cast<uint32_t*>(smem + (win - base) + b * 256u + (i & 31) * 8u) = lo | (hi << 16);
+      *reinterpret_cast<uint32_t*>(smem + (win - base) + b * 256u + (i & 31) * 4u) = lo | (hi << 16);
     }
   }
   if (WF == kFmtW2) {  // per-lane codebook LUT: entry b of lane l at win + 256 b + 8 l
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       if (WF == kFmtW2) {
         sl = e;
         if (P.select == 1 && P.select_map[e] >= 0) sl = -1;
+        if (P.split == 2 && P.offsets[e + 1] - P.offsets[e] < kSplitRows) sl = -1;
       } else {
         sl = P.wslot_of ? P.wslot_of[e] : e;  // E4M3: workspace slot; MX4: cache slot (< 0: skipped)
         if (sl >= P.E) {                      // beyond the E slots the weight tensor map spans
@@ -440,7 +445,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
     const int bsel = d >> 2;       // weight block 0 / 1
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;   // row within the 128-row block
-    const uint32_t lanebase = win + 8u * static_cast<uint32_t>(lane);
+    // lane l's table entries: 8 bytes at 8 l (2-bit: 4 bf16 per byte) or 4
+    // bytes at 4 l (MXFP4: 2 bf16 per byte), so a warp's lookups take one
+    // shared-memory wavefront per 128 bytes (lane l always in the same banks)
+    const uint32_t lanebase = win + (WF == kFmtMX4 ? 4u : 8u) * static_cast<uint32_t>(lane);
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     // weight row (within the expert) of block bsel of pair blk
     auto wrow = [&](int blk) {
@@ -511,22 +519,11 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
       }
     } else if (WF == kFmtMX4) {  // MXFP4: E2M1 [slot][R][K/2] fed by TMA, E8M0 [slot][R][K/32] loaded here
       constexpr int RD = ring_depth<WF, NT>();
-      constexpr int D = 6;  // scale loads in flight (two E8M0 bytes per stage)
       const int64_t mat_s = static_cast<int64_t>(P.R) * (P.K / 32);
       const uint8_t* e8 = reinterpret_cast<const uint8_t*>(P.wscale);
-      uint32_t sb[D];
-      const uint8_t* ep = e8;
+      const uint8_t* ep = e8;  // the load cursor's scale pair (this thread's row)
       auto rebase = [&]() { ep = e8 + wslot[pe] * mat_s + static_cast<int64_t>(wrow(pblk)) * (P.K / 32); };
       if (pi < total) rebase();
-      auto load = [&](uint32_t& sc) {
-        if (pi >= total) return;
-        sc = __ldg(reinterpret_cast<const uint16_t*>(ep));
-        if (next_tile()) {
-          if (pi < total) rebase();
-        } else {
-          ep += 2;
-        }
-      };
       // this thread's row: tile row m of block bsel, 32 bytes written with the
       // 32-byte swizzle (16-byte chunk h at chunk h ^ ((m >> 2) & 1)); a
       // quarter-warp's 8 rows then cover all 32 banks
@@ -537,62 +534,99 @@ __global__ void __launch_bounds__(kTmThreads, 1) tmem_mm_kernel(const __grid_con
         const uint32_t b = x == 0 ? 0x0040u : (x == 255 ? 0x7FC0u : (x << 7));
         return b | (b << 16);
       };
+      // one stage: the row's 64 E2M1 codes of the ring slot, scaled by the
+      // stage's E8M0 pair sc (group 0 low byte), into this lane's A columns
+      auto stage = [&](uint32_t L, uint32_t sc) -> bool {
+        const int s = L % kTS, c = L % RD;
+        if (!mbar_wait(&code_full[c], (L / RD) & 1, P.wait)) return false;
+        uint4 q[2];
+        const uint32_t qo = qrow + static_cast<uint32_t>(c * kQStage);
 #pragma unroll
-      for (int d0 = 0; d0 < D; ++d0) load(sb[d0]);
-      for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
+        for (int h = 0; h < 2; ++h)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
+                       : "r"(qo + ((static_cast<uint32_t>(h) ^ qx) << 4))
+                       : "memory");
+        if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1, P.wait)) return false;
+        tm_fence_after();
+        if ((sc & 0xffu) == 255u || (sc >> 8) == 255u) set_err(P.dev_err, MOE_DEVERR_NAN_SCALE);
+        const uint32_t s0 = scale2(sc & 0xffu), s1 = scale2(sc >> 8);
+        uint32_t o[32];
 #pragma unroll
-        for (int d0 = 0; d0 < D; ++d0) {
-          const uint32_t L = L0 + d0;
-          if (L < Ltot && ok) {
-            const int s = L % kTS, c = L % RD;
-            if (!mbar_wait(&code_full[c], (L / RD) & 1, P.wait)) {
-              ok = false;
-              break;
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ww[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+          const uint32_t sh = h ? s1 : s0;  // bytes 0..15: group 0, 16..31: group 1
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            uint32_t a[4];
+            asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(a[0]) : "r"(ww[wi]), "r"(lanebase));
+            asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(a[1]) : "r"(ww[wi]), "r"(lanebase));
+            asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(a[2]) : "r"(ww[wi]), "r"(lanebase));
+            asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(a[3]) : "r"(ww[wi]), "r"(lanebase));
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+              uint32_t ent;
+              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ent) : "r"(a[bb]));
+              o[16 * h + 4 * wi + bb] = bf16x2_mul(ent, sh);
             }
-            uint4 q[2];
-            const uint32_t qo = qrow + static_cast<uint32_t>(c * kQStage);
+          }
+        }
+        tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
+        tm_st_wait();
+        tm_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&code_empty[c]);  // after tcgen05.st consumed values from every word read
+          mbar_arrive(&full_a[bsel * kTS + s]);
+        }
+        return true;
+      };
+      if (P.K % 512 == 0 && (reinterpret_cast<uintptr_t>(e8) & 15) == 0) {
+        // 16-byte scale loads, one per 8 stages (a warp's 2-byte loads from 32
+        // rows cost 32 L1 wavefronts each, as many as its table lookups), one
+        // group of 8 ahead; a tile's K-blocks are a multiple of 8, so a group
+        // never straddles two tiles
+        auto load8 = [&](uint4& v) {
+          if (pi >= total) return;
+          v = __ldg(reinterpret_cast<const uint4*>(ep));
+          pkb += 7;
+          if (next_tile()) {
+            if (pi < total) rebase();
+          } else {
+            ep += 16;
+          }
+        };
+        uint4 nxt = make_uint4(0, 0, 0, 0);
+        load8(nxt);
+        for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += 8) {
+          const uint4 cur = nxt;
+          load8(nxt);
+          const uint32_t w4[4] = {cur.x, cur.y, cur.z, cur.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
-                           : "r"(qo + ((static_cast<uint32_t>(h) ^ qx) << 4))
-                           : "memory");
-            if (L >= kTS && !mbar_wait(&empty[bsel * kTS + s], ((L / kTS) - 1) & 1, P.wait)) {
-              ok = false;
-            } else {
-              tm_fence_after();
-              const uint32_t sc = sb[d0];
-              if ((sc & 0xffu) == 255u || (sc >> 8) == 255u) set_err(P.dev_err, MOE_DEVERR_NAN_SCALE);
-              const uint32_t s0 = scale2(sc & 0xffu), s1 = scale2(sc >> 8);
-              uint32_t o[32];
+          for (int j = 0; j < 8; ++j)
+            if (ok) ok = stage(L0 + j, (w4[j >> 1] >> (16 * (j & 1))) & 0xffffu);
+        }
+      } else {
+        constexpr int D = 6;  // 2-byte scale loads in flight
+        uint32_t sb[D];
+        auto load = [&](uint32_t& sc) {
+          if (pi >= total) return;
+          sc = __ldg(reinterpret_cast<const uint16_t*>(ep));
+          if (next_tile()) {
+            if (pi < total) rebase();
+          } else {
+            ep += 2;
+          }
+        };
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t ww[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
-                const uint32_t sh = h ? s1 : s0;  // bytes 0..15: group 0, 16..31: group 1
+        for (int d0 = 0; d0 < D; ++d0) load(sb[d0]);
+        for (uint32_t L0 = 0; L0 < Ltot && ok && !aborted(); L0 += D) {
 #pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                  uint32_t a[4];
-                  asm("prmt.b32 %0, %1, %2, 0x7604;" : "=r"(a[0]) : "r"(ww[wi]), "r"(lanebase));
-                  asm("prmt.b32 %0, %1, %2, 0x7614;" : "=r"(a[1]) : "r"(ww[wi]), "r"(lanebase));
-                  asm("prmt.b32 %0, %1, %2, 0x7624;" : "=r"(a[2]) : "r"(ww[wi]), "r"(lanebase));
-                  asm("prmt.b32 %0, %1, %2, 0x7634;" : "=r"(a[3]) : "r"(ww[wi]), "r"(lanebase));
-#pragma unroll
-                  for (int bb = 0; bb < 4; ++bb) {
-                    uint32_t ent;
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ent) : "r"(a[bb]));
-                    o[16 * h + 4 * wi + bb] = bf16x2_mul(ent, sh);
-                  }
-                }
-              }
+          for (int d0 = 0; d0 < D; ++d0) {
+            const uint32_t L = L0 + d0;
+            if (L < Ltot && ok) {
+              ok = stage(L, sb[d0]);
               load(sb[d0]);
-              tm_st32(tmem + tlane + kColA + static_cast<uint32_t>(s * 64 + bsel * 32), o);
-              tm_st_wait();
-              tm_fence_before();
-              __syncwarp();
-              if (lane == 0) {
-                mbar_arrive(&code_empty[c]);  // after tcgen05.st consumed values from every word read
-                mbar_arrive(&full_a[bsel * kTS + s]);
-              }
             }
           }
         }
@@ -813,6 +847,7 @@ cudaError_t launch_tmem_mm(const MMArgs& a, int rows_total, cudaStream_t s) {
   P.wslot_of = a.wslot_of;
   P.select_map = a.select_map;
   P.select = a.select;
+  P.split = a.split;
   P.offsets = a.offsets;
   P.ebeg = a.expert_begin;
   P.eend = a.expert_end;

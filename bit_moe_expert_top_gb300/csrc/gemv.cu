@@ -437,6 +437,22 @@ cudaError_t launch_t(const GemvParams& P0, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const MMArgs& a, cudaStream_t s) {
+  if (a.mode == MOE_MODE_SPLIT) {
+    // groups of one row on the table GEMV, larger ones on the tensor core;
+    // the two launches cover disjoint experts (so disjoint output rows)
+    MMArgs v = a, g = a;
+    v.mode = MOE_MODE_GEMV;
+    v.split = 1;
+    g.mode = MOE_MODE_GEMM;
+    g.split = 2;
+    if (a.wkind == kW2 && a.ws && a.ws_rows > 0 && lut_supported(v) && tmem_mm_supported(g)) {
+      const cudaError_t e = launch_tmem_mm(g, a.act_rows, s);
+      return e != cudaSuccess ? e : launch_lut_gemv(v, a.ws, s);
+    }
+    MMArgs all = a;  // a shape either side does not take: every group on the GEMV
+    all.mode = MOE_MODE_GEMV;
+    return launch_gemv(all, s);
+  }
   // AUTO: the tensor-core GEMM for prefill-sized calls over permuted rows; the
   // GEMV for decode-sized ones (one 128-row tile per expert would be mostly idle)
   const bool want_gemm =

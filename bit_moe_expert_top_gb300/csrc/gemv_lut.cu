@@ -73,6 +73,7 @@ struct LutParams {
   int select;
   const int32_t* wslot;     // expert -> slot of the weight arrays (NULL: slot = expert)
   int slot_lo, slot_hi;     // with wslot: only experts whose slot lies in [slot_lo, slot_hi)
+  int split;                // 1: only groups of fewer than kSplitRows rows
   const int32_t* offsets;
   int E, N, K, R;           // R = weight rows per expert
   int NSL;                  // K slices
@@ -193,6 +194,7 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
         bool sel = c > 0;
         if (sel && P.select == 1) sel = P.select_map[e] < 0;
         if (sel && P.select == 2) sel = P.select_map[e] >= 0;
+        if (sel && P.split == 1) sel = c < kSplitRows;
         int ws = e;
         if (P.wslot) {
           ws = P.wslot[e];
@@ -615,6 +617,7 @@ static LutParams lut_params(const MMArgs& a, void* ws) {
   P.wslot = a.wslot_of;
   P.slot_lo = a.slot_lo;
   P.slot_hi = a.slot_hi;
+  P.split = a.split;
   P.offsets = a.offsets;
   P.E = a.E;
   P.N = a.N;

@@ -77,6 +77,11 @@ cudaError_t launch_mxfp4_to_fp8(const uint8_t* e2m1, const uint8_t* e8m0, const 
 // ---- expert matmuls on CUDA cores (gemv.cu)
 enum WeightKind { kW2 = 0, kMXFP4 = 1, kFP8 = 2 };
 
+// MOE_MODE_SPLIT: groups of this many rows or more go to the tensor-core
+// kernel (one pass over the expert's weights for all its rows), smaller ones
+// to the table GEMV (one pass per row).
+constexpr int kSplitRows = 2;
+
 struct MMArgs {
   int stage;  // MOE_STAGE_*
   const void* act;
@@ -97,6 +102,8 @@ struct MMArgs {
   const int32_t* select_map;  // per-expert map read by `select`
   int select;                 // 0: all experts; 1: experts with select_map[e] < 0 (the
                               // 2-bit pass skips delta-cached experts); 2: select_map[e] >= 0
+  int split;                  // 0: every group; 1: groups of fewer than kSplitRows rows;
+                              // 2: groups of kSplitRows rows or more (MOE_MODE_SPLIT halves)
   const int32_t* offsets;
   int expert_begin, expert_end;
   int E, N, K;

@@ -9,7 +9,9 @@ with the weight path chosen by the layer's format:
 
 * ``w2``    2-bit codebook experts (``moe_w2_mm``);
 * ``mixed`` 2-bit base plus an FP4 delta cache: experts with a cache slot go
-            through ``moe_mxfp4_mm``, the others through ``moe_w2_mm``;
+            through ``moe_mxfp4_mm``, the others through ``moe_w2_mm``
+            (optionally split by group size: one row on the table GEMV, more
+            on the tensor core);
 * ``fp8``   MXFP4 experts converted per expert batch into a reused FP8
             workspace ring (``mxfp4_to_fp8_ws`` on a side stream) ahead of the
             FP8 matmuls on the main stream, the conversion of the next batch
@@ -67,7 +69,7 @@ class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
-                 resident=None, stage_slots: int = 64, fused: bool = True):
+                 resident=None, stage_slots: int = 64, fused: bool = True, split: bool = False):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
@@ -76,11 +78,16 @@ class MoELayer:
         staging slots for the routed host-resident experts of one step.
         fused (w2, decode-sized steps on the table GEMV): FC1 and FC2 in one
         cooperative launch (moe_w2_decode_fused) instead of two calls; the
-        default (measured ~1.5 % faster per decode step)."""
+        default (measured ~1.5 % faster per decode step).
+        split (mixed, tensor-core cache path): the 2-bit experts' calls in
+        MOE_MODE_SPLIT (one-row groups on the table GEMV, larger ones on the
+        tensor core); off by default: at 64 tokens (~2.8 rows per touched
+        2-bit expert) it measured 6 % slower than the table GEMV alone."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
         self.fused = fused and fmt == "w2"
+        self.split = split and fmt == "mixed"
         self.gemm_min_rows = gemm_min_rows
         dev = self.device
         if fmt in ("w2", "mixed", "w2host"):
@@ -269,10 +276,19 @@ class MoELayer:
                                           L.FMT_BF16, b.fws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
                 L.moe_combine(b.y, L.FMT_BF16, b.w, b.inv, T, k, H, b.out, self.out_fmt)
                 return b.out
+            # split: 2-bit experts of a mixed layer on gathered rows, single-row groups
+            # on the table GEMV, larger ones on the tensor core (one pass over their weights)
+            split = mx_tc and self.split
+            w2_mode = (L.MODE_SPLIT if self.mode == L.MODE_AUTO else self.mode) if split else self.mode
             with self._timed("w2_fc1"):
-                L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
-                            L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
-                            mode=self.mode, ws=b.ws, dev_err=b.dev_err)
+                if split:
+                    L.moe_w2_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H,
+                                b.h, L.FMT_BF16, expert_slot=self.expert_slot, mode=w2_mode, ws=b.ws,
+                                dev_err=b.dev_err)
+                else:
+                    L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
+                                L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
+                                mode=self.mode, ws=b.ws, dev_err=b.dev_err)
             if self.fmt == "mixed" and mx_tc:
                 with self._timed("mx_fc1"):
                     L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
@@ -285,7 +301,7 @@ class MoELayer:
                                    expert_slot=self.expert_slot, mode=self.mode, dev_err=b.dev_err)
             with self._timed("w2_fc2"):
                 L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
-                            expert_slot=self.expert_slot, mode=self.mode, ws=b.ws, dev_err=b.dev_err)
+                            expert_slot=self.expert_slot, mode=w2_mode, ws=b.ws, dev_err=b.dev_err)
             if self.fmt == "mixed":
                 with self._timed("mx_fc2"):
                     L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,

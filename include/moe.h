@@ -111,6 +111,7 @@ extern "C" {
 #define MOE_MODE_AUTO 0  /* GEMV for small groups, tensor-core GEMM for large ones */
 #define MOE_MODE_GEMV 1  /* CUDA-core grouped GEMV (any group size)               */
 #define MOE_MODE_GEMM 2  /* tcgen05 tensor-core grouped GEMM                      */
+#define MOE_MODE_SPLIT 3 /* moe_w2_mm only: per group, GEMV for one row, GEMM for more */
 
 /* Library version (MOE_ABI_VERSION). */
 MOE_API int moe_version(void);
@@ -255,6 +256,12 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * neither runs as GEMV (MXFP8_BF16 output excepted: MOE_ERR_UNSUPPORTED).
  * AUTO = GEMM when act_row is NULL, act_rows >= 2048 and the shape is
  * supported, else GEMV.
+ * SPLIT (moe_w2_mm only; act_row must be NULL): groups of one row go to the
+ * table GEMV (which streams an expert's weights once per row) and groups of
+ * two rows or more to the tensor-core GEMM (once per expert for all its rows
+ * in a 32- or 128-row token tile), as two launches over disjoint experts;
+ * needs a workspace and a shape both take, else every group runs as GEMV.
+ * Each row's result is that of the path its group took.
  *   ws, ws_bytes (moe_w2_mm): scratch of the 2-bit GEMV, at least
  *        moe_w2_mm_workspace_size(stage, A, N, K) bytes for A permuted rows,
  *        256-byte aligned.  Its contents on entry do not matter (every value
