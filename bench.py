@@ -117,29 +117,26 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workloads
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean of
-# the FC1 and FC2 launches) of the dominant kernel, from the ncu captures
-# summarised under profiles/; reported only while the kernel source is the
-# one that was captured (sha256 of the file named).
-_TRAFFIC = {
-    "decode": {"bytes": 250.31e6, "src": "gemv_lut.cu",
-               "src_sha256": "8415d1fcfcc286234ba3f206d24193dda346e22e404a9c5f80995019f668640f"},
-    "prefill_bf16": {"bytes": 2312.48e6, "src": "gemm_tmem.cu",
-                     "src_sha256": "c76ee4c57ee6b3e3352415b0bf3e9cc8766c3baf143397685942f1bdf29fe09e"},
-}
+# DRAM bytes per expert-matmul call (dram__bytes_read.sum +
+# dram__bytes_write.sum of the kernels one timed call launches, averaged over
+# the step's calls, as `achieved` is), from the one-pass ncu captures of the
+# full-size workloads summarised under profiles/; reported only while the
+# kernels' sources are the ones captured (sha256 over the files named).
+_TRAFFIC = {}
 
 
-def _traffic(w):
+def _traffic(name):
     import hashlib
-    ent = _TRAFFIC.get(w.name)
+    ent = _TRAFFIC.get(name)
     if not ent or ent["bytes"] is None:
         return None
-    src = os.path.join(ROOT, "bit_moe_expert_top_gb300", "csrc", ent["src"])
-    try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except OSError:
-        return None
-    return ent["bytes"] if digest == ent["src_sha256"] else None
+    h = hashlib.sha256()
+    for f in ent["src"]:
+        try:
+            h.update(open(os.path.join(ROOT, "bit_moe_expert_top_gb300", "csrc", f), "rb").read())
+        except OSError:
+            return None
+    return ent["bytes"] if h.hexdigest() == ent["src_sha256"] else None
 
 
 def flops_per_assignment(w):
@@ -322,7 +319,7 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
 
     peaks = _peaks()
     decode = _decode_like(w)
-    traffic = _traffic(w) if tokens is None and experts is None else None
+    traffic = _traffic(name) if tokens is None and experts is None else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

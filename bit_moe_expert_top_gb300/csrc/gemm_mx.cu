@@ -547,11 +547,11 @@ cudaError_t launch_mx_t(const CUtensorMap& mb, const CUtensorMap& ma, const MxPa
   if (P.K % 512 == 0 && reinterpret_cast<uintptr_t>(P.act_scale) % 16 == 0) {  // 16-byte scale loads
     cudaError_t e = set_smem_limit(mx_mm_kernel<AF, NT, true>, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_pdl(mx_mm_kernel<AF, NT, true>, dim3(device_info().sms), dim3(kMxThreads), smem, s, mb, ma, P);
+    return launch_pdl(mx_mm_kernel<AF, NT, true>, dim3(matmul_ctas()), dim3(kMxThreads), smem, s, mb, ma, P);
   }
   cudaError_t e = set_smem_limit(mx_mm_kernel<AF, NT, false>, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(mx_mm_kernel<AF, NT, false>, dim3(device_info().sms), dim3(kMxThreads), smem, s, mb, ma, P);
+  return launch_pdl(mx_mm_kernel<AF, NT, false>, dim3(matmul_ctas()), dim3(kMxThreads), smem, s, mb, ma, P);
 }
 
 }  // namespace

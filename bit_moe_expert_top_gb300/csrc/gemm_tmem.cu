@@ -820,7 +820,7 @@ cudaError_t launch_tm(const MMArgs& a, const CUtensorMap& map, const CUtensorMap
   const size_t smem = pre + static_cast<size_t>(kTS) * NT * kKB * 2 + ring_bytes<WF, NT>() + 1024;
   cudaError_t e = set_smem_limit(tmem_mm_kernel<WF, NT>, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(tmem_mm_kernel<WF, NT>, dim3(device_info().sms), dim3(kTmThreads), smem, s, map, cmap, smap, P);
+  return launch_pdl(tmem_mm_kernel<WF, NT>, dim3(matmul_ctas()), dim3(kTmThreads), smem, s, map, cmap, smap, P);
 }
 
 }  // namespace

@@ -49,6 +49,12 @@ cudaError_t set_smem_limit(K* kernel, int bytes) {
 // kernels (moe_set_wait_limit).
 long long wait_limit();
 
+// SMs reserved for the MXFP4 -> FP8 workspace conversion on this device
+// (moe_set_conversion_sms; 0: none), and the CTAs of a persistent
+// tensor-core matmul (one per SM that is not reserved).
+int conversion_sms();
+int matmul_ctas();
+
 // ---- route / permute / combine (route_permute.cu)
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* dev_err,
                          cudaStream_t s);

@@ -69,7 +69,8 @@ class MoELayer:
     def __init__(self, fmt: str, E: int, H: int, I: int, k: int, device="cuda", *,
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
-                 resident=None, stage_slots: int = 64, fused: bool = True, split: bool = False):
+                 resident=None, stage_slots: int = 64, fused: bool = True, split: bool = False,
+                 conv_sms: int = 0):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
@@ -82,7 +83,11 @@ class MoELayer:
         split (mixed, tensor-core cache path): the 2-bit experts' calls in
         MOE_MODE_SPLIT (one-row groups on the table GEMV, larger ones on the
         tensor core); off by default: at 64 tokens (~2.8 rows per touched
-        2-bit expert) it measured 6 % slower than the table GEMV alone."""
+        2-bit expert) it measured 6 % slower than the table GEMV alone.
+        conv_sms (fp8, tensor-core path): SMs reserved for the workspace
+        conversion of the next batches while the current batch multiplies on
+        the others (moe_set_conversion_sms), 0: conversion and matmul each
+        take the whole GPU in turn."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
@@ -123,6 +128,7 @@ class MoELayer:
                                   for b in range(0, E, fp8_batch)]
             self.batch_slots = [self.ws_slot[b:min(E, b + fp8_batch)].contiguous() for b in range(0, E, fp8_batch)]
             self.conv_stream = torch.cuda.Stream(device=dev)
+            self.conv_sms = conv_sms
         torch.cuda.synchronize(dev)
 
     def _host_pool(self, resident, stage_slots):
@@ -392,7 +398,19 @@ class MoELayer:
             converted[i].record(conv)
 
         for i in range(min(self.ring, nb)):
-            convert(i)
+            convert(i)  # nothing to overlap yet: the whole GPU
+        # the later conversions on reserved SMs beside the matmuls (the
+        # setting is read when each call launches, also under graph capture)
+        prev = L.moe_set_conversion_sms(self.conv_sms) if tc and self.conv_sms > 0 else None
+        try:
+            self._fp8_ring(b, tc, nb, convert, converted, consumed, main)
+        finally:
+            if prev is not None:
+                L.moe_set_conversion_sms(prev)
+        main.wait_stream(conv)
+
+    def _fp8_ring(self, b, tc, nb, convert, converted, consumed, main):
+        E, H, I = self.E, self.H, self.I
         for i in range(nb):
             e0 = i * self.batch
             e1 = min(E, e0 + self.batch)
@@ -420,7 +438,6 @@ class MoELayer:
             consumed[i].record(main)
             if i + self.ring < nb:
                 convert(i + self.ring)
-        main.wait_stream(conv)
 
     # ------------------------------------------------------------ delta cache
     def attach_store(self, store, decay_shift: int = 31):

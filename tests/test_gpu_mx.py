@@ -19,7 +19,7 @@ from bit_moe_expert_top_gb300 import synth
 from oracle import codecs as C
 from oracle import moe as M
 
-from tests._gpu import DEV, dev, host
+from tests._gpu import DEV, dev, host, make_layer, run_layer
 from tests.test_gpu_layer import _check_full, _check_sampled
 from tests.test_gpu_multitile import MULTI, _compare, _exact_fc1, _nt, _sms, _tiles, _weights
 
@@ -179,3 +179,48 @@ def test_prefill_fp8_full_size_largest_groups_every_row(fmt):
         W1, W2 = acc(e)
         _compare(got_h[rows], _exact_fc1(_mx_values(xq[rows], xs[rows]), W1, I), H)
         _compare(got_y[rows], _mx_values(hq[rows], hs[rows]) @ W2.T, I)
+
+
+def test_conversion_on_reserved_sms_is_bit_identical():
+    """mxfp4_to_fp8_ws with SMs reserved (moe_set_conversion_sms): the same
+    bytes as the whole-GPU conversion, flags included; the setting is
+    restored afterwards."""
+    g = np.random.default_rng(5)
+    n_exp, rows, K = 6, 256, 512
+    q = g.integers(0, 256, size=(n_exp, rows, K // 2), dtype=np.uint8)
+    s = g.integers(110, 135, size=(n_exp, rows, K // 32), dtype=np.uint8)
+    s[3, 7, 2] = 255                                              # one NaN scale
+    experts = np.array([5, 0, 3, 2], dtype=np.int32)
+    slots = np.array([1, 3, 0, 2], dtype=np.int32)
+    outs = []
+    for n in (0, 7):
+        prev = L.moe_set_conversion_sms(n)
+        try:
+            ws = torch.full((4, rows, K), 0xAB, dtype=torch.uint8, device=DEV)
+            err = torch.zeros(1, dtype=torch.int32, device=DEV)
+            L.mxfp4_to_fp8_ws(dev(q), dev(s), dev(experts), rows, K, ws, dev(slots), dev_err=err)
+            outs.append((host(ws), L.moe_get_error(err)))
+        finally:
+            L.moe_set_conversion_sms(prev)
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert outs[0][1] == outs[1][1] and outs[0][1] & L.DEVERR_NAN_SCALE
+    assert L.moe_set_conversion_sms(0) == 0
+
+
+def test_fp8_layer_with_reserved_conversion_sms_is_bit_identical():
+    """The FP8-workspace layer with SMs reserved for the side-stream
+    conversion (smaller matmul grid, conversion beside it): output, h and y
+    bit-identical to the layer without the reservation."""
+    w = synth.get_workload("prefill_fp8").replace(E=48, H=1024, I=512, T=700, k=4)
+    ml, _, _ = make_layer(w, out_fmt=L.FMT_BF16, mode=L.MODE_GEMM)
+    x = synth.make_x(w)
+    lg = synth.make_logits(w, x_bits=x)
+    outs = []
+    for conv in (0, 20):
+        ml.conv_sms = conv
+        out, b = run_layer(ml, x, lg)
+        assert L.moe_get_error(b.dev_err) == 0
+        outs.append((out.clone(), b.h.clone(), b.y.clone()))
+    for a, c in zip(outs[0], outs[1]):
+        assert torch.equal(a, c)
+    assert L.moe_set_conversion_sms(0) == 0                     # the layer restored the setting
