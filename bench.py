@@ -443,8 +443,8 @@ def launches_per_step(ml, T):
         return 3 + (1 if mx_tc else 0) + 2 * 2 + 2 * 1
     if ml.fmt == "mxfp4":
         return 6
-    if ml.fmt == "w2host":  # route, permute, stage select, fill, 3 x (table GEMV + summing kernel), combine
-        return 11
+    if ml.fmt == "w2host":  # route, permute, stage select, fill, combine + 3 (4 with side SMs) x (table GEMV + sums)
+        return 5 + 2 * (4 if ml.side_sms > 0 else 3)
     nb = (ml.E + ml.batch - 1) // ml.batch
     return 4 + 4 * nb
 

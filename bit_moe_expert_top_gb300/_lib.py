@@ -24,7 +24,7 @@ STAGE_FC1_SWIGLU, STAGE_FC2 = 1, 2
 MODE_AUTO, MODE_GEMV, MODE_GEMM, MODE_SPLIT = 0, 1, 2, 3
 
 # every entry point declared in include/moe.h
-EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wait_limit", "moe_set_conversion_sms",
+EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wait_limit", "moe_set_side_sms",
            "moe_check_bounded_wait", "moe_route", "moe_permute_workspace_size",
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
@@ -45,7 +45,7 @@ _SIGS = {
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_get_error": (_I, [_P, _P, _P]),
     "moe_set_wait_limit": (_L, [_L]),
-    "moe_set_conversion_sms": (_I, [_I]),
+    "moe_set_side_sms": (_I, [_I]),
     "moe_check_bounded_wait": (_I, [_L, _P, _P]),
     "moe_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_permute_workspace_size": (_S, [_I, _I, _I]),
@@ -124,8 +124,8 @@ def moe_set_wait_limit(cycles: int) -> int:
     return int(lib().moe_set_wait_limit(cycles))
 
 
-def moe_set_conversion_sms(n: int) -> int:
-    return int(lib().moe_set_conversion_sms(n))
+def moe_set_side_sms(n: int) -> int:
+    return int(lib().moe_set_side_sms(n))
 
 
 def moe_check_bounded_wait(cycles, dev_err, stream=None):

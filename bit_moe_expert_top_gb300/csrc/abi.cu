@@ -67,7 +67,7 @@ struct SmemLimit {
 std::mutex g_smem_mu;
 std::vector<SmemLimit> g_smem;
 std::atomic<long long> g_wait{kWaitCycles};
-std::atomic<int> g_conv_sms{0};
+std::atomic<int> g_side_sms{0};
 }  // namespace
 
 cudaError_t set_smem_limit(const void* kernel, int bytes) {
@@ -85,13 +85,13 @@ cudaError_t set_smem_limit(const void* kernel, int bytes) {
 
 long long wait_limit() { return g_wait.load(std::memory_order_relaxed); }
 
-int conversion_sms() {
-  const int n = g_conv_sms.load(std::memory_order_relaxed);
+int side_sms() {
+  const int n = g_side_sms.load(std::memory_order_relaxed);
   const int sms = device_info().sms;
   return n > 0 && n < sms ? n : 0;
 }
 
-int matmul_ctas() { return device_info().sms - conversion_sms(); }
+int matmul_ctas() { return device_info().sms - side_sms(); }
 
 static int check_device() {
   const DeviceInfo& d = device_info();
@@ -124,9 +124,9 @@ long long moe_set_wait_limit(long long cycles) {
   return g_wait.exchange(cycles);
 }
 
-int moe_set_conversion_sms(int n) {
+int moe_set_side_sms(int n) {
   if (n < 0 || n > 1024) return -1;
-  return g_conv_sms.exchange(n);
+  return g_side_sms.exchange(n);
 }
 
 int moe_check_bounded_wait(long long cycles, uint32_t* dev_err, void* stream) {

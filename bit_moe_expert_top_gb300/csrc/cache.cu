@@ -190,6 +190,39 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const int32_t* __restri
   }
 }
 
+// The same copy on the side SMs (moe_set_side_sms): one CTA of 1024
+// threads per side SM (its unused shared-memory request is over half an
+// SM's, so no second CTA fits beside it); the CTAs walk every slot's bytes
+// together, four 16-byte loads in flight per thread, which keeps a few SMs
+// enough to fill the CPU-GPU link.
+constexpr int kFillThreads = 1024;
+constexpr int kFillPinSmem = 120 * 1024;
+
+__global__ void __launch_bounds__(kFillThreads, 1) cache_fill_sm_kernel(const int32_t* __restrict__ promoted, int S,
+                                                                        const FillArgs F) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (int s = 0; s < S; ++s) {
+    const int e = promoted[s];
+    if (e < 0) continue;
+    for (int a = 0; a < F.n; ++a) {
+      const size_t n16 = F.bytes[a] / 16;
+      const uint4* src = reinterpret_cast<const uint4*>(F.src[a] + static_cast<size_t>(e) * F.bytes[a]);
+      uint4* dst = reinterpret_cast<uint4*>(F.dst[a] + static_cast<size_t>(s) * F.bytes[a]);
+      size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+      for (; i + 3 * stride < n16; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[i + u * stride] = v[u];
+      }
+      for (; i < n16; i += stride) dst[i] = __ldcs(src + i);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_cache_select(const int32_t* offsets, int E, uint32_t* counts, int decay_shift, int S,
@@ -215,6 +248,12 @@ cudaError_t launch_cache_fill(const int32_t* promoted, int S, int n, const void*
     F.dst[a] = static_cast<uint8_t*>(dst[a]);
     F.bytes[a] = bytes[a];
     if (bytes[a] > most) most = bytes[a];
+  }
+  if (const int nside = side_sms()) {  // the side SMs only, beside a persistent matmul
+    const cudaError_t e = set_smem_limit(cache_fill_sm_kernel, kFillPinSmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(cache_fill_sm_kernel, dim3(static_cast<unsigned>(nside)), dim3(kFillThreads), kFillPinSmem, s,
+                      promoted, S, F);
   }
   // enough blocks per slot that one slot's copy spreads over the GPU when few
   // slots change (the usual case between decode steps)

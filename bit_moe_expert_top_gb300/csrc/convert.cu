@@ -140,7 +140,7 @@ __global__ void mxfp4_to_fp8_kernel(const uint8_t* __restrict__ e2m1, const uint
   if (overflow) set_err(dev_err, MOE_DEVERR_OVERFLOW);
 }
 
-// The same conversion on a fixed set of SMs (moe_set_conversion_sms): one
+// The same conversion on the side SMs (moe_set_side_sms): one
 // CTA of 1024 threads per reserved SM (its unused shared-memory request is
 // over half an SM's, so no second CTA fits beside it), every thread with
 // kConvU blocks' loads in flight, enough for one SM to pull its share of HBM
@@ -228,7 +228,7 @@ cudaError_t launch_mxfp4_to_fp8(const uint8_t* e2m1, const uint8_t* e8m0, const 
   const int64_t gpm = static_cast<int64_t>(rows) * (K / 32);
   const int64_t work = gpm * n_experts;
   if (work == 0) return cudaSuccess;
-  if (const int n = conversion_sms()) {  // the reserved SMs only, beside a persistent matmul
+  if (const int n = side_sms()) {  // the reserved SMs only, beside a persistent matmul
     const cudaError_t e = set_smem_limit(mxfp4_to_fp8_sm_kernel, kConvPinSmem);
     if (e != cudaSuccess) return e;
     mxfp4_to_fp8_sm_kernel<<<n, kConvThreads, kConvPinSmem, s>>>(e2m1, e8m0, experts, n_experts, gpm, ws,

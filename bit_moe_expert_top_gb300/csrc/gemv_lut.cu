@@ -638,7 +638,7 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s) {
   const LutParams P = lut_params(a, ws);
   cudaError_t e = set_smem_limit(w2_lut_kernel, kLutSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(w2_lut_kernel, dim3(device_info().sms), dim3(kLutThreads), kLutSmem, s, P);
+  e = launch_pdl(w2_lut_kernel, dim3(matmul_ctas()), dim3(kLutThreads), kLutSmem, s, P);
   if (e != cudaSuccess) return e;
   // the finishing kernel as a programmatic dependent: its launch overlaps the
   // main kernel's tail; its pdl_wait orders the scratch reads

@@ -49,10 +49,10 @@ cudaError_t set_smem_limit(K* kernel, int bytes) {
 // kernels (moe_set_wait_limit).
 long long wait_limit();
 
-// SMs reserved for the MXFP4 -> FP8 workspace conversion on this device
-// (moe_set_conversion_sms; 0: none), and the CTAs of a persistent
-// tensor-core matmul (one per SM that is not reserved).
-int conversion_sms();
+// SMs reserved on this device for the side-stream copy kernels (workspace
+// conversion, expert cache fill; moe_set_side_sms; 0: none), and the CTAs of
+// a persistent matmul (one per SM that is not reserved).
+int side_sms();
 int matmul_ctas();
 
 // ---- route / permute / combine (route_permute.cu)

@@ -70,7 +70,7 @@ class MoELayer:
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 16, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
                  resident=None, stage_slots: int = 64, fused: bool = True, split: bool = False,
-                 conv_sms: int = 0):
+                 side_sms: Optional[int] = None):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
@@ -84,15 +84,20 @@ class MoELayer:
         MOE_MODE_SPLIT (one-row groups on the table GEMV, larger ones on the
         tensor core); off by default: at 64 tokens (~2.8 rows per touched
         2-bit expert) it measured 6 % slower than the table GEMV alone.
-        conv_sms (fp8, tensor-core path): SMs reserved for the workspace
-        conversion of the next batches while the current batch multiplies on
-        the others (moe_set_conversion_sms), 0: conversion and matmul each
-        take the whole GPU in turn."""
+        side_sms (fp8 on the tensor-core path, w2host): SMs reserved for the
+        side-stream copy (the workspace conversion of the next batches, the
+        staging of host-resident experts) while the matmuls run on the
+        others (moe_set_side_sms); 0: copy and matmul each take the whole GPU
+        in turn.  Default: 16 for w2host (the copy is bound by the CPU-GPU
+        link, which 16 SMs keep full; measured 10 % faster per decode step),
+        0 for fp8 (one SM converts only ~47 GB/s: every count measured
+        slower)."""
         self.fmt, self.E, self.H, self.I, self.k = fmt, E, H, I, k
         self.device = torch.device(device)
         self.out_fmt, self.mode = out_fmt, mode
         self.fused = fused and fmt == "w2"
         self.split = split and fmt == "mixed"
+        self.side_sms = side_sms if side_sms is not None else (16 if fmt == "w2host" else 0)
         self.gemm_min_rows = gemm_min_rows
         dev = self.device
         if fmt in ("w2", "mixed", "w2host"):
@@ -128,7 +133,6 @@ class MoELayer:
                                   for b in range(0, E, fp8_batch)]
             self.batch_slots = [self.ws_slot[b:min(E, b + fp8_batch)].contiguous() for b in range(0, E, fp8_batch)]
             self.conv_stream = torch.cuda.Stream(device=dev)
-            self.conv_sms = conv_sms
         torch.cuda.synchronize(dev)
 
     def _host_pool(self, resident, stage_slots):
@@ -319,26 +323,51 @@ class MoELayer:
     def _host_step(self, x, b: StepBuffers):
         """Grouping, staging of the routed host-resident experts on a side
         stream, FC1 over the resident experts meanwhile, FC1 over the staged
-        ones once their copy has landed, then FC2 over all (table GEMV)."""
+        ones once their copy has landed, then FC2 over all (table GEMV).
+        With side SMs (``side_sms``) the copy holds a few SMs and the resident
+        experts' FC1 and FC2 both run beside it on the others; the staged
+        experts' FC1 and FC2 follow once it has landed."""
         E, H, I, k, R, S = self.E, self.H, self.I, self.k, self.R, self.S
         self._permute(b, dev_err=b.dev_err)
         L.moe_stage_select(b.offsets, self.res_slot, R, self.weight_slot, self.staged, dev_err=b.dev_err)
         main = torch.cuda.current_stream(self.device)
         cs = self.copy_stream
         cs.wait_stream(main)
-        L.moe_cache_fill(self.staged, self.store, [p[R:] for p in self.pool], self.pool_bytes, stream=cs)
-        landed = torch.cuda.Event()
-        landed.record(cs)
-        with self._timed("w2_fc1"):
-            if R:
-                L.moe_w2_mm_slots(L.STAGE_FC1_SWIGLU, x, self.c1k, self.s1k, b.offsets, self.weight_slot, 0, R, E, I,
-                                  H, b.h, L.FMT_BF16, b.ws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
-            main.wait_event(landed)
-            L.moe_w2_mm_slots(L.STAGE_FC1_SWIGLU, x, self.c1k, self.s1k, b.offsets, self.weight_slot, R, R + S, E,
-                              I, H, b.h, L.FMT_BF16, b.ws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
-        with self._timed("w2_fc2"):
-            L.moe_w2_mm_slots(L.STAGE_FC2, b.h, self.c2k, self.s2k, b.offsets, self.weight_slot, 0, R + S, E, H, I,
-                              b.y, L.FMT_BF16, b.ws, dev_err=b.dev_err)
+        side = self.side_sms > 0
+        prev = L.moe_set_side_sms(self.side_sms) if side else None
+        try:
+            L.moe_cache_fill(self.staged, self.store, [p[R:] for p in self.pool], self.pool_bytes, stream=cs)
+            landed = torch.cuda.Event()
+            landed.record(cs)
+
+            def fc1(lo, hi):
+                L.moe_w2_mm_slots(L.STAGE_FC1_SWIGLU, x, self.c1k, self.s1k, b.offsets, self.weight_slot, lo, hi, E,
+                                  I, H, b.h, L.FMT_BF16, b.ws, act_row=b.perm, act_row_div=k, dev_err=b.dev_err)
+
+            def fc2(lo, hi):
+                L.moe_w2_mm_slots(L.STAGE_FC2, b.h, self.c2k, self.s2k, b.offsets, self.weight_slot, lo, hi, E, H, I,
+                                  b.y, L.FMT_BF16, b.ws, dev_err=b.dev_err)
+
+            if side:
+                with self._timed("w2_resident"):
+                    if R:
+                        fc1(0, R)
+                        fc2(0, R)
+                with self._timed("w2_staged"):
+                    main.wait_event(landed)
+                    fc1(R, R + S)
+                    fc2(R, R + S)
+            else:
+                with self._timed("w2_fc1"):
+                    if R:
+                        fc1(0, R)
+                    main.wait_event(landed)
+                    fc1(R, R + S)
+                with self._timed("w2_fc2"):
+                    fc2(0, R + S)
+        finally:
+            if prev is not None:
+                L.moe_set_side_sms(prev)
 
     def capture(self, T: int) -> "LayerGraph":
         """The whole layer step for T tokens captured once into a CUDA graph
@@ -401,12 +430,12 @@ class MoELayer:
             convert(i)  # nothing to overlap yet: the whole GPU
         # the later conversions on reserved SMs beside the matmuls (the
         # setting is read when each call launches, also under graph capture)
-        prev = L.moe_set_conversion_sms(self.conv_sms) if tc and self.conv_sms > 0 else None
+        prev = L.moe_set_side_sms(self.side_sms) if tc and self.side_sms > 0 else None
         try:
             self._fp8_ring(b, tc, nb, convert, converted, consumed, main)
         finally:
             if prev is not None:
-                L.moe_set_conversion_sms(prev)
+                L.moe_set_side_sms(prev)
         main.wait_stream(conv)
 
     def _fp8_ring(self, b, tc, nb, convert, converted, consumed, main):

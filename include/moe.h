@@ -34,8 +34,8 @@
  *    moe_get_error.
  *  - Thread-safe: the only host-side global state is a per-device property
  *    cache, a per-device record of the kernels whose shared-memory limit was
- *    raised, the bounded-wait limit (moe_set_wait_limit), the conversion SM
- *    reservation (moe_set_conversion_sms) and the per-device
+ *    raised, the bounded-wait limit (moe_set_wait_limit), the side-SM
+ *    reservation (moe_set_side_sms) and the per-device
  *    address of moe_w2_mm_noalloc's scratch.
  *  - Every on-chip wait of a pipeline (mbarrier phases) is bounded: a wait
  *    that runs past the limit makes its kernel stop, set MOE_DEVERR_TIMEOUT and
@@ -131,17 +131,21 @@ MOE_API int moe_get_error(const uint32_t* dev_err, void* stream, uint32_t* bits)
  * limit.  Process-wide; host only. */
 MOE_API long long moe_set_wait_limit(long long cycles);
 
-/* Reserves n SMs of the device for the MXFP4 -> FP8 workspace conversion, so
- * that the conversion of the next expert batch runs beside the current
- * batch's matmuls on another stream ("国产GPU完成MoE大模型Day-0适配" §四).
- * With 0 < n < the SM count, the persistent tensor-core matmuls (moe_w2_mm /
- * moe_mxfp4_mm in GEMM mode) launched after this call take one CTA per
- * remaining SM and mxfp4_to_fp8_ws launches n CTAs that hold one SM each, so
- * the two share the GPU whatever order they start in; results are unchanged
- * (every tile and block is computed the same way).  0 (the default) gives
- * every launch the whole GPU.  Returns the previous value, or -1 (setting
- * unchanged) for n < 0 or n > 1024.  Process-wide; host only. */
-MOE_API int moe_set_conversion_sms(int n);
+/* Reserves n SMs of the device for the copy kernels that run on a side
+ * stream beside the expert matmuls: the MXFP4 -> FP8 workspace conversion of
+ * the next expert batch ("国产GPU完成MoE大模型Day-0适配" §四: conversion
+ * overlapped with the current batch's matmuls on another stream) and the copy
+ * of routed host-resident experts into device slots (moe_cache_fill; the blog
+ * "这个项目我们能学到什么?", "GPU作为专家缓存").  With 0 < n < the SM count,
+ * the persistent matmul kernels launched after this call (moe_w2_mm /
+ * moe_w2_mm_slots on the table GEMV, moe_w2_mm / moe_mxfp4_mm in GEMM mode)
+ * take one CTA per remaining SM, and mxfp4_to_fp8_ws / moe_cache_fill launch
+ * n CTAs that hold one SM each, so the two share the GPU whatever order they
+ * start in; results are unchanged (every tile, row and block is computed the
+ * same way).  0 (the default) gives every launch the whole GPU.  Returns the
+ * previous value, or -1 (setting unchanged) for n < 0 or n > 1024.
+ * Process-wide; host only. */
+MOE_API int moe_set_side_sms(int n);
 
 /* Self-test of the bounded wait (no counterpart in the pages): launches one
  * warp that waits, with limit `cycles` (1 .. 3e9), on a shared-memory

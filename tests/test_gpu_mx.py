@@ -182,7 +182,7 @@ def test_prefill_fp8_full_size_largest_groups_every_row(fmt):
 
 
 def test_conversion_on_reserved_sms_is_bit_identical():
-    """mxfp4_to_fp8_ws with SMs reserved (moe_set_conversion_sms): the same
+    """mxfp4_to_fp8_ws with SMs reserved (moe_set_side_sms): the same
     bytes as the whole-GPU conversion, flags included; the setting is
     restored afterwards."""
     g = np.random.default_rng(5)
@@ -194,17 +194,17 @@ def test_conversion_on_reserved_sms_is_bit_identical():
     slots = np.array([1, 3, 0, 2], dtype=np.int32)
     outs = []
     for n in (0, 7):
-        prev = L.moe_set_conversion_sms(n)
+        prev = L.moe_set_side_sms(n)
         try:
             ws = torch.full((4, rows, K), 0xAB, dtype=torch.uint8, device=DEV)
             err = torch.zeros(1, dtype=torch.int32, device=DEV)
             L.mxfp4_to_fp8_ws(dev(q), dev(s), dev(experts), rows, K, ws, dev(slots), dev_err=err)
             outs.append((host(ws), L.moe_get_error(err)))
         finally:
-            L.moe_set_conversion_sms(prev)
+            L.moe_set_side_sms(prev)
     assert np.array_equal(outs[0][0], outs[1][0])
     assert outs[0][1] == outs[1][1] and outs[0][1] & L.DEVERR_NAN_SCALE
-    assert L.moe_set_conversion_sms(0) == 0
+    assert L.moe_set_side_sms(0) == 0
 
 
 def test_fp8_layer_with_reserved_conversion_sms_is_bit_identical():
@@ -217,10 +217,10 @@ def test_fp8_layer_with_reserved_conversion_sms_is_bit_identical():
     lg = synth.make_logits(w, x_bits=x)
     outs = []
     for conv in (0, 20):
-        ml.conv_sms = conv
+        ml.side_sms = conv
         out, b = run_layer(ml, x, lg)
         assert L.moe_get_error(b.dev_err) == 0
         outs.append((out.clone(), b.h.clone(), b.y.clone()))
     for a, c in zip(outs[0], outs[1]):
         assert torch.equal(a, c)
-    assert L.moe_set_conversion_sms(0) == 0                     # the layer restored the setting
+    assert L.moe_set_side_sms(0) == 0                     # the layer restored the setting

@@ -58,20 +58,23 @@ def test_stage_select_matches_its_definition(E, R, S):
         assert bool(L.moe_get_error(err) & L.DEVERR_OVERFLOW) == over
 
 
-def _pair(w, resident, S=64):
+def _pair(w, resident, S=64, side_sms=0):
     raw = synth.make_w2_layer(w)
     full = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV)
     off = MoELayer("w2host", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV,
-                   resident=resident, stage_slots=S)
+                   resident=resident, stage_slots=S, side_sms=side_sms)
     return raw, full, off
 
 
-@pytest.mark.parametrize("name,frac", [("small", 0.4), ("decode", 0.5)])
-def test_host_resident_layer_bit_identical_to_device_layer(name, frac):
+@pytest.mark.parametrize("name,frac,side", [("small", 0.4, 0), ("decode", 0.5, 0), ("small", 0.4, 12),
+                                            ("decode", 0.5, 16)])
+def test_host_resident_layer_bit_identical_to_device_layer(name, frac, side):
+    """side: SMs reserved for the staging copy, the resident experts' FC1 and
+    FC2 running beside it on the others (moe_set_side_sms)."""
     w = (synth.get_workload("tiny").replace(E=48, H=1024, I=512, k=4, T=16, logits="uniform") if name == "small"
          else synth.get_workload("decode"))
     resident = list(range(0, w.E, int(round(1 / frac))))        # every other / every 2.5th expert on the device
-    raw, full, offl = _pair(w, resident)
+    raw, full, offl = _pair(w, resident, side_sms=side)
     assert offl.R == len(resident) and offl.store[0].is_pinned()
     for bi in range(2):
         x = synth.make_x(w, 0, tid_offset=bi)
@@ -87,6 +90,7 @@ def test_host_resident_layer_bit_identical_to_device_layer(name, frac):
         assert cold > 0                                          # some routed experts came over the link
         assert torch.equal(out_o, out_f)
         assert torch.equal(bo.y, bf.y)
+        assert L.moe_set_side_sms(0) == 0                        # the layer restored the setting
         tok = [0, w.T - 1]
         ref = M.layer(x, lg, w.k, M.w2_expert_weights(*raw), profile="bf16", tokens=tok)
         err, _ = rel_err(host(out_o)[tok], ref["out"])
