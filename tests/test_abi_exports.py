@@ -74,3 +74,24 @@ def test_noalloc_limit_matches_header(lib_path):
     assert lib.moe_w2_mm_workspace_size(L.STAGE_FC1_SWIGLU, 128, 2048, 4096) > cap
     assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 255, 4096, 2048) <= cap
     assert lib.moe_w2_mm_workspace_size(L.STAGE_FC2, 256, 4096, 2048) > cap
+
+
+def test_side_sms_setting_rules(lib_path):
+    """moe_set_side_sms (host only): returns the previous value, rejects
+    counts outside [0, 1024] with -1 and leaves the setting unchanged."""
+    from bit_moe_expert_top_gb300 import _lib as L
+    lib = L.lib()
+    prev = lib.moe_set_side_sms(12)
+    assert lib.moe_set_side_sms(-1) == -1
+    assert lib.moe_set_side_sms(1025) == -1
+    assert lib.moe_set_side_sms(prev) == 12
+    assert L.moe_set_side_sms(prev) == prev
+
+
+def test_split_mode_constant_matches_header(lib_path):
+    """The binding's mode numbers are the header's, MOE_MODE_SPLIT included."""
+    from bit_moe_expert_top_gb300 import _lib as L
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    for name, val in (("AUTO", L.MODE_AUTO), ("GEMV", L.MODE_GEMV), ("GEMM", L.MODE_GEMM), ("SPLIT", L.MODE_SPLIT)):
+        m = re.search(rf"#define MOE_MODE_{name} (\d+)", src)
+        assert m and int(m.group(1)) == val
