@@ -135,7 +135,7 @@ _TRAFFIC = {
                     "src_sha256": "06ffb5709f2843c3905f50859122a3abba95f5bc1a61cc2fd71750663f4e3906"},
     "prefill_fp8_direct": {"bytes": 4672.81e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                           "src_sha256": "8a341d7cc4d6d2a583b06ae1e6218506944e96338ae8d48528ee46cb31d86a81"},
-    "prefill_fp8": {"bytes": 445.64e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
+    "prefill_fp8": {"bytes": 1832.02e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                    "src_sha256": "8a341d7cc4d6d2a583b06ae1e6218506944e96338ae8d48528ee46cb31d86a81"},
     "decode_host": {"bytes": 246.31e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
                    "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
