@@ -264,6 +264,8 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
         torch.cuda.synchronize()
         off = bufs[li].offsets.cpu().numpy()
         work_bytes[i] = mls[li].touched_weight_bytes(off)
+        if i == 0:
+            group_rows = np.diff(off)
         staged[i] = mls[li].staged_bytes(off) if mls[li].fmt == "w2host" else 0
         if L.moe_get_error(bufs[li].dev_err) != 0:
             raise RuntimeError(f"{name}: device error flags set during warm-up")
@@ -365,6 +367,11 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
            "tflops": round(tot_flops / (t_max / 1e3) / 1e12, 2),
            "roofline": roof, "kernels_us": kernels_us,
            "gpu_launches": steps * launches_per_step(mls[0], w.T)}
+    # the expert group sizes of the first token batch (rows per expert)
+    edges = [0, 1, 16, 64, 256, 1024, 4096, 1 << 30]
+    rec["groups"] = {"min": int(group_rows.min()), "max": int(group_rows.max()),
+                     "empty": int((group_rows == 0).sum()), "touched": int((group_rows > 0).sum()),
+                     "hist_edges": edges[:-1], "hist": np.histogram(group_rows, bins=edges)[0].tolist()}
     if mls[0].fmt == "w2host":
         sb = sum(staged[i % batches] for i in range(steps))
         rec["host_resident"] = {"resident_experts": mls[0].R, "staging_slots": mls[0].S,
@@ -433,6 +440,7 @@ def run_gpu(args):
         "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values()),
         "clocks": head.get("clocks"),
     }
+    res["groups"] = head["groups"]
     if "host_resident" in head:
         res["host_resident"] = head["host_resident"]
     if subs:
