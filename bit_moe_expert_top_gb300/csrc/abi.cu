@@ -226,23 +226,31 @@ int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int32_t* exp
                      "mxfp4_to_fp8_ws");
 }
 
+// Argument checks shared by the expert-matmul calls.  Returns MOE_OK, a
+// status, or kNoRows when the activation has no rows: the call then does
+// nothing (its buffers may be empty, their pointers NULL).
+constexpr int kNoRows = -1;
+
 static int check_mm(const char* who, int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale,
-                    const int32_t* offsets, int E, int N, int K, const void* out, int out_fmt,
+                    int act_rows, const int32_t* offsets, int E, int N, int K, const void* out, int out_fmt,
                     const uint8_t* out_scale) {
   if (stage != MOE_STAGE_FC1_SWIGLU && stage != MOE_STAGE_FC2) return fail(MOE_ERR_ARG, "%s: bad stage", who);
   if (mode < MOE_MODE_AUTO || mode > MOE_MODE_SPLIT) return fail(MOE_ERR_ARG, "%s: bad mode", who);
   if (E < 1 || E > 1024 || N <= 0 || K <= 0 || N % 128 || K % 128 || K > 8192)
     return fail(MOE_ERR_ARG, "%s: bad shape (N, K multiples of 128, K <= 8192, 1 <= E <= 1024)", who);
   if (act_fmt != MOE_FMT_BF16 && act_fmt != MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "%s: act_fmt", who);
-  if (act_fmt == MOE_FMT_MXFP8 && (!act_scale || !aligned(act_scale, 4)))
-    return fail(MOE_ERR_ARG, "%s: act_scale NULL or not 4-byte aligned", who);
-  if (!act || !offsets || !out || !aligned(act, 16)) return fail(MOE_ERR_ARG, "%s: NULL or misaligned pointer", who);
   if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32 && out_fmt != MOE_FMT_MXFP8 && out_fmt != MOE_FMT_MXFP8_BF16)
     return fail(MOE_ERR_ARG, "%s: out_fmt", who);
   if (out_fmt == MOE_FMT_MXFP8_BF16 && stage != MOE_STAGE_FC1_SWIGLU)
     return fail(MOE_ERR_ARG, "%s: MXFP8_BF16 output is for FC1", who);
-  if (out_fmt == MOE_FMT_MXFP8 && (stage != MOE_STAGE_FC1_SWIGLU || !out_scale))
-    return fail(MOE_ERR_ARG, "%s: MXFP8 output is for FC1 with out_scale", who);
+  if (out_fmt == MOE_FMT_MXFP8 && stage != MOE_STAGE_FC1_SWIGLU)
+    return fail(MOE_ERR_ARG, "%s: MXFP8 output is for FC1", who);
+  if (act_rows < 0) return fail(MOE_ERR_ARG, "%s: act_rows < 0", who);
+  if (act_rows == 0) return kNoRows;
+  if (act_fmt == MOE_FMT_MXFP8 && (!act_scale || !aligned(act_scale, 4)))
+    return fail(MOE_ERR_ARG, "%s: act_scale NULL or not 4-byte aligned", who);
+  if (!act || !offsets || !out || !aligned(act, 16)) return fail(MOE_ERR_ARG, "%s: NULL or misaligned pointer", who);
+  if (out_fmt == MOE_FMT_MXFP8 && !out_scale) return fail(MOE_ERR_ARG, "%s: MXFP8 output needs out_scale", who);
   return check_device();
 }
 
@@ -257,8 +265,8 @@ int moe_w2_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* 
               const int32_t* act_row, int act_row_div, const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
               const int32_t* expert_slot, int E, int N, int K, void* out, int out_fmt, uint8_t* out_scale, void* ws,
               size_t ws_bytes, uint32_t* dev_err, void* stream) {
-  if (int r = check_mm("moe_w2_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
-    return r;
+  if (int r = check_mm("moe_w2_mm", stage, mode, act, act_fmt, act_scale, act_rows, offsets, E, N, K, out, out_fmt, out_scale))
+    return r == kNoRows ? MOE_OK : r;
   if (!codes_k || !scales_k || !aligned(codes_k, 16) || !aligned(scales_k, 16))
     return fail(MOE_ERR_ARG, "moe_w2_mm: weights NULL or not 16-byte aligned");
   if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_w2_mm: act_rows < 0");
@@ -305,9 +313,9 @@ int moe_w2_mm_noalloc(int stage, const void* act, int act_rows, const int32_t* a
                       const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
                       const int32_t* expert_slot, int E, int N, int K, int rows, void* out, int out_fmt,
                       uint32_t* dev_err, void* stream) {
-  if (int r = check_mm("moe_w2_mm_noalloc", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, offsets, E, N, K, out,
+  if (int r = check_mm("moe_w2_mm_noalloc", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, act_rows, offsets, E, N, K, out,
                        out_fmt, nullptr))
-    return r;
+    return r == kNoRows ? MOE_OK : r;
   if (out_fmt == MOE_FMT_MXFP8) return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: out_fmt must be BF16 or F32");
   if (!codes_k || !scales_k || !aligned(codes_k, 16) || !aligned(scales_k, 16))
     return fail(MOE_ERR_ARG, "moe_w2_mm_noalloc: weights NULL or not 16-byte aligned");
@@ -364,9 +372,9 @@ int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_row, int
                         const uint16_t* scales1, const uint8_t* codes2, const uint16_t* scales2,
                         const int32_t* offsets, const int32_t* expert_slot, int E, int H, int I, void* h, void* y,
                         int y_fmt, void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
-  if (int r = check_mm("moe_w2_decode_fused", MOE_STAGE_FC1_SWIGLU, MOE_MODE_GEMV, x, MOE_FMT_BF16, nullptr, offsets,
+  if (int r = check_mm("moe_w2_decode_fused", MOE_STAGE_FC1_SWIGLU, MOE_MODE_GEMV, x, MOE_FMT_BF16, nullptr, act_rows, offsets,
                        E, I, H, h, MOE_FMT_BF16, nullptr))
-    return r;
+    return r == kNoRows ? MOE_OK : r;
   if (!y || !aligned(h, 16) || (y_fmt != MOE_FMT_BF16 && y_fmt != MOE_FMT_F32))
     return fail(MOE_ERR_ARG, "moe_w2_decode_fused: h / y / y_fmt");
   if (!codes1 || !scales1 || !codes2 || !scales2 || !aligned(codes1, 16) || !aligned(scales1, 16) ||
@@ -429,9 +437,9 @@ int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_
                  void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
   (void)ws;
   (void)ws_bytes;
-  if (int r = check_mm("moe_mxfp4_mm", stage, mode, act, act_fmt, act_scale, offsets, E, N, K, out, out_fmt, out_scale))
-    return r;
   if (mode == MOE_MODE_SPLIT) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: MOE_MODE_SPLIT is for 2-bit weights");
+  if (int r = check_mm("moe_mxfp4_mm", stage, mode, act, act_fmt, act_scale, act_rows, offsets, E, N, K, out, out_fmt, out_scale))
+    return r == kNoRows ? MOE_OK : r;
   if (act_row && act_row_div < 1) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_row_div < 1");
   if (act_rows < 0) return fail(MOE_ERR_ARG, "moe_mxfp4_mm: act_rows < 0");
   if (expert_begin < 0 || expert_end > E || expert_begin > expert_end)
@@ -503,9 +511,9 @@ int moe_w2_mm_slots(int stage, const void* act, int act_rows, const int32_t* act
                     const uint8_t* codes_k, const uint16_t* scales_k, const int32_t* offsets,
                     const int32_t* weight_slot, int slot_lo, int slot_hi, int E, int N, int K, void* out, int out_fmt,
                     void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
-  if (int r = check_mm("moe_w2_mm_slots", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, offsets, E, N, K, out,
+  if (int r = check_mm("moe_w2_mm_slots", stage, MOE_MODE_GEMV, act, MOE_FMT_BF16, nullptr, act_rows, offsets, E, N, K, out,
                        out_fmt, nullptr))
-    return r;
+    return r == kNoRows ? MOE_OK : r;
   if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32) return fail(MOE_ERR_ARG, "moe_w2_mm_slots: out_fmt");
   if (!codes_k || !scales_k || !weight_slot || !aligned(codes_k, 16) || !aligned(scales_k, 16))
     return fail(MOE_ERR_ARG, "moe_w2_mm_slots: weights / slot map NULL or misaligned");

@@ -261,7 +261,11 @@ MOE_API int mxfp4_to_fp8_ws(const uint8_t* e2m1, const uint8_t* e8m0, const int3
  * tensor-core path (GEMM) also takes out_fmt MXFP8_BF16 (h MXFP8-rounded, as
  * bf16), the form its FC2 reads.  Rounding:
  * out = RNE of the fp32 result into out_fmt.  Rows of unselected experts are
- * left untouched.
+ * left untouched.  A call whose activation has no rows (act_rows == 0, e.g.
+ * an empty token batch) checks its scalar arguments and otherwise does
+ * nothing: its buffers may be empty and their pointers NULL.  This holds for
+ * every expert-matmul entry point (moe_w2_mm, moe_w2_mm_noalloc,
+ * moe_w2_decode_fused, moe_mxfp4_mm, moe_w2_mm_slots).
  * Modes: GEMV = CUDA-core kernels (2-bit with a workspace and K a multiple
  * of 512: shared-memory partial-sum tables with K split in 512-element
  * slices over CTAs; otherwise, and for MXFP4 / FP8: register decode); GEMM =
