@@ -57,7 +57,11 @@ namespace {
 constexpr int kMxWarps = 16;
 constexpr int kMxThreads = kMxWarps * 32;
 constexpr int kKS = 128;        // K elements per stage: 4 MMAs of K = 32, one E8M0 word per row
-constexpr int kMS = 4;          // pipeline stages
+// pipeline stages: 4 with 128-token tiles; 5 with 32-token tiles, where a
+// stage is small (36 KB) and the weight bytes in flight are what bound the
+// decode-sized launch (one stage carries 16 KB of packed weights from HBM)
+template <int NT>
+__host__ __device__ constexpr int mx_stages() { return NT == 32 ? 5 : 4; }
 constexpr int kMTab = 12288;    // barriers, flags, tile tables (E <= 1024)
 constexpr int kMStg = 16384;    // epilogue staging: 8 warps x [32 tokens][32 outputs] x 2 bytes
 constexpr uint32_t kSFCols = 16;  // TMEM scale columns per stage: SFA block 0 (+0), block 1 (+4), SFB (+8)
@@ -68,9 +72,9 @@ template <int NT>
 __host__ __device__ constexpr int mx_stage_bytes() { return NT * kKS + 2 * 128 * kKS; }
 template <int NT>
 __host__ __device__ constexpr size_t mx_smem_bytes() {
-  return 1024 + kMTab + kMStg + static_cast<size_t>(kMS) * mx_stage_bytes<NT>();
+  return 1024 + kMTab + kMStg + static_cast<size_t>(mx_stages<NT>()) * mx_stage_bytes<NT>();
 }
-static_assert(mx_smem_bytes<128>() <= 232448, "shared memory");
+static_assert(mx_smem_bytes<128>() <= 232448 && mx_smem_bytes<32>() <= 232448, "shared memory");
 
 struct MxParams {
   const uint8_t* act_scale;  // E8M0 [rows_total][K/32] of the activation rows
@@ -102,6 +106,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_mm_kernel(const __grid_const
   constexpr int kBTile = NT * kKS;        // token bytes per stage
   constexpr int kABlock = 128 * kKS;      // shared bytes of one weight block per stage
   constexpr int kStage = mx_stage_bytes<NT>();
+  constexpr int kMS = mx_stages<NT>();
   constexpr uint32_t kATx = AF == kAE2M1 ? 128u * kKS / 2 : 128u * kKS;  // bytes a weight-block copy moves
   constexpr uint32_t kSF0 = 2 * NT;                   // first scale column (after D_0, D_1)
   constexpr uint32_t kSFU = kSF0 + kMS * kSFCols;     // FP8 workspace: the unit weight scales
