@@ -128,15 +128,15 @@ _TRAFFIC = {
     "decode_unfused": {"bytes": 256.51e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
                       "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
     "decode_mxfp4": {"bytes": 401.82e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
-                    "src_sha256": "8a341d7cc4d6d2a583b06ae1e6218506944e96338ae8d48528ee46cb31d86a81"},
+                    "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
     "mixed_decode": {"bytes": 630.41e6, "src": ['gemv_lut.cu', 'gemm_tmem.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                     "src_sha256": "4f7fa1efceafe52ea65964c2381153348ac85af55f506bca3629c11bc93039b3"},
     "prefill_bf16": {"bytes": 2301.51e6, "src": ['gemm_tmem.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                     "src_sha256": "06ffb5709f2843c3905f50859122a3abba95f5bc1a61cc2fd71750663f4e3906"},
-    "prefill_fp8_direct": {"bytes": 4672.81e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
-                          "src_sha256": "8a341d7cc4d6d2a583b06ae1e6218506944e96338ae8d48528ee46cb31d86a81"},
-    "prefill_fp8": {"bytes": 1832.02e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
-                   "src_sha256": "8a341d7cc4d6d2a583b06ae1e6218506944e96338ae8d48528ee46cb31d86a81"},
+    "prefill_fp8_direct": {"bytes": 4672.7e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
+                          "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
+    "prefill_fp8": {"bytes": 1820.26e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
+                   "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
     "decode_host": {"bytes": 246.31e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
                    "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
 }
