@@ -447,6 +447,12 @@ def run_gpu(args):
         res["workloads"] = subs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.workload, steps=1)
+        # the oracle beside two more configurations, on 16-token samples, in
+        # the sub-records of those names (the FP8 profile's oracle takes about
+        # a minute of one core per token: left out of the default run)
+        for name in ("mixed_decode", "prefill_bf16"):
+            if name in subs:
+                subs[name]["cpu_baseline"] = cpu_baseline(name, steps=1, max_tokens=16)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -627,11 +633,14 @@ def oracle_steps(workload, steps, max_tokens=None):
     return times, procs, cores, ntok
 
 
-def cpu_baseline(workload, steps=1):
-    """The oracle on the host cores, whole layer steps of `workload`."""
+def cpu_baseline(workload, steps=1, max_tokens=None):
+    """The oracle on the host cores, whole layer steps of `workload` (or a
+    bounded sample of `max_tokens` of its tokens)."""
     from bit_moe_expert_top_gb300 import synth
     w = synth.get_workload(workload)
     max_tok = w.T if _decode_like(w) else 16   # prefill steps: a bounded token sample
+    if max_tokens is not None:
+        max_tok = min(max_tok, max_tokens)
     try:
         times, procs, cores, ntok = oracle_steps(workload, steps, max_tok)
     except Exception as e:  # reported, not fatal to the GPU line
