@@ -48,7 +48,7 @@ constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kBuildWarps = 16;               // warps that build a segment's tables
 constexpr int kBR = 16;                       // weight rows per batch (4 row quads; 32-row batches measured slower)
 constexpr int kSW = 512;                      // K elements per slice
-constexpr int kPrologue = 12288;              // shared bytes below the table window
+constexpr int kPrologue = 16640;              // shared bytes below the table window
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
@@ -60,7 +60,9 @@ constexpr int kXBufOff = kSegTabOff + 8 * kSegCap;  // bf16 [2][kSW]
 static_assert(kXBufOff + 2 * kSW * 2 <= kPrologue, "prologue overflow");
 static_assert(4 * (kMaxE + 1) <= kSegTabOff, "prologue overflow");
 constexpr int kSlotTabOff = 8192;             // int [E]: weight slot of each expert
-static_assert(kXBufOff + 2 * kSW * 2 <= kSlotTabOff && kSlotTabOff + 4 * kMaxE <= kPrologue, "prologue overflow");
+constexpr int kOffTabOff = 12288;             // int [E+1]: offsets[e], the first permuted row of expert e
+static_assert(kXBufOff + 2 * kSW * 2 <= kSlotTabOff && kSlotTabOff + 4 * kMaxE <= kOffTabOff, "prologue overflow");
+static_assert(kOffTabOff + 4 * (kMaxE + 1) <= kPrologue, "prologue overflow");
 
 struct LutParams {
   const uint16_t* act;
@@ -168,18 +170,14 @@ MOE_D void rs_level2(float2* v, int lane, int m) {
   }
 }
 
-// The table GEMV of one call (FC1 or FC2) by one CTA of the persistent grid.
-MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
+// Shared-memory prologue of one call (FC1 or FC2) by one CTA: the selected
+// rows before each expert (pref), each expert's weight slot and first
+// permuted row.  Reads only the grouping (offsets) and the expert maps.
+MOE_D void lut_prologue(const LutParams& P, uint8_t* smem) {
   int* pref = reinterpret_cast<int*>(smem);  // [E+1] selected permuted rows before expert e
   int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);  // [E] weight slot of expert e
-
+  int* off_s = reinterpret_cast<int*>(smem + kOffTabOff);      // [E+1] offsets
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t base = smem_u32(smem);
-  const uint32_t table_win = (base + kPrologue + 65535u) & ~65535u;
-  float* table_f = reinterpret_cast<float*>(smem + (table_win - base));
-  const uint32_t lanebase = table_win + 4u * static_cast<uint32_t>(lane);
-  const int NSL = P.NSL, NB = P.NB;
-  const bool fc1 = P.fc1 != 0;
 
   // ---- selected rows per expert, exclusive prefix: every thread loads the
   // counts of experts 2t and 2t+1 at once (one round trip), then a block scan
@@ -190,17 +188,18 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
     for (int h = 0; h < 2; ++h) {
       const int e = 2 * tid + h;
       if (e < P.E) {
-        const int c = P.offsets[e + 1] - P.offsets[e];
+        const int lo = P.offsets[e], hi = P.offsets[e + 1];
+        const int c = hi - lo;
+        const int sm = P.select ? P.select_map[e] : 0;
+        const int ws = P.wslot ? P.wslot[e] : e;
         bool sel = c > 0;
-        if (sel && P.select == 1) sel = P.select_map[e] < 0;
-        if (sel && P.select == 2) sel = P.select_map[e] >= 0;
+        if (sel && P.select == 1) sel = sm < 0;
+        if (sel && P.select == 2) sel = sm >= 0;
         if (sel && P.split == 1) sel = c < kSplitRows;
-        int ws = e;
-        if (P.wslot) {
-          ws = P.wslot[e];
-          sel = sel && ws >= P.slot_lo && ws < P.slot_hi;
-        }
+        if (P.wslot) sel = sel && ws >= P.slot_lo && ws < P.slot_hi;
         slot_tab[e] = ws;
+        off_s[e] = lo;
+        if (e == P.E - 1) off_s[P.E] = hi;
         if (sel) n[h] = c;
       }
     }
@@ -221,9 +220,14 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
     if (tid == kLutThreads - 1) pref[P.E] = excl + local;  // the total (also for E = 1024)
   }
   __syncthreads();
+}
 
-  // ---- the permuted row of every selected row for the finishing kernel
-  // (-1 where the row is skipped: beyond the scratch, or a bad token index)
+// The permuted row of every selected row, for the summing step (-1 where
+// the row is skipped: beyond the scratch, or a bad token index); global.
+MOE_D void lut_rows(const LutParams& P, const uint8_t* smem) {
+  const int* pref = reinterpret_cast<const int*>(smem);
+  const int* off_s = reinterpret_cast<const int*>(smem + kOffTabOff);
+  const int tid = threadIdx.x;
   {
     const int nsel = pref[P.E];
     if (blockIdx.x == 0 && tid == 0) P.rows_hdr[0] = nsel;
@@ -234,7 +238,7 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
         const int mid = (lo + hi) >> 1;
         if (pref[mid] <= i) lo = mid; else hi = mid;
       }
-      const int p = P.offsets[lo] + (i - pref[lo]);
+      const int p = off_s[lo] + (i - pref[lo]);
       bool ok = p < P.A;
       if (ok) {
         const int row = P.act_row ? P.act_row[p] / P.act_row_div : p;
@@ -243,17 +247,40 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
       P.rows_hdr[1 + i] = ok ? p : -1;
     }
   }
+}
+
+// The table GEMV of one call (FC1 or FC2) by one CTA of the persistent grid,
+// after lut_prologue.
+MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
+  int* pref = reinterpret_cast<int*>(smem);
+  int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);
+  const int* off_s = reinterpret_cast<const int*>(smem + kOffTabOff);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t table_win = (base + kPrologue + 65535u) & ~65535u;
+  float* table_f = reinterpret_cast<float*>(smem + (table_win - base));
+  const uint32_t lanebase = table_win + 4u * static_cast<uint32_t>(lane);
+  const int NSL = P.NSL, NB = P.NB;
+  const bool fc1 = P.fc1 != 0;
 
   // ---- this CTA's unit range; unit = (selected row, slice, batch), batch fastest
   const int64_t per_row = static_cast<int64_t>(NSL) * NB;
   const int64_t total = static_cast<int64_t>(pref[P.E]) * per_row;
   const int64_t u_beg = total * blockIdx.x / gridDim.x;
   const int64_t u_end = total * (blockIdx.x + 1) / gridDim.x;
+  if (u_beg >= u_end) return;
 
   const int64_t mat_codes = static_cast<int64_t>(P.R) * (P.K / 4);    // bytes per expert
   const int64_t mat_scales = static_cast<int64_t>(P.R) * (P.K / 32);  // bf16 per expert
   const int64_t slice_codes = static_cast<int64_t>(P.R) * (kSW / 4);
   const int64_t slice_scales = static_cast<int64_t>(P.R) * (kSW / 32);
+  // byte offsets of a batch's four row quads from its first: FC1 batches are
+  // quads 2rb, 2rb+1 (gate rows) and N/4 + 2rb, N/4 + 2rb + 1 (up rows); FC2
+  // batches quads 4rb .. 4rb+3.  A quad is 512 code bytes and 128 scale bytes.
+  const uint32_t cstep = fc1 ? 1024u : 2048u, sstep = fc1 ? 256u : 512u;
+  const uint32_t chi = fc1 ? static_cast<uint32_t>(P.N) * 128u : 1024u;
+  const uint32_t shi = fc1 ? static_cast<uint32_t>(P.N) * 32u : 256u;
+  const uint32_t sum_step = static_cast<uint32_t>(NSL) * kBR;           // scratch floats per batch
 
   uint4 v[4];
   uint2 sc[4];
@@ -267,27 +294,25 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
     }
     return lo;
   };
-  // quad index (rows 4Q..4Q+3 of the expert) of quad q of batch rb: FC1
-  // batches are 8 gate rows then the 8 matching up rows
-  auto quad_of = [&](int rb, int q) -> uint32_t {
-    if (fc1) return static_cast<uint32_t>(q < 2 ? rb * 2 + q : (P.N >> 2) + rb * 2 + (q - 2));
-    return static_cast<uint32_t>(rb * 4 + q);
-  };
   // this lane's code / scale addresses in slice s of expert e
   auto codes_at = [&](int e, int sl) { return P.codes + slot_tab[e] * mat_codes + sl * slice_codes + lane * 16; };
   auto scales_at = [&](int e, int sl) {
     return reinterpret_cast<const uint8_t*>(P.scales + slot_tab[e] * mat_scales + sl * slice_scales) + (lane >> 1) * 8;
   };
   auto issue = [&](const uint8_t* gc, const uint8_t* gs, int rb) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t Q = quad_of(rb, q);
-      v[q] = ldg_stream(gc + Q * 512u);
-      sc[q] = ldg_stream2(gs + Q * 128u);
-    }
+    const uint8_t* c0 = gc + static_cast<uint32_t>(rb) * cstep;
+    const uint8_t* c2 = c0 + chi;
+    const uint8_t* s0 = gs + static_cast<uint32_t>(rb) * sstep;
+    const uint8_t* s2 = s0 + shi;
+    v[0] = ldg_stream(c0);
+    v[1] = ldg_stream(c0 + 512);
+    v[2] = ldg_stream(c2);
+    v[3] = ldg_stream(c2 + 512);
+    sc[0] = ldg_stream2(s0);
+    sc[1] = ldg_stream2(s0 + 128);
+    sc[2] = ldg_stream2(s2);
+    sc[3] = ldg_stream2(s2 + 128);
   };
-
-  if (u_beg >= u_end) return;
 
   // ---- the CTA's segments (one per (selected row, slice) table): their
   // permuted row and token row, looked up once for all of them in parallel
@@ -295,13 +320,14 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
   // each segment's 512 activations brought into shared memory by cp.async
   // one segment ahead
   const int64_t seg_first = u_beg / NB;
-  const int64_t nseg = (u_end - 1) / NB - seg_first + 1;
+  const int64_t seg_last = (u_end - 1) / NB;
+  const int64_t nseg = seg_last - seg_first + 1;
   int2* seg_tab = reinterpret_cast<int2*>(smem + kSegTabOff);
   const uint16_t* xbuf = reinterpret_cast<const uint16_t*>(smem + kXBufOff);
   auto seg_lookup = [&](int64_t sg) -> int2 {  // (p, row; row = -1 if the segment is skipped)
     const int ps = static_cast<int>(sg / NSL);
     const int ee = expert_of(ps);
-    const int pp = P.offsets[ee] + (ps - pref[ee]);
+    const int pp = off_s[ee] + (ps - pref[ee]);
     if (pp >= P.A) {  // the scratch does not cover this row: report and skip
       set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
       return make_int2(pp, -1);
@@ -322,7 +348,7 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
   // activations of segment sg into buffer sg & 1: 128 threads x 8 bytes; one
   // cp.async group per call on every thread (empty where nothing is copied)
   auto prefetch_x = [&](int64_t sg) {
-    if (sg < seg_first + nseg && tid < kSW / 4) {
+    if (sg <= seg_last && tid < kSW / 4) {
       const int2 si = seg_info(sg);
       if (si.y >= 0) {
         const int sl = static_cast<int>(sg % NSL);
@@ -332,6 +358,16 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
     }
     cp_async_commit();
   };
+  // segment sg: its weight pointers and the end of the CTA's batches in it
+  // (batch indices inside a segment are 32-bit: NB <= K/8)
+  auto seg_ptrs = [&](int64_t sg, const uint8_t*& gc, const uint8_t*& gs) {
+    const int ps = static_cast<int>(sg / NSL);
+    const int sl = static_cast<int>(sg - static_cast<int64_t>(ps) * NSL);
+    const int ee = expert_of(ps);
+    gc = codes_at(ee, sl);
+    gs = scales_at(ee, sl);
+  };
+  auto seg_hi = [&](int64_t sg) { return sg == seg_last ? static_cast<int>(u_end - sg * NB) : NB; };
   prefetch_x(seg_first);
   prefetch_x(seg_first + 1);
   // A warp's units: batches warp, warp + 16, ... of each segment (one segment
@@ -339,28 +375,32 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
   // unit go out while the current one is consumed, also across a segment
   // boundary; the row checks (which need global loads) only gate the table
   // build and the stores, never the weight loads.
-  int64_t seg = u_beg / NB;
-  int psel = static_cast<int>(seg / NSL);
-  int s = static_cast<int>(seg - static_cast<int64_t>(psel) * NSL);
-  int e = expert_of(psel);
-  const uint8_t* gcodes = codes_at(e, s);
-  const uint8_t* gscales = scales_at(e, s);
-  int64_t seg_end = min(u_end, (seg + 1) * NB);
-  int64_t uw = u_beg + warp;
+  int64_t seg = seg_first;
+  const uint8_t* gcodes;
+  const uint8_t* gscales;
+  seg_ptrs(seg, gcodes, gscales);
+  int rb_hi = seg_hi(seg);
+  int rb = static_cast<int>(u_beg - seg * NB) + warp;
   bool pending = false;
-  if (uw < seg_end) {
-    issue(gcodes, gscales, static_cast<int>(uw - seg * NB));
+  if (rb < rb_hi) {
+    issue(gcodes, gscales, rb);
     pending = true;
   }
   while (true) {
-    const int64_t seg0 = seg * NB;
-    const bool has_next = seg_end < u_end;
-    const int64_t nseg_end = min(u_end, seg_end + NB);
+    const bool has_next = seg < seg_last;
+    const uint8_t* ncodes = gcodes;
+    const uint8_t* nscales = gscales;
+    int nrb_hi = 0;
+    if (has_next) {
+      seg_ptrs(seg + 1, ncodes, nscales);
+      nrb_hi = seg_hi(seg + 1);
+    }
     const int2 si = seg_info(seg);
-    const int p = si.x;
     const bool valid = si.y >= 0;
-    if (!pending && uw < seg_end) {
-      issue(gcodes, gscales, static_cast<int>(uw - seg0));
+    const int s = static_cast<int>(seg % NSL);
+    float* const sbase = P.scratch + (static_cast<size_t>(si.x) * NB * NSL + s) * kBR + (lane >> 1);
+    if (!pending && rb < rb_hi) {
+      issue(gcodes, gscales, rb);
       pending = true;
     }
 
@@ -392,69 +432,71 @@ MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
     __syncthreads();
     prefetch_x(seg + 2);  // into the buffer this build has finished reading
 
-    while (uw < seg_end) {
-      const int rb = static_cast<int>(uw - seg0);
-      // the warp's next unit: the same segment, or its first batch of the next
-      int64_t un = uw + kLutWarps;
-      const uint8_t* nc = gcodes;
-      const uint8_t* ns = gscales;
-      int rbn = rb + kLutWarps;
-      bool more = un < seg_end;
-      if (!more) {
-        un = seg_end + warp;
-        more = has_next && un < nseg_end;
-        if (more) {
-          const int64_t nseg = seg + 1;
-          const int np = static_cast<int>(nseg / NSL);
-          const int nsl = static_cast<int>(nseg - static_cast<int64_t>(np) * NSL);
-          const int ne = expert_of(np);
-          nc = codes_at(ne, nsl);
-          ns = scales_at(ne, nsl);
+    bool more = false;
+    if (rb < rb_hi) {
+      while (true) {
+        // the warp's next unit: the same segment, or its first batch of the next
+        const int rb_same = rb + kLutWarps;
+        const bool same = rb_same < rb_hi;
+        int rbn = rb_same;
+        const uint8_t* nc = gcodes;
+        const uint8_t* ns = gscales;
+        more = same;
+        if (!same) {
           rbn = warp;
+          more = has_next && warp < nrb_hi;
+          nc = ncodes;
+          ns = nscales;
         }
-      }
-      if (valid) {
+        if (valid) {
+          const uint8_t* c0 = nc + static_cast<uint32_t>(rbn) * cstep;
+          const uint8_t* s0 = ns + static_cast<uint32_t>(rbn) * sstep;
+          const uint8_t* const cq[4] = {c0, c0 + 512, c0 + chi, c0 + chi + 512};
+          const uint8_t* const sq[4] = {s0, s0 + 128, s0 + shi, s0 + shi + 128};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 w4 = v[q];
-          const uint2 s4 = sc[q];
-          acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
-          acc[2 * q + 1] = word_pair(w4.z, w4.w, s4.y, lanebase);
-          if (more) {  // the next unit's loads go out while this one is consumed
-            const uint32_t Q = quad_of(rbn, q);
-            v[q] = ldg_stream(nc + Q * 512u);
-            sc[q] = ldg_stream2(ns + Q * 128u);
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w4 = v[q];
+            const uint2 s4 = sc[q];
+            acc[2 * q] = word_pair(w4.x, w4.y, s4.x, lanebase);
+            acc[2 * q + 1] = word_pair(w4.z, w4.w, s4.y, lanebase);
+            if (more) {  // the next unit's loads go out while this one is consumed
+              v[q] = ldg_stream(cq[q]);
+              sc[q] = ldg_stream2(sq[q]);
+            }
           }
+          // ---- reduce-scatter: afterwards lanes 2r and 2r + 1 hold the slice
+          // sum of batch row r
+          rs_level2<4>(acc, lane, 16);
+          rs_level2<2>(acc, lane, 8);
+          rs_level2<1>(acc, lane, 4);
+          const bool hi = (lane & 2) != 0;
+          const float keep = hi ? acc[0].y : acc[0].x;
+          const float send = hi ? acc[0].x : acc[0].y;
+          float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          if ((lane & 1) == 0) __stcg(sbase + static_cast<uint32_t>(rb) * sum_step, sum);
+        } else if (more) {
+          issue(nc, ns, rbn);
         }
-        // ---- reduce-scatter: afterwards lanes 2r and 2r + 1 hold the slice
-        // sum of batch row r
-        rs_level2<4>(acc, lane, 16);
-        rs_level2<2>(acc, lane, 8);
-        rs_level2<1>(acc, lane, 4);
-        const bool hi = (lane & 2) != 0;
-        const float keep = hi ? acc[0].y : acc[0].x;
-        const float send = hi ? acc[0].x : acc[0].y;
-        float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        const size_t cell = static_cast<size_t>(p) * NB + rb;
-        if ((lane & 1) == 0) __stcg(P.scratch + (cell * NSL + s) * kBR + (lane >> 1), sum);
-      } else if (more) {
-        issue(nc, ns, rbn);
+        if (!same) break;
+        rb = rb_same;
       }
-      uw = un;
-      pending = more;
     }
+    pending = more;
     if (!has_next) break;
     // ---- advance to the next segment
-    uw = seg_end + warp;
     ++seg;
-    psel = static_cast<int>(seg / NSL);
-    s = static_cast<int>(seg - static_cast<int64_t>(psel) * NSL);
-    e = expert_of(psel);
-    gcodes = codes_at(e, s);
-    gscales = scales_at(e, s);
-    seg_end = nseg_end;
+    gcodes = ncodes;
+    gscales = nscales;
+    rb_hi = nrb_hi;
+    rb = warp;
   }
+}
+
+MOE_D void lut_run(const LutParams& P, uint8_t* smem) {
+  lut_prologue(P, smem);
+  lut_rows(P, smem);
+  lut_main(P, smem);
 }
 
 __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams P) {
@@ -464,31 +506,48 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_lut_kernel(const LutParams 
   lut_run(P, smem);
 }
 
+// The NSL (<= kMaxSlices) slice sums at sp (stride kBR) added in slice
+// order; every load is issued before the first add.
+constexpr int kMaxSlices = 16;  // K <= 8192
+MOE_D float slice_total(const float* sp, int NSL) {
+  float v[kMaxSlices];
+#pragma unroll
+  for (int q = 0; q < kMaxSlices; ++q) v[q] = q < NSL ? __ldcg(sp + q * kBR) : 0.f;
+  float t = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxSlices; ++q)
+    if (q < NSL) t += v[q];
+  return t;
+}
+
 // One output of the finishing step: the NSL slice sums of selected row i,
-// output n, added in slice order; SwiGLU for FC1; rounded and stored.
-MOE_D void finish_one(const LutParams& P, int i, int n) {
+// output n, added in slice order, SwiGLU for FC1, in t; returns the output's
+// element index, or -1 where the row is skipped.
+MOE_D int64_t finish_value(const LutParams& P, int i, int n, float& t) {
   const int NSL = P.NSL, NB = P.NB;
   const int p = __ldcg(P.rows_hdr + 1 + i);
-  if (p < 0) return;
-  float t;
+  if (p < 0) return -1;
   if (P.fc1) {  // batch n/8: rows 0..7 gate rows, 8..15 the matching up rows
     const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 3)) * NSL * kBR + (n & 7);
-    float g = 0.f, u = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < NSL; ++q) {
-      g += __ldcg(sp + q * kBR);
-      u += __ldcg(sp + q * kBR + 8);
-    }
+    const float g = slice_total(sp, NSL);
+    const float u = slice_total(sp + 8, NSL);
     t = silu_f32(g) * u;
   } else {
     const float* sp = P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * kBR + (n & 15);
-    t = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < NSL; ++q) t += __ldcg(sp + q * kBR);
+    t = slice_total(sp, NSL);
   }
-  const size_t o = static_cast<size_t>(p) * P.N + n;
+  return static_cast<int64_t>(p) * P.N + n;
+}
+
+MOE_D void finish_store(const LutParams& P, int64_t o, float t) {
   if (P.out_fmt == MOE_FMT_F32) static_cast<float*>(P.out)[o] = t;
   else static_cast<uint16_t*>(P.out)[o] = f32_to_bf16_rne(t);
+}
+
+MOE_D void finish_one(const LutParams& P, int i, int n) {
+  float t;
+  const int64_t o = finish_value(P, i, n, t);
+  if (o >= 0) finish_store(P, o, t);
 }
 
 // Sums the NSL slice sums of every output in slice order, applies SwiGLU for
@@ -510,12 +569,19 @@ __global__ void __launch_bounds__(256) w2_lut_finish_kernel(const LutParams P) {
 // it reaches k * gridDim.x.  The wait is bounded: past the limit the CTA
 // records MOE_DEVERR_TIMEOUT and the kernel returns (the others then time out
 // too).
-MOE_D bool grid_barrier(unsigned int* cnt, unsigned int target, long long limit, uint32_t* dev_err) {
-  __shared__ int s_ok;
+// The barrier in two halves, so that a CTA can do work of its own between
+// its arrival and its wait.
+MOE_D void grid_arrive(unsigned int* cnt) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this CTA's results before its arrival
     atomicAdd(cnt, 1u);
+  }
+}
+
+MOE_D bool grid_wait(unsigned int* cnt, unsigned int target, long long limit, uint32_t* dev_err) {
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
     const long long t0 = clock64();
     int ok = 1;
     while (true) {
@@ -536,12 +602,25 @@ MOE_D bool grid_barrier(unsigned int* cnt, unsigned int target, long long limit,
   return s_ok != 0;
 }
 
+MOE_D bool grid_barrier(unsigned int* cnt, unsigned int target, long long limit, uint32_t* dev_err) {
+  grid_arrive(cnt);
+  return grid_wait(cnt, target, limit, dev_err);
+}
+
+// The finishing step over the whole grid, two outputs per thread and round
+// (both outputs' loads go out before either is added up).
 MOE_D void finish_grid(const LutParams& P) {
   const int lim = min(__ldcg(P.rows_hdr), P.A);
   const int64_t total = static_cast<int64_t>(lim) * P.N;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    finish_one(P, static_cast<int>(idx / P.N), static_cast<int>(idx % P.N));
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += 2 * stride) {
+    const int64_t idx2 = idx + stride;
+    float t1 = 0.f, t2 = 0.f;
+    const int64_t o1 = finish_value(P, static_cast<int>(idx / P.N), static_cast<int>(idx % P.N), t1);
+    const int64_t o2 = idx2 < total ? finish_value(P, static_cast<int>(idx2 / P.N), static_cast<int>(idx2 % P.N), t2) : -1;
+    if (o1 >= 0) finish_store(P, o1, t1);
+    if (o2 >= 0) finish_store(P, o2, t2);
+  }
 }
 
 // FC1 + SwiGLU and FC2 of the 2-bit decode layer in one persistent launch:
@@ -553,10 +632,15 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_decode_fused_kernel(const L
   pdl_wait();
   pdl_trigger();
   lut_run(P1, smem);
-  if (!grid_barrier(bar, gridDim.x, wait, P1.dev_err)) return;
+  grid_arrive(bar);
+  // FC2's shared-memory prologue needs only the grouping: it runs while the
+  // other CTAs finish FC1 (FC1 no longer reads this CTA's shared memory)
+  lut_prologue(P2, smem);
+  if (!grid_wait(bar, gridDim.x, wait, P1.dev_err)) return;
   finish_grid(P1);
   if (!grid_barrier(bar, 2 * gridDim.x, wait, P1.dev_err)) return;
-  lut_run(P2, smem);
+  lut_rows(P2, smem);  // after every CTA's FC1 sums have read the row list
+  lut_main(P2, smem);
   if (!grid_barrier(bar, 3 * gridDim.x, wait, P1.dev_err)) return;
   finish_grid(P2);
   // leave the counter at zero for the next launch: the last CTA to arrive
