@@ -48,21 +48,20 @@ constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kBuildWarps = 16;               // warps that build a segment's tables
 constexpr int kBR = 16;                       // weight rows per batch (4 row quads; 32-row batches measured slower)
 constexpr int kSW = 512;                      // K elements per slice
-constexpr int kPrologue = 16640;              // shared bytes below the table window
+constexpr int kPrologue = 18688;              // shared bytes below the table window
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
 // prologue layout: pref [E+1] ints, then the CTA's segment table and the
 // double-buffered activation slice of the table builds
-constexpr int kSegTabOff = 4352;              // int2 [kSegCap]: (permuted row, token row or -1)
-constexpr int kSegCap = 128;
-constexpr int kXBufOff = kSegTabOff + 8 * kSegCap;  // bf16 [2][kSW]
-static_assert(kXBufOff + 2 * kSW * 2 <= kPrologue, "prologue overflow");
-static_assert(4 * (kMaxE + 1) <= kSegTabOff, "prologue overflow");
+constexpr int kXBufOff = 4352;                // bf16 [2][kSW]
+static_assert(4 * (kMaxE + 1) <= kXBufOff, "prologue overflow");
 constexpr int kSlotTabOff = 8192;             // int [E]: weight slot of each expert
 constexpr int kOffTabOff = 12288;             // int [E+1]: offsets[e], the first permuted row of expert e
 static_assert(kXBufOff + 2 * kSW * 2 <= kSlotTabOff && kSlotTabOff + 4 * kMaxE <= kOffTabOff, "prologue overflow");
-static_assert(kOffTabOff + 4 * (kMaxE + 1) <= kPrologue, "prologue overflow");
+constexpr int kSegTabOff = 16640;             // int4 [kSegCap]: (permuted row, token row or -1, weight slot, slice)
+constexpr int kSegCap = 128;
+static_assert(kOffTabOff + 4 * (kMaxE + 1) <= kSegTabOff && kSegTabOff + 16 * kSegCap <= kPrologue, "prologue overflow");
 
 struct LutParams {
   const uint16_t* act;
@@ -294,11 +293,6 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
     }
     return lo;
   };
-  // this lane's code / scale addresses in slice s of expert e
-  auto codes_at = [&](int e, int sl) { return P.codes + slot_tab[e] * mat_codes + sl * slice_codes + lane * 16; };
-  auto scales_at = [&](int e, int sl) {
-    return reinterpret_cast<const uint8_t*>(P.scales + slot_tab[e] * mat_scales + sl * slice_scales) + (lane >> 1) * 8;
-  };
   auto issue = [&](const uint8_t* gc, const uint8_t* gs, int rb) {
     const uint8_t* c0 = gc + static_cast<uint32_t>(rb) * cstep;
     const uint8_t* c2 = c0 + chi;
@@ -322,26 +316,28 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
   const int64_t seg_first = u_beg / NB;
   const int64_t seg_last = (u_end - 1) / NB;
   const int64_t nseg = seg_last - seg_first + 1;
-  int2* seg_tab = reinterpret_cast<int2*>(smem + kSegTabOff);
+  int4* seg_tab = reinterpret_cast<int4*>(smem + kSegTabOff);
   const uint16_t* xbuf = reinterpret_cast<const uint16_t*>(smem + kXBufOff);
-  auto seg_lookup = [&](int64_t sg) -> int2 {  // (p, row; row = -1 if the segment is skipped)
+  // (p, row, weight slot, slice; row = -1 if the segment is skipped)
+  auto seg_lookup = [&](int64_t sg) -> int4 {
     const int ps = static_cast<int>(sg / NSL);
+    const int sl = static_cast<int>(sg - static_cast<int64_t>(ps) * NSL);
     const int ee = expert_of(ps);
     const int pp = off_s[ee] + (ps - pref[ee]);
     if (pp >= P.A) {  // the scratch does not cover this row: report and skip
       set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
-      return make_int2(pp, -1);
+      return make_int4(pp, -1, slot_tab[ee], sl);
     }
     const int rr = P.act_row ? P.act_row[pp] / P.act_row_div : pp;
     if (rr < 0 || rr >= P.act_rows) {
       set_err(P.dev_err, MOE_DEVERR_BAD_ID);
-      return make_int2(pp, -1);
+      return make_int4(pp, -1, slot_tab[ee], sl);
     }
-    return make_int2(pp, rr);
+    return make_int4(pp, rr, slot_tab[ee], sl);
   };
   for (int i = tid; i < nseg && i < kSegCap; i += kLutThreads) seg_tab[i] = seg_lookup(seg_first + i);
   __syncthreads();
-  auto seg_info = [&](int64_t sg) -> int2 {
+  auto seg_info = [&](int64_t sg) -> int4 {
     const int64_t i = sg - seg_first;
     return i < kSegCap ? seg_tab[i] : seg_lookup(sg);
   };
@@ -349,9 +345,9 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
   // cp.async group per call on every thread (empty where nothing is copied)
   auto prefetch_x = [&](int64_t sg) {
     if (sg <= seg_last && tid < kSW / 4) {
-      const int2 si = seg_info(sg);
+      const int4 si = seg_info(sg);
       if (si.y >= 0) {
-        const int sl = static_cast<int>(sg % NSL);
+        const int sl = si.w;
         cp_async8(smem_u32(xbuf) + static_cast<uint32_t>(((sg - seg_first) & 1) * kSW * 2 + 8 * tid),
                   P.act + static_cast<size_t>(si.y) * P.K + sl * kSW + 4 * tid);
       }
@@ -361,17 +357,17 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
   // segment sg: its weight pointers and the end of the CTA's batches in it
   // (batch indices inside a segment are 32-bit: NB <= K/8)
   auto seg_ptrs = [&](int64_t sg, const uint8_t*& gc, const uint8_t*& gs) {
-    const int ps = static_cast<int>(sg / NSL);
-    const int sl = static_cast<int>(sg - static_cast<int64_t>(ps) * NSL);
-    const int ee = expert_of(ps);
-    gc = codes_at(ee, sl);
-    gs = scales_at(ee, sl);
+    const int4 si = seg_info(sg);
+    gc = P.codes + si.z * mat_codes + si.w * slice_codes + lane * 16;
+    gs = reinterpret_cast<const uint8_t*>(P.scales + si.z * mat_scales + si.w * slice_scales) + (lane >> 1) * 8;
   };
   auto seg_hi = [&](int64_t sg) { return sg == seg_last ? static_cast<int>(u_end - sg * NB) : NB; };
   prefetch_x(seg_first);
   prefetch_x(seg_first + 1);
-  // A warp's units: batches warp, warp + 16, ... of each segment (one segment
-  // = one (row, slice) table) of the CTA's range.  The loads of a warp's next
+  // A warp's units: the CTA's units u_beg, u_beg + 1, ... go round-robin to
+  // the 16 warps (unit u to warp (u - u_beg) mod 16), so that every warp
+  // gets the same number of batches within one; in a segment (one (row,
+  // slice) table) a warp takes every 16th batch.  The loads of a warp's next
   // unit go out while the current one is consumed, also across a segment
   // boundary; the row checks (which need global loads) only gate the table
   // build and the stores, never the weight loads.
@@ -391,13 +387,15 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
     const uint8_t* ncodes = gcodes;
     const uint8_t* nscales = gscales;
     int nrb_hi = 0;
+    // this warp's first batch of the next segment
+    const int nrb_first = (warp - static_cast<int>(((seg + 1) * NB - u_beg) & 15)) & 15;
     if (has_next) {
       seg_ptrs(seg + 1, ncodes, nscales);
       nrb_hi = seg_hi(seg + 1);
     }
-    const int2 si = seg_info(seg);
+    const int4 si = seg_info(seg);
     const bool valid = si.y >= 0;
-    const int s = static_cast<int>(seg % NSL);
+    const int s = si.w;
     float* const sbase = P.scratch + (static_cast<size_t>(si.x) * NB * NSL + s) * kBR + (lane >> 1);
     if (!pending && rb < rb_hi) {
       issue(gcodes, gscales, rb);
@@ -443,8 +441,8 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
         const uint8_t* ns = gscales;
         more = same;
         if (!same) {
-          rbn = warp;
-          more = has_next && warp < nrb_hi;
+          rbn = nrb_first;
+          more = has_next && nrb_first < nrb_hi;
           nc = ncodes;
           ns = nscales;
         }
@@ -489,7 +487,7 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
     gcodes = ncodes;
     gscales = nscales;
     rb_hi = nrb_hi;
-    rb = warp;
+    rb = nrb_first;
   }
 }
 
