@@ -14,13 +14,14 @@ layer of weights, as sub-records of the line (``workloads``): prefill_bf16
 (8192 tokens, 2-bit experts on the tensor cores), prefill_fp8 (16384 tokens,
 MXFP4 experts through the FP8 workspace), prefill_fp8_direct (the same
 workload with the MXFP4 experts multiplied as stored, no workspace),
-decode_unfused (the headline decode with FC1 and FC2 as two calls instead of
-one fused launch), decode_mxfp4 (the decode shapes with MXFP4 experts on the
-block-scaled FP8 tensor core, MXFP8 tokens),
-mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache entries)
-and decode_host (the decode workload with every expert in pinned host memory
-and half of them resident on the device: the routed others are copied over
-the CPU-GPU link each step).
+decode_fused (the headline decode as four calls: route, permute, FC1 + FC2
+in one launch, combine; the headline runs the whole step as one launch),
+decode_unfused (the same with FC1 and FC2 as two calls), decode_mxfp4 (the
+decode shapes with MXFP4 experts on the block-scaled FP8 tensor core, MXFP8
+tokens), mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache
+entries) and decode_host (the decode workload with every expert in pinned
+host memory and half of them resident on the device: the routed others are
+copied over the CPU-GPU link each step).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead: whole layer steps of the same workload, its tokens split over one
@@ -173,8 +174,9 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
     hosted = name.endswith("_host")    # 2-bit experts in host memory, half of them resident on the device
     unfused = name.endswith("_unfused")  # the 2-bit decode's FC1 and FC2 as two calls (not one launch)
     as_mx4 = name.endswith("_mxfp4")     # the workload with MXFP4 experts on the block-scaled tensor core
+    four = name.endswith("_fused")       # the 2-bit decode step as four calls (FC1 + FC2 in one launch)
     base = name
-    for suf in ("_direct", "_host", "_unfused", "_mxfp4"):
+    for suf in ("_direct", "_host", "_unfused", "_mxfp4", "_fused"):
         if name.endswith(suf):
             base = name[:-len(suf)]
     w = synth.get_workload(base)
@@ -192,7 +194,7 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
                           resident=range(0, w.E, 2), stage_slots=w.T * w.k)
         elif w.weights == "w2":
             ml = MoELayer("w2", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l), out_fmt=L.FMT_BF16,
-                          fused=not unfused)
+                          fused=not unfused, single_launch=not (four or unfused))
         elif w.weights == "mixed":
             ml = MoELayer("mixed", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l),
                           mx=synth.make_mxfp4_layer(w, n=w.n_hot, seed=0, layer=l),
@@ -341,9 +343,11 @@ def measure(name, args, device, world, layers, *, clocks=None, tokens=None, expe
     traffic = _traffic(name) if tokens is None and experts is None else None
     if decode:
         achieved = graph_bytes / (mm_ms / 1e3) / 1e9
+        single = any(lbl == "w2_layer_single_launch" for lbl, _, _ in graph_ev)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": "expert matmuls (FC1+FC2 launches of the step)",
+                "kernel": ("the single-launch layer kernel (routing, grouping, FC1+FC2, combine)" if single else
+                           "expert matmuls (FC1+FC2 launches of the step)"),
                 "peak_src": f"{peaks['src']} HBM copy rate",
                 "bytes_per_launch": round(graph_bytes / n_mm), "launch_us": round(mm_ms / n_mm * 1e3, 2)}
     else:
@@ -465,6 +469,8 @@ def launches_per_step(ml, T):
     table GEMV with its summing kernel (2-bit decode) or one tensor-core
     kernel, plus two workspace conversions per expert batch on the FP8 path."""
     tc = ml.use_gemm(T)
+    if ml.fmt == "w2" and ml.single_launch and not tc and T * ml.k <= 256 and ml.k <= 16 and ml.E <= 1024:
+        return 1  # the whole step in one launch
     if ml.fmt == "w2" and ml.fused and not tc:  # route, permute, fused FC1+FC2, combine
         return 4
     if ml.fmt == "w2":
@@ -685,9 +691,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct",
-                             "decode_host", "decode_unfused", "decode_mxfp4"])
+                             "decode_host", "decode_unfused", "decode_mxfp4", "decode_fused"])
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--sub", default="decode_unfused,decode_mxfp4,prefill_bf16,prefill_fp8,prefill_fp8_direct,"
+    ap.add_argument("--sub", default="decode_fused,decode_unfused,decode_mxfp4,prefill_bf16,prefill_fp8,prefill_fp8_direct,"
                                      "mixed_decode,decode_host",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,

@@ -29,7 +29,8 @@ EXPORTS = ["moe_version", "moe_last_error_string", "moe_get_error", "moe_set_wai
            "moe_permute", "moe_unpermute", "moe_w2_repack", "moe_dequant_w2", "moe_dequant_mxfp4",
            "mxfp4_to_fp8_ws", "moe_w2_mm_workspace_size", "moe_w2_mm", "moe_w2_mm_noalloc", "moe_mxfp4_mm",
            "moe_combine", "moe_cache_select", "moe_cache_fill", "moe_stage_select", "moe_w2_mm_slots",
-           "moe_w2_decode_fused_workspace_size", "moe_w2_decode_fused"]
+           "moe_w2_decode_fused_workspace_size", "moe_w2_decode_fused", "moe_w2_decode_layer_workspace_size",
+           "moe_w2_decode_layer"]
 W2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -66,6 +67,9 @@ _SIGS = {
     "moe_stage_select": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P]),
     "moe_w2_decode_fused_workspace_size": (_S, [_I, _I, _I]),
     "moe_w2_decode_fused": (_I, [_P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _S, _P, _P]),
+    "moe_w2_decode_layer_workspace_size": (_S, [_I, _I, _I, _I]),
+    "moe_w2_decode_layer": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I,
+                                 _P, _S, _P, _P]),
     "moe_w2_mm_slots": (_I, [_I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _S, _P, _P]),
 }
 
@@ -253,3 +257,17 @@ def moe_w2_decode_fused(x, codes1, scales1, codes2, scales2, offsets, E, H, I, h
     _check(lib().moe_w2_decode_fused(_ptr(x), x.shape[0], _ptr(act_row), act_row_div, _ptr(codes1), _ptr(scales1),
                                      _ptr(codes2), _ptr(scales2), _ptr(offsets), _ptr(expert_slot), E, H, I,
                                      _ptr(h), _ptr(y), y_fmt, _ptr(ws), nbytes, _ptr(dev_err), _stream(stream)))
+
+
+def moe_w2_decode_layer_workspace_size(T, k, H, I) -> int:
+    return int(lib().moe_w2_decode_layer_workspace_size(T, k, H, I))
+
+
+def moe_w2_decode_layer(logits, x, k, codes1, scales1, codes2, scales2, H, I, ids, w, offsets, perm, inv, h, y, out,
+                        out_fmt, ws, dev_err=None, stream=None):
+    T, E = logits.shape
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().moe_w2_decode_layer(_ptr(logits), _ptr(x), T, E, k, _ptr(codes1), _ptr(scales1), _ptr(codes2),
+                                     _ptr(scales2), H, I, _ptr(ids), _ptr(w), _ptr(offsets), _ptr(perm), _ptr(inv),
+                                     _ptr(h), _ptr(y), _ptr(out), out_fmt, _ptr(ws), nbytes, _ptr(dev_err),
+                                     _stream(stream)))

@@ -430,6 +430,91 @@ int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_row, int
   return cuda_status(launch_w2_decode_fused(a1, a2, ws, static_cast<cudaStream_t>(stream)), "moe_w2_decode_fused");
 }
 
+size_t moe_w2_decode_layer_workspace_size(int T, int k, int H, int I) {
+  if (T <= 0 || k <= 0 || static_cast<int64_t>(T) * k > 0x7fffffff) return 0;
+  return moe_w2_decode_fused_workspace_size(T * k, H, I);
+}
+
+int moe_w2_decode_layer(const float* logits, const void* x, int T, int E, int k, const uint8_t* codes1,
+                        const uint16_t* scales1, const uint8_t* codes2, const uint16_t* scales2, int H, int I,
+                        int32_t* ids, float* w, int32_t* offsets, int32_t* perm, int32_t* inv, void* h, void* y,
+                        void* out, int out_fmt, void* ws, size_t ws_bytes, uint32_t* dev_err, void* stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E) return fail(MOE_ERR_ARG, "moe_w2_decode_layer: bad shape");
+  if (!offsets) return fail(MOE_ERR_ARG, "moe_w2_decode_layer: offsets NULL");
+  if (out_fmt != MOE_FMT_BF16 && out_fmt != MOE_FMT_F32) return fail(MOE_ERR_ARG, "moe_w2_decode_layer: out_fmt");
+  if (H <= 0 || I <= 0) return fail(MOE_ERR_ARG, "moe_w2_decode_layer: H / I");
+  if (int r = check_device()) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0)  // no assignments: every group empty, nothing else to write
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s), "moe_w2_decode_layer");
+  if (!logits || !x || !ids || !w || !perm || !inv || !h || !y || !out || !aligned(x, 16) || !aligned(h, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_decode_layer: NULL pointer, or x / h not 16-byte aligned");
+  if (!codes1 || !scales1 || !codes2 || !scales2 || !aligned(codes1, 16) || !aligned(scales1, 16) ||
+      !aligned(codes2, 16) || !aligned(scales2, 16))
+    return fail(MOE_ERR_ARG, "moe_w2_decode_layer: weights NULL or not 16-byte aligned");
+  if (!ws || !aligned(ws, 256) || ws_bytes <= 256) return fail(MOE_ERR_ARG, "moe_w2_decode_layer: workspace");
+  if (!layer_supported(T, E, k))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_w2_decode_layer: T*k above 256 or k above 16");
+  const int A = T * k;
+  MMArgs a1{}, a2{};
+  for (MMArgs* a : {&a1, &a2}) {
+    a->act_fmt = MOE_FMT_BF16;
+    a->mode = MOE_MODE_GEMV;
+    a->wkind = kW2;
+    a->offsets = nullptr;  // the grouping's, in the kernel's shared memory
+    a->expert_begin = 0;
+    a->expert_end = E;
+    a->E = E;
+    a->dev_err = dev_err;
+    a->wait = wait_limit();
+  }
+  a1.stage = MOE_STAGE_FC1_SWIGLU;
+  a1.act = x;
+  a1.act_rows = T;
+  a1.act_row = nullptr;  // the grouping's perm, in shared memory
+  a1.act_row_div = k;
+  a1.wq = codes1;
+  a1.wscale = scales1;
+  a1.N = I;
+  a1.K = H;
+  a1.out = h;
+  a1.out_fmt = MOE_FMT_BF16;
+  a2.stage = MOE_STAGE_FC2;
+  a2.act = h;
+  a2.act_rows = 0x7fffffff;  // h rows are the permuted rows themselves
+  a2.act_row = nullptr;
+  a2.act_row_div = 1;
+  a2.wq = codes2;
+  a2.wscale = scales2;
+  a2.N = H;
+  a2.K = I;
+  a2.out = y;
+  a2.out_fmt = MOE_FMT_BF16;
+  if (!lut_supported(a1) || !lut_supported(a2))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_w2_decode_layer: H and I must be multiples of 512");
+  const size_t lws = ws_bytes - 256;
+  for (MMArgs* a : {&a1, &a2}) {
+    a->ws = static_cast<uint8_t*>(ws) + 256;
+    a->ws_bytes = lws;
+    a->ws_rows = lut_workspace_rows(a->stage, lws, a->N, a->K);
+    if (a->ws_rows < A) return fail(MOE_ERR_WS_SMALL, "moe_w2_decode_layer: workspace below T*k rows");
+  }
+  LayerArgs la;
+  la.logits = logits;
+  la.T = T;
+  la.E = E;
+  la.k = k;
+  la.ids = ids;
+  la.w = w;
+  la.offsets = offsets;
+  la.perm = perm;
+  la.inv = inv;
+  la.y = y;
+  la.out = out;
+  la.out_fmt = out_fmt;
+  return cuda_status(launch_w2_decode_layer(la, a1, a2, ws, s), "moe_w2_decode_layer");
+}
+
 int moe_mxfp4_mm(int stage, int mode, const void* act, int act_fmt, const uint8_t* act_scale, int act_rows,
                  const int32_t* act_row, int act_row_div, const uint8_t* e2m1, const uint8_t* e8m0, const uint8_t* fp8_ws,
                  const int32_t* ws_slot_of_expert, const int32_t* offsets, const int32_t* expert_slot,

@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 
@@ -48,7 +49,7 @@ constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kBuildWarps = 16;               // warps that build a segment's tables
 constexpr int kBR = 16;                       // weight rows per batch (4 row quads; 32-row batches measured slower)
 constexpr int kSW = 512;                      // K elements per slice
-constexpr int kPrologue = 18688;              // shared bytes below the table window
+constexpr int kPrologue = 26896;              // shared bytes below the table window
 constexpr int kTableBytes = 2 * 65536;        // [j>>1][b][j&1][32 lanes] fp32
 constexpr int kLutSmem = kPrologue + 65536 + kTableBytes;
 constexpr int kMaxE = 1024;
@@ -61,7 +62,15 @@ constexpr int kOffTabOff = 12288;             // int [E+1]: offsets[e], the firs
 static_assert(kXBufOff + 2 * kSW * 2 <= kSlotTabOff && kSlotTabOff + 4 * kMaxE <= kOffTabOff, "prologue overflow");
 constexpr int kSegTabOff = 16640;             // int4 [kSegCap]: (permuted row, token row or -1, weight slot, slice)
 constexpr int kSegCap = 128;
-static_assert(kOffTabOff + 4 * (kMaxE + 1) <= kSegTabOff && kSegTabOff + 16 * kSegCap <= kPrologue, "prologue overflow");
+static_assert(kOffTabOff + 4 * (kMaxE + 1) <= kSegTabOff, "prologue overflow");
+// the single-launch decode layer's routing and grouping (A = T*k <= kLayerA)
+constexpr int kLayerA = 256;
+constexpr int kLayerIds = 18688;              // int [kLayerA]: ids
+constexpr int kLayerW = kLayerIds + 4 * kLayerA;      // float [kLayerA]: w
+constexpr int kLayerPerm = kLayerW + 4 * kLayerA;     // int [kLayerA]: perm
+constexpr int kLayerInv = kLayerPerm + 4 * kLayerA;   // int [kLayerA]: inv
+constexpr int kLayerOffs = kLayerInv + 4 * kLayerA;   // int [kMaxE + 1]: offsets
+static_assert(kSegTabOff + 16 * kSegCap <= kLayerIds && kLayerOffs + 4 * (kMaxE + 1) <= kPrologue, "prologue overflow");
 
 struct LutParams {
   const uint16_t* act;
@@ -75,6 +84,7 @@ struct LutParams {
   const int32_t* wslot;     // expert -> slot of the weight arrays (NULL: slot = expert)
   int slot_lo, slot_hi;     // with wslot: only experts whose slot lies in [slot_lo, slot_hi)
   int split;                // 1: only groups of fewer than kSplitRows rows
+  int layer;                // single-launch layer: bit 0 offsets, bit 1 act_row from its shared-memory arrays
   const int32_t* offsets;
   int E, N, K, R;           // R = weight rows per expert
   int NSL;                  // K slices
@@ -176,6 +186,7 @@ MOE_D void lut_prologue(const LutParams& P, uint8_t* smem) {
   int* pref = reinterpret_cast<int*>(smem);  // [E+1] selected permuted rows before expert e
   int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);  // [E] weight slot of expert e
   int* off_s = reinterpret_cast<int*>(smem + kOffTabOff);      // [E+1] offsets
+  const int32_t* offsets = (P.layer & 1) ? reinterpret_cast<const int32_t*>(smem + kLayerOffs) : P.offsets;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- selected rows per expert, exclusive prefix: every thread loads the
@@ -187,7 +198,7 @@ MOE_D void lut_prologue(const LutParams& P, uint8_t* smem) {
     for (int h = 0; h < 2; ++h) {
       const int e = 2 * tid + h;
       if (e < P.E) {
-        const int lo = P.offsets[e], hi = P.offsets[e + 1];
+        const int lo = offsets[e], hi = offsets[e + 1];
         const int c = hi - lo;
         const int sm = P.select ? P.select_map[e] : 0;
         const int ws = P.wslot ? P.wslot[e] : e;
@@ -226,6 +237,7 @@ MOE_D void lut_prologue(const LutParams& P, uint8_t* smem) {
 MOE_D void lut_rows(const LutParams& P, const uint8_t* smem) {
   const int* pref = reinterpret_cast<const int*>(smem);
   const int* off_s = reinterpret_cast<const int*>(smem + kOffTabOff);
+  const int32_t* act_row = (P.layer & 2) ? reinterpret_cast<const int32_t*>(smem + kLayerPerm) : P.act_row;
   const int tid = threadIdx.x;
   {
     const int nsel = pref[P.E];
@@ -240,7 +252,7 @@ MOE_D void lut_rows(const LutParams& P, const uint8_t* smem) {
       const int p = off_s[lo] + (i - pref[lo]);
       bool ok = p < P.A;
       if (ok) {
-        const int row = P.act_row ? P.act_row[p] / P.act_row_div : p;
+        const int row = act_row ? act_row[p] / P.act_row_div : p;
         ok = row >= 0 && row < P.act_rows;
       }
       P.rows_hdr[1 + i] = ok ? p : -1;
@@ -254,6 +266,7 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
   int* pref = reinterpret_cast<int*>(smem);
   int* slot_tab = reinterpret_cast<int*>(smem + kSlotTabOff);
   const int* off_s = reinterpret_cast<const int*>(smem + kOffTabOff);
+  const int32_t* act_row = (P.layer & 2) ? reinterpret_cast<const int32_t*>(smem + kLayerPerm) : P.act_row;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
   const uint32_t table_win = (base + kPrologue + 65535u) & ~65535u;
@@ -328,7 +341,7 @@ MOE_D void lut_main(const LutParams& P, uint8_t* smem) {
       set_err(P.dev_err, MOE_DEVERR_OVERFLOW);
       return make_int4(pp, -1, slot_tab[ee], sl);
     }
-    const int rr = P.act_row ? P.act_row[pp] / P.act_row_div : pp;
+    const int rr = act_row ? act_row[pp] / P.act_row_div : pp;
     if (rr < 0 || rr >= P.act_rows) {
       set_err(P.dev_err, MOE_DEVERR_BAD_ID);
       return make_int4(pp, -1, slot_tab[ee], sl);
@@ -646,6 +659,155 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_decode_fused_kernel(const L
   if (threadIdx.x == 0 && atomicAdd(bar, 1u) == 4 * gridDim.x - 1) atomicExch(bar, 0u);
 }
 
+// ------------------------------------------------------------------ one launch for the decode layer
+constexpr int kLayerK = 16;  // experts per token at most
+
+struct LayerParams {
+  const float* logits;  // [T][E]
+  int T, E, k;
+  int32_t* ids;         // [T][k] out
+  float* w;             // [T][k] out
+  int32_t* offsets;     // [E+1] out
+  int32_t* perm;        // [A] out
+  int32_t* inv;         // [A] out
+  uint16_t* y;          // bf16 [A][H] out
+  void* out;            // [T][H] out, out_fmt
+  int out_fmt;
+  uint32_t* dev_err;
+};
+
+// Routing and grouping of the whole step by one CTA into its shared memory
+// (every CTA computes the same; CTA 0 also writes them out): route_token per
+// token (the routing kernel's arithmetic), then moe_permute's stable
+// counting sort (rows of one expert in increasing assignment order).
+template <int NPL>
+MOE_D void layer_route(const LayerParams& L, uint8_t* smem) {
+  int* ids_s = reinterpret_cast<int*>(smem + kLayerIds);
+  float* w_s = reinterpret_cast<float*>(smem + kLayerW);
+  int* perm_s = reinterpret_cast<int*>(smem + kLayerPerm);
+  int* inv_s = reinterpret_cast<int*>(smem + kLayerInv);
+  int* offs_s = reinterpret_cast<int*>(smem + kLayerOffs);
+  const uint32_t base = smem_u32(smem);
+  int* cnt = reinterpret_cast<int*>(smem + (((base + kPrologue + 65535u) & ~65535u) - base));  // the table window, free here
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int A = L.T * L.k, E = L.E;
+  bool nan = false;
+  for (int t = warp; t < L.T; t += kLutWarps) {
+    int id;
+    float wt;
+    nan |= route_token<NPL>(L.logits + static_cast<size_t>(t) * E, E, L.k, lane, id, wt);
+    if (lane < L.k) {
+      ids_s[t * L.k + lane] = id;
+      w_s[t * L.k + lane] = wt;
+    }
+  }
+  if (nan && lane == 0 && blockIdx.x == 0) set_err(L.dev_err, MOE_DEVERR_NAN_LOGIT);
+  for (int e = tid; e < E; e += kLutThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int a = tid; a < A; a += kLutThreads) atomicAdd(&cnt[ids_s[a]], 1);
+  __syncthreads();
+  {  // offsets: exclusive scan of the counts, experts 2t and 2t+1 per thread
+    __shared__ int lay_wsum[kLutWarps];
+    const int n0 = 2 * tid < E ? cnt[2 * tid] : 0;
+    const int n1 = 2 * tid + 1 < E ? cnt[2 * tid + 1] : 0;
+    int incl = n0 + n1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) lay_wsum[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += lay_wsum[w2];
+    const int excl = before + incl - n0 - n1;
+    if (2 * tid <= E) offs_s[2 * tid] = excl;
+    if (2 * tid + 1 <= E) offs_s[2 * tid + 1] = excl + n0;
+    if (tid == kLutThreads - 1) offs_s[E] = excl + n0 + n1;  // the total (also for E = 1024)
+  }
+  __syncthreads();
+  for (int a = tid; a < A; a += kLutThreads) {  // stable: rank among the expert's earlier assignments
+    const int e = ids_s[a];
+    int r = 0;
+    for (int b2 = 0; b2 < a; ++b2) r += ids_s[b2] == e;
+    const int pos = offs_s[e] + r;
+    perm_s[pos] = a;
+    inv_s[a] = pos;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int a = tid; a < A; a += kLutThreads) {
+      L.ids[a] = ids_s[a];
+      L.w[a] = w_s[a];
+      L.perm[a] = perm_s[a];
+      L.inv[a] = inv_s[a];
+    }
+    for (int e = tid; e <= E; e += kLutThreads) L.offsets[e] = offs_s[e];
+  }
+}
+
+// FC2's summing step and the weighted combine in one pass: output n of token
+// t sums the slices of its k rows (y, rounded to bf16 and stored) and adds
+// them up in slot order as moe_combine does (out = sum_j w_j * y_j, fmaf from
+// zero).  Every row is one token's slot, so each y element is written once.
+MOE_D void layer_finish(const LutParams& P, const LayerParams& L, const uint8_t* smem) {
+  const float* w_s = reinterpret_cast<const float*>(smem + kLayerW);
+  const int* inv_s = reinterpret_cast<const int*>(smem + kLayerInv);
+  const int H = P.N, NSL = P.NSL, NB = P.NB, k = L.k;
+  const int64_t total = static_cast<int64_t>(L.T) * H;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / H), n = static_cast<int>(idx % H);
+    float v[kLayerK];
+#pragma unroll
+    for (int j = 0; j < kLayerK; ++j) {  // every slot's loads before the first store
+      v[j] = 0.f;
+      if (j < k) {
+        const int p = inv_s[t * k + j];
+        v[j] = slice_total(P.scratch + (static_cast<size_t>(p) * NB + (n >> 4)) * NSL * kBR + (n & 15), NSL);
+      }
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kLayerK; ++j) {
+      if (j < k) {
+        const int p = inv_s[t * k + j];
+        const uint16_t yb = f32_to_bf16_rne(v[j]);
+        L.y[static_cast<size_t>(p) * H + n] = yb;
+        acc = fmaf(w_s[t * k + j], __uint_as_float(static_cast<uint32_t>(yb) << 16), acc);
+      }
+    }
+    if (L.out_fmt == MOE_FMT_F32) static_cast<float*>(L.out)[static_cast<size_t>(t) * H + n] = acc;
+    else static_cast<uint16_t*>(L.out)[static_cast<size_t>(t) * H + n] = f32_to_bf16_rne(acc);
+  }
+}
+
+// The whole 2-bit decode layer in one persistent launch: routing and
+// grouping (every CTA, shared memory), FC1 tables, barrier, FC1 sums -> h,
+// barrier, FC2 tables, barrier, FC2 sums -> y with the combine -> out.  Same
+// arithmetic and order as moe_route, moe_permute, moe_w2_decode_fused and
+// moe_combine.
+template <int NPL>
+__global__ void __launch_bounds__(kLutThreads, 1) w2_decode_layer_kernel(const LayerParams L, const LutParams P1,
+                                                                        const LutParams P2, unsigned int* bar,
+                                                                        long long wait) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
+  layer_route<NPL>(L, smem);
+  lut_run(P1, smem);
+  grid_arrive(bar);
+  lut_prologue(P2, smem);
+  if (!grid_wait(bar, gridDim.x, wait, P1.dev_err)) return;
+  finish_grid(P1);
+  if (!grid_barrier(bar, 2 * gridDim.x, wait, P1.dev_err)) return;
+  lut_rows(P2, smem);
+  lut_main(P2, smem);
+  if (!grid_barrier(bar, 3 * gridDim.x, wait, P1.dev_err)) return;
+  layer_finish(P2, L, smem);
+  if (threadIdx.x == 0 && atomicAdd(bar, 1u) == 4 * gridDim.x - 1) atomicExch(bar, 0u);
+}
+
 }  // namespace
 
 // Scratch of the table GEMV: a row header (the selected-row count, then the
@@ -700,6 +862,7 @@ static LutParams lut_params(const MMArgs& a, void* ws) {
   P.slot_lo = a.slot_lo;
   P.slot_hi = a.slot_hi;
   P.split = a.split;
+  P.layer = 0;
   P.offsets = a.offsets;
   P.E = a.E;
   P.N = a.N;
@@ -750,6 +913,50 @@ cudaError_t launch_w2_decode_fused(const MMArgs& fc1, const MMArgs& fc2, void* w
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, w2_decode_fused_kernel, P1, P2, bar, fc1.wait);
+}
+
+bool layer_supported(int T, int E, int k) { return T * k <= kLayerA && k <= kLayerK && k <= 32 && E <= kMaxE; }
+
+cudaError_t launch_w2_decode_layer(const LayerArgs& la, const MMArgs& fc1, const MMArgs& fc2, void* ws,
+                                   cudaStream_t s) {
+  unsigned int* bar = static_cast<unsigned int*>(ws);
+  void* lws = static_cast<uint8_t*>(ws) + 256;
+  LutParams P1 = lut_params(fc1, lws), P2 = lut_params(fc2, lws);
+  P1.layer = 3;  // FC1 reads token rows through the grouping's perm
+  P2.layer = 1;
+  LayerParams L;
+  L.logits = la.logits;
+  L.T = la.T;
+  L.E = la.E;
+  L.k = la.k;
+  L.ids = la.ids;
+  L.w = la.w;
+  L.offsets = la.offsets;
+  L.perm = la.perm;
+  L.inv = la.inv;
+  L.y = static_cast<uint16_t*>(la.y);
+  L.out = la.out;
+  L.out_fmt = la.out_fmt;
+  L.dev_err = fc1.dev_err;
+  auto kern = la.E <= 128 ? w2_decode_layer_kernel<4>
+              : la.E <= 256 ? w2_decode_layer_kernel<8>
+              : la.E <= 512 ? w2_decode_layer_kernel<16>
+                            : w2_decode_layer_kernel<32>;
+  cudaError_t e = set_smem_limit(kern, kLutSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_info().sms);
+  cfg.blockDim = dim3(kLutThreads);
+  cfg.dynamicSmemBytes = kLutSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, L, P1, P2, bar, fc1.wait);
 }
 
 }  // namespace moe

@@ -367,6 +367,35 @@ MOE_API int moe_w2_decode_fused(const void* x, int act_rows, const int32_t* act_
                         int E, int H, int I, void* h, void* y, int y_fmt, void* ws, size_t ws_bytes,
                         uint32_t* dev_err, void* stream);
 
+/* One whole 2-bit decode layer step in ONE kernel launch (vLLM-Moet README,
+ * "MoET hybrid": the decode MoE inside a captured CUDA graph; here routing,
+ * grouping, both expert matmuls and the combine are one persistent
+ * cooperative kernel).  Computes exactly
+ *   moe_route(logits -> ids, w), moe_permute(ids -> offsets, perm, inv; no
+ *   gather), moe_w2_decode_fused(x via perm / k -> h, y bf16),
+ *   moe_combine(y, w, inv -> out)
+ * with the same arithmetic and order: every output is bit-identical to
+ * those four calls.  Every CTA routes and groups the whole step in its own
+ * shared memory; the combine runs inside FC2's summing step.
+ *   logits   float [T][E]; x bf16 [T][H]
+ *   codes1/scales1, codes2/scales2  w2l weights of W1 [E][2I][H/4] and W2
+ *   ids int32 [T][k], w float [T][k], offsets int32 [E+1], perm / inv int32
+ *            [T*k], h bf16 [T*k][I], y bf16 [T*k][H]: out, as the four calls
+ *            write them; out [T][H] in out_fmt (BF16 or F32)
+ *   ws       >= moe_w2_decode_layer_workspace_size(T, k, H, I) bytes, the
+ *            workspace of moe_w2_decode_fused for T*k rows (same barrier
+ *            counter rule: zero before the first call, left at zero)
+ * Limits: T*k <= 256, k <= 16, E <= 1024, H and I multiples of 512, else
+ * MOE_ERR_UNSUPPORTED (T*k, k) or MOE_ERR_ARG (E, k > E).  T = 0 zeroes
+ * offsets and launches nothing.  A NaN logit sets NAN_LOGIT, as moe_route
+ * does.  Grid barriers are bounded waits (MOE_DEVERR_TIMEOUT). */
+MOE_API size_t moe_w2_decode_layer_workspace_size(int T, int k, int H, int I);
+MOE_API int moe_w2_decode_layer(const float* logits, const void* x, int T, int E, int k,
+                        const uint8_t* codes1, const uint16_t* scales1, const uint8_t* codes2,
+                        const uint16_t* scales2, int H, int I, int32_t* ids, float* w, int32_t* offsets,
+                        int32_t* perm, int32_t* inv, void* h, void* y, void* out, int out_fmt, void* ws,
+                        size_t ws_bytes, uint32_t* dev_err, void* stream);
+
 /* As moe_w2_mm for MXFP4 weights (blog "这个项目我们能学到什么?": the FP4
  * delta cache of hot experts; OCP MX E2M1 + E8M0), or for FP8 workspace
  * weights ("国产GPU完成MoE大模型Day-0适配" §四: the matmul reads the reused FP8

@@ -25,7 +25,8 @@ def test_fused_decode_bit_identical_to_two_calls(name):
         w = synth.get_workload("prefill_bf16").replace(T=64)
     raw = synth.make_w2_layer(w)
     two = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, fused=False)
-    one = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, fused=True)
+    one = MoELayer("w2", w.E, w.H, w.I, w.k, w2=raw, out_fmt=L.FMT_F32, mode=L.MODE_GEMV, fused=True,
+                   single_launch=False)
     for bi in range(2):
         x = synth.make_x(w, 0, tid_offset=bi)
         lg = synth.make_logits(w, 0, x_bits=x, tid_offset=bi)
@@ -48,7 +49,7 @@ def test_fused_decode_repeats_and_captures():
     captured graph give the same bits."""
     w = synth.get_workload("decode")
     ml = MoELayer("w2", w.E, w.H, w.I, w.k, w2=synth.make_w2_layer(w), out_fmt=L.FMT_BF16, mode=L.MODE_GEMV,
-                  fused=True)
+                  fused=True, single_launch=False)
     x = dev(synth.make_x(w).view(np.int16))
     lg = dev(synth.make_logits(w))
     b = ml.buffers(w.T)
