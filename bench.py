@@ -124,22 +124,24 @@ class ClockSampler:
 # full-size workloads summarised under profiles/; reported only while the
 # kernels' sources are the ones captured (sha256 over the files named).
 _TRAFFIC = {
-    "decode": {"bytes": 502.38e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
-              "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
-    "decode_unfused": {"bytes": 256.51e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
-                      "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
+    "decode": {"bytes": 502.01e6, "src": ['gemv_lut.cu', 'route_common.cuh', 'layer_args.cuh', 'common.cuh', 'internal.cuh'],
+              "src_sha256": "f92cc99f3185016de95fd124607792099b63d927df7f80a21004c711b6821197"},
+    "decode_unfused": {"bytes": 256.41e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
+                      "src_sha256": "de98d0ad9b8c3dd7a2b4ce048d86a28525492fcf9d4a9699e9c5ef260829d1ad"},
     "decode_mxfp4": {"bytes": 401.82e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                     "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
-    "mixed_decode": {"bytes": 630.41e6, "src": ['gemv_lut.cu', 'gemm_tmem.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
-                    "src_sha256": "4f7fa1efceafe52ea65964c2381153348ac85af55f506bca3629c11bc93039b3"},
+    "mixed_decode": {"bytes": 629.99e6, "src": ['gemv_lut.cu', 'gemm_tmem.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
+                    "src_sha256": "350ed422ca5fe44defdf4982b1fe492f8b6c200e57003035770a87365985a35b"},
     "prefill_bf16": {"bytes": 2301.51e6, "src": ['gemm_tmem.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                     "src_sha256": "06ffb5709f2843c3905f50859122a3abba95f5bc1a61cc2fd71750663f4e3906"},
     "prefill_fp8_direct": {"bytes": 4672.7e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                           "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
     "prefill_fp8": {"bytes": 1820.26e6, "src": ['gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
                    "src_sha256": "1a9c10657aee666beceae0f930ecc4cd471d2af6ee8fecee9b83a0d9316c0f85"},
-    "decode_host": {"bytes": 246.31e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
-                   "src_sha256": "57a4898e90aed720c5e27ae98cee09a0bb76aa1fe560cb15f5d9d9f2dbcf5bce"},
+    "decode_host": {"bytes": 246.23e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
+                   "src_sha256": "de98d0ad9b8c3dd7a2b4ce048d86a28525492fcf9d4a9699e9c5ef260829d1ad"},
+    "decode_fused": {"bytes": 501.93e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
+                    "src_sha256": "de98d0ad9b8c3dd7a2b4ce048d86a28525492fcf9d4a9699e9c5ef260829d1ad"},
 }
 
 

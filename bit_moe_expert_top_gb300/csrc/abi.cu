@@ -10,6 +10,7 @@
 
 #include "../../include/moe.h"
 #include "internal.cuh"
+#include "layer_args.cuh"
 
 namespace moe {
 

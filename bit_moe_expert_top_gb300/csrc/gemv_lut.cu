@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "layer_args.cuh"
 #include "route_common.cuh"
 
 namespace moe {

@@ -130,23 +130,6 @@ cudaError_t launch_lut_gemv(const MMArgs& a, void* ws, cudaStream_t s);
 // FC1 and FC2 of the table GEMV in one cooperative launch; ws = 256 bytes of
 // barrier counter, then the table GEMV's workspace (shared by both stages)
 cudaError_t launch_w2_decode_fused(const MMArgs& fc1, const MMArgs& fc2, void* ws, cudaStream_t s);
-// The single-launch decode layer (gemv_lut.cu): routing and grouping outputs
-// and the combine's, around the fused FC1 + FC2 of launch_w2_decode_fused.
-struct LayerArgs {
-  const float* logits;
-  int T, E, k;
-  int32_t* ids;
-  float* w;
-  int32_t* offsets;
-  int32_t* perm;
-  int32_t* inv;
-  void* y;
-  void* out;
-  int out_fmt;
-};
-bool layer_supported(int T, int E, int k);
-cudaError_t launch_w2_decode_layer(const LayerArgs& la, const MMArgs& fc1, const MMArgs& fc2, void* ws,
-                                   cudaStream_t s);
 bool gemm_supported(const MMArgs& a);
 cudaError_t launch_gemm_tc(const MMArgs& a, int rows_total, cudaStream_t s);
 // tensor-core grouped matmul with the dequantised weights in TMEM (gemm_tmem.cu)
