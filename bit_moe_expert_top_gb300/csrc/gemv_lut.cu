@@ -783,6 +783,31 @@ MOE_D void layer_finish(const LutParams& P, const LayerParams& L, const uint8_t*
   }
 }
 
+// FC1's summing step of the single-launch layer over the whole grid: every
+// row is valid and selected row i is permuted row i (all experts, all
+// rows), so no row list is read; two outputs per thread and round.
+MOE_D void finish_grid_all(const LutParams& P, int A) {
+  const int64_t total = static_cast<int64_t>(A) * P.N;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += 2 * stride) {
+    const int64_t idx2 = idx + stride;
+    const int p1 = static_cast<int>(idx / P.N), n1 = static_cast<int>(idx % P.N);
+    const float* s1 = P.scratch + (static_cast<size_t>(p1) * P.NB + (n1 >> 3)) * P.NSL * kBR + (n1 & 7);
+    const float g1 = slice_total(s1, P.NSL), u1 = slice_total(s1 + 8, P.NSL);
+    float g2 = 0.f, u2 = 0.f;
+    int p2 = 0, n2 = 0;
+    if (idx2 < total) {
+      p2 = static_cast<int>(idx2 / P.N);
+      n2 = static_cast<int>(idx2 % P.N);
+      const float* s2 = P.scratch + (static_cast<size_t>(p2) * P.NB + (n2 >> 3)) * P.NSL * kBR + (n2 & 7);
+      g2 = slice_total(s2, P.NSL);
+      u2 = slice_total(s2 + 8, P.NSL);
+    }
+    finish_store(P, static_cast<int64_t>(p1) * P.N + n1, silu_f32(g1) * u1);
+    if (idx2 < total) finish_store(P, static_cast<int64_t>(p2) * P.N + n2, silu_f32(g2) * u2);
+  }
+}
+
 // The whole 2-bit decode layer in one persistent launch: routing and
 // grouping (every CTA, shared memory), FC1 tables, barrier, FC1 sums -> h,
 // barrier, FC2 tables, barrier, FC2 sums -> y with the combine -> out.  Same
@@ -796,13 +821,13 @@ __global__ void __launch_bounds__(kLutThreads, 1) w2_decode_layer_kernel(const L
   pdl_wait();
   pdl_trigger();
   layer_route<NPL>(L, smem);
-  lut_run(P1, smem);
+  lut_prologue(P1, smem);  // (no row list: the summing steps below index rows directly)
+  lut_main(P1, smem);
   grid_arrive(bar);
   lut_prologue(P2, smem);
   if (!grid_wait(bar, gridDim.x, wait, P1.dev_err)) return;
-  finish_grid(P1);
+  finish_grid_all(P1, L.T * L.k);
   if (!grid_barrier(bar, 2 * gridDim.x, wait, P1.dev_err)) return;
-  lut_rows(P2, smem);
   lut_main(P2, smem);
   if (!grid_barrier(bar, 3 * gridDim.x, wait, P1.dev_err)) return;
   layer_finish(P2, L, smem);
