@@ -22,6 +22,8 @@ CASES = {
     "odd k": dict(E=24, H=1024, I=512, k=3, T=13),
     "one token": dict(E=8, H=512, I=512, k=2, T=1),
     "largest": dict(E=1024, H=512, I=512, k=16, T=16),
+    "E 129..256": dict(E=200, H=512, I=1024, k=6, T=10),
+    "E 257..512": dict(E=257, H=512, I=512, k=5, T=7),
 }
 
 
