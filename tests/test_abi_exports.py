@@ -95,3 +95,28 @@ def test_split_mode_constant_matches_header(lib_path):
     for name, val in (("AUTO", L.MODE_AUTO), ("GEMV", L.MODE_GEMV), ("GEMM", L.MODE_GEMM), ("SPLIT", L.MODE_SPLIT)):
         m = re.search(rf"#define MOE_MODE_{name} (\d+)", src)
         assert m and int(m.group(1)) == val
+
+
+def test_decode_layer_host_rules(lib_path):
+    """moe_w2_decode_layer (host-side checks, no launch): its workspace is the
+    fused launch's for T*k rows, zero for no rows or a K the table GEMV does
+    not take; shapes it cannot take are refused before any device call."""
+    from bit_moe_expert_top_gb300 import _lib as L
+    lib = L.lib()
+    assert lib.moe_w2_decode_layer_workspace_size(8, 8, 4096, 2048) == lib.moe_w2_decode_fused_workspace_size(64, 4096, 2048) > 0
+    assert lib.moe_w2_decode_layer_workspace_size(0, 8, 4096, 2048) == 0
+    assert lib.moe_w2_decode_layer_workspace_size(8, 8, 640, 2048) == 0
+    null = [None] * 24
+
+    def call(T, E, k, out_fmt=L.FMT_BF16, offsets=None):
+        a = list(null)
+        a[2], a[3], a[4], a[9], a[10], a[13], a[19] = T, E, k, 512, 512, offsets, out_fmt
+        a[21] = 0
+        return lib.moe_w2_decode_layer(*a)
+
+    assert call(-1, 8, 2) == L.MOE_ERR_ARG          # negative token count
+    assert call(4, 8, 9) == L.MOE_ERR_ARG           # k > E
+    assert call(4, 1025, 2) == L.MOE_ERR_ARG        # E above 1024
+    assert call(4, 8, 2) == L.MOE_ERR_ARG           # offsets NULL
+    # output format (checked before any pointer is read: the offsets address is never used)
+    assert call(4, 8, 2, out_fmt=L.FMT_MXFP8, offsets=256) == L.MOE_ERR_ARG
