@@ -25,6 +25,10 @@ Precision profiles (where the definition rounds):
     §四): weights are the E4M3 workspace values; x is MXFP8-quantised per
     token in blocks of 32 along H; g, u fp32; h = fp32(silu(g)*u) is
     MXFP8-quantised along I; y = RNE_bf16(W2 h_q); out as above.
+  * per expert (``expert_profile``): each expert's rows follow the profile
+    named for that expert, e.g. the delta cache's MXFP4 experts in "fp8"
+    (FP8 as the compute precision of MXFP4 experts, §四) and the 2-bit
+    experts in "bf16"; the combine is unchanged.
 
 Each dot product is accumulated in fp64 and rounded once to fp32.
 """
@@ -154,14 +158,16 @@ ExpertWeights = Callable[[int], Tuple[np.ndarray, np.ndarray]]
 
 
 def layer(x_bits: np.ndarray, logits: np.ndarray, k: int, expert_weights: ExpertWeights,
-          profile: str = "bf16", tokens: Optional[Iterable[int]] = None) -> Dict[str, np.ndarray]:
+          profile: str = "bf16", tokens: Optional[Iterable[int]] = None,
+          expert_profile: Optional[Callable[[int], str]] = None) -> Dict[str, np.ndarray]:
     """The routed-expert FFN for the tokens ``tokens`` (default all).
 
     ``expert_weights(e)`` returns the dequantised (W1 [2I,H], W2 [H,I]) float64
     values of expert e in the profile's weight format.  Routing runs over all
     tokens; the FFN and combine only over the requested ones.  Each expert's
-    weights are fetched once.  Returns dict(ids, w, y [n,k,H], out fp32 [n,H],
-    tokens)."""
+    weights are fetched once.  ``expert_profile(e)``, if given, names the
+    profile of expert e (overriding ``profile``).  Returns dict(ids, w,
+    y [n,k,H], out fp32 [n,H], tokens)."""
     ids, w, _ = route(logits, k)
     T = ids.shape[0]
     tok = np.arange(T) if tokens is None else np.asarray(list(tokens), dtype=np.int64)
@@ -169,10 +175,11 @@ def layer(x_bits: np.ndarray, logits: np.ndarray, k: int, expert_weights: Expert
     sub_ids = ids[tok]
     H = x.shape[1]
     y = np.zeros((tok.size, k, H))
-    ffn = {"bf16": expert_ffn_bf16, "fp8": expert_ffn_fp8}[profile]
+    ffns = {"bf16": expert_ffn_bf16, "fp8": expert_ffn_fp8}
     for e in np.unique(sub_ids):
         rows, slots = np.nonzero(sub_ids == e)
         W1, W2 = expert_weights(int(e))
+        ffn = ffns[expert_profile(int(e)) if expert_profile else profile]
         y[rows, slots] = ffn(x[rows], W1, W2)
     out = combine(y, w[tok])
     return dict(ids=ids, w=w, y=y, out=out, tokens=tok)

@@ -247,3 +247,29 @@ def test_mixed_accessor_routes_hot_experts_to_mxfp4():
             assert np.array_equal(W1, C.decode_mxfp4(mx[0][slot[e]], mx[1][slot[e]]))
         else:
             assert np.array_equal(W1, C.decode_w2(raw[0][e], raw[1][e]))
+
+
+def test_per_expert_profile_selects_each_experts_rows():
+    """expert_profile: every assignment's y is the one its expert's profile
+    gives (fp8 for the delta-cache experts, bf16 for the 2-bit ones), taken
+    from full runs in each single profile, and the output is their combine."""
+    w = synth.get_workload("tiny").replace(E=6, k=3, T=10, n_hot=2, weights="mixed", logits="zipf")
+    slot = synth.hot_experts(w)
+    raw = synth.make_w2_layer(w)
+    mx = synth.make_mxfp4_layer(w, n=2)
+    get = M.mixed_expert_weights(M.w2_expert_weights(*raw), M.mxfp4_expert_weights(*mx), slot)
+    x = synth.make_x(w)
+    lg = synth.make_logits(w, x_bits=x)
+    mixed = M.layer(x, lg, w.k, get, expert_profile=lambda e: "fp8" if slot[e] >= 0 else "bf16")
+    bf = M.layer(x, lg, w.k, get, profile="bf16")
+    fp = M.layer(x, lg, w.k, get, profile="fp8")
+    cached = slot[mixed["ids"]] >= 0
+    assert cached.any() and (~cached).any()
+    want_y = np.where(cached[:, :, None], fp["y"], bf["y"])
+    assert np.array_equal(mixed["y"], want_y)
+    assert not np.array_equal(fp["y"][cached], bf["y"][cached])   # the profiles really differ there
+    out = np.zeros((w.T, w.H))
+    for t in range(w.T):
+        for j in range(w.k):
+            out[t] += float(mixed["w"][t, j]) * want_y[t, j]
+    assert np.allclose(mixed["out"], out, rtol=1e-6, atol=0)  # fp32 of the fp64 sum (summation order aside)
