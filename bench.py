@@ -19,7 +19,9 @@ in one launch, combine; the headline runs the whole step as one launch),
 decode_unfused (the same with FC1 and FC2 as two calls), decode_mxfp4 (the
 decode shapes with MXFP4 experts on the block-scaled FP8 tensor core, MXFP8
 tokens), mixed_decode (64 tokens, 2-bit experts plus 64 MXFP4 delta-cache
-entries) and decode_host (the decode workload with every expert in pinned
+entries, all in the bf16 profile), mixed_decode_fp8cache (the same with the
+cache experts on the block-scaled FP8 tensor core, MXFP8 tokens: their rows
+in the fp8 profile) and decode_host (the decode workload with every expert in pinned
 host memory and half of them resident on the device: the routed others are
 copied over the CPU-GPU link each step).
 
@@ -177,8 +179,9 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
     unfused = name.endswith("_unfused")  # the 2-bit decode's FC1 and FC2 as two calls (not one launch)
     as_mx4 = name.endswith("_mxfp4")     # the workload with MXFP4 experts on the block-scaled tensor core
     four = name.endswith("_fused")       # the 2-bit decode step as four calls (FC1 + FC2 in one launch)
+    fp8cache = name.endswith("_fp8cache")  # mixed: the cache experts on the block-scaled FP8 tensor core
     base = name
-    for suf in ("_direct", "_host", "_unfused", "_mxfp4", "_fused"):
+    for suf in ("_direct", "_host", "_unfused", "_mxfp4", "_fused", "_fp8cache"):
         if name.endswith(suf):
             base = name[:-len(suf)]
     w = synth.get_workload(base)
@@ -200,7 +203,7 @@ def build_workload(name, layers, batches, device, tokens=None, experts=None):
         elif w.weights == "mixed":
             ml = MoELayer("mixed", w.E, w.H, w.I, w.k, device, w2=synth.make_w2_layer(w, 0, l),
                           mx=synth.make_mxfp4_layer(w, n=w.n_hot, seed=0, layer=l),
-                          expert_slot=synth.hot_experts(w, 0), out_fmt=L.FMT_BF16)
+                          expert_slot=synth.hot_experts(w, 0), out_fmt=L.FMT_BF16, cache_fp8=fp8cache)
         else:
             ml = MoELayer("fp8", w.E, w.H, w.I, w.k, device, mx=synth.make_mxfp4_layer(w, seed=0, layer=l),
                           out_fmt=L.FMT_BF16)
@@ -477,9 +480,9 @@ def launches_per_step(ml, T):
         return 4
     if ml.fmt == "w2":
         return 6 if tc else 7
-    if ml.fmt == "mixed":
-        mx_tc = ml.mx_tensor_path()
-        return 3 + (1 if mx_tc else 0) + 2 * 2 + 2 * 1
+    if ml.fmt == "mixed":  # route, permute (+ gather), 2 x (table GEMV + sums), 2 x cache-expert matmul, combine
+        gather = ml.mx_tensor_path() or ml.cache_fp8
+        return 3 + (1 if gather else 0) + 2 * 2 + 2 * 1
     if ml.fmt == "mxfp4":
         return 6
     if ml.fmt == "w2host":  # route, permute, stage select, fill, combine + 3 (4 with side SMs) x (table GEMV + sums)
@@ -720,10 +723,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "mixed_decode", "prefill_bf16", "prefill_fp8", "prefill_fp8_direct",
-                             "decode_host", "decode_unfused", "decode_mxfp4", "decode_fused"])
+                             "decode_host", "decode_unfused", "decode_mxfp4", "decode_fused",
+                             "mixed_decode_fp8cache"])
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--sub", default="decode_fused,decode_unfused,decode_mxfp4,prefill_bf16,prefill_fp8,prefill_fp8_direct,"
-                                     "mixed_decode,decode_host",
+                                     "mixed_decode,mixed_decode_fp8cache,decode_host",
                     help="other workloads timed in the same run as sub-records ('' for none)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small cases for profiler captures)")

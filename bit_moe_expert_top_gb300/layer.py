@@ -63,6 +63,8 @@ class StepBuffers:
     ws: Optional[torch.Tensor] = None
     pws: Optional[torch.Tensor] = None   # grouping scratch of large steps (multi-CTA)
     fws: Optional[torch.Tensor] = None   # scratch of the fused FC1+FC2 launch
+    h8: Optional[torch.Tensor] = None    # mixed with cache_fp8: the cache experts' h as MXFP8 codes
+    h8_scale: Optional[torch.Tensor] = None
 
 
 class MoELayer:
@@ -70,7 +72,7 @@ class MoELayer:
                  w2=None, mx=None, expert_slot=None, fp8_batch: int = 64, fp8_ring: int = 2,
                  out_fmt: int = L.FMT_F32, mode: int = L.MODE_AUTO, gemm_min_rows: int = 2048,
                  resident=None, stage_slots: int = 64, fused: bool = True, split: bool = False,
-                 side_sms: Optional[int] = None, single_launch: bool = True):
+                 side_sms: Optional[int] = None, single_launch: bool = True, cache_fp8: bool = False):
         """Weights are canonical host arrays (see synth.py / include/moe.h):
         w2 = (codes1, scales1, codes2, scales2) stacked over experts;
         mx = (q1, s1, q2, s2) stacked over cache slots (mixed) or experts (fp8);
@@ -91,6 +93,10 @@ class MoELayer:
         whole step (routing, grouping, FC1 + FC2, combine) as one launch of
         moe_w2_decode_layer instead of four calls; bit-identical outputs;
         the default (measured 5 % faster per decode step).
+        cache_fp8 (mixed): the delta-cache (MXFP4) experts on the block-scaled
+        FP8 tensor core with MXFP8 tokens and an MXFP8 h (their rows in the
+        fp8 profile; the 2-bit experts stay in bf16); off by default, which
+        keeps the whole layer in the bf16 profile.
         side_sms (fp8 on the tensor-core path, w2host): SMs reserved for the
         side-stream copy (the workspace conversion of the next batches, the
         staging of host-resident experts) while the matmuls run on the
@@ -105,6 +111,7 @@ class MoELayer:
         self.fused = fused and fmt == "w2"
         self.single_launch = single_launch and self.fused
         self.split = split and fmt == "mixed"
+        self.cache_fp8 = cache_fp8 and fmt == "mixed"
         self.side_sms = side_sms if side_sms is not None else (16 if fmt == "w2host" else 0)
         self.gemm_min_rows = gemm_min_rows
         dev = self.device
@@ -209,14 +216,16 @@ class MoELayer:
             h_scale=torch.empty((A, I // 32), dtype=torch.uint8, device=dev) if fp8 else None,
             y=torch.empty((A, H), dtype=torch.int16, device=dev),
             out=torch.empty((T, H), dtype=torch.float32 if self.out_fmt == L.FMT_F32 else torch.int16, device=dev),
-            x_perm=(torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 else
+            x_perm=(torch.empty((A, H), dtype=torch.uint8, device=dev) if fp8 or self.cache_fp8 else
                     torch.empty((A, H), dtype=torch.int16, device=dev)
                     if gather or self.fmt == "fp8" or self.mx_tensor_path() else None),
-            x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 else None,
+            x_perm_scale=torch.empty((A, H // 32), dtype=torch.uint8, device=dev) if fp8 or self.cache_fp8 else None,
             dev_err=torch.zeros(1, dtype=torch.int32, device=dev),
             ws=self._gemv_ws(A) if self.fmt in ("w2", "mixed", "w2host") and not gather else None,
             pws=self._permute_ws(T),
             fws=self._fused_ws(A) if self.fused and not gather else None,
+            h8=torch.empty((A, I), dtype=torch.uint8, device=dev) if self.cache_fp8 else None,
+            h8_scale=torch.empty((A, I // 32), dtype=torch.uint8, device=dev) if self.cache_fp8 else None,
         )
 
     def _fused_ws(self, A: int) -> Optional[torch.Tensor]:
@@ -289,7 +298,10 @@ class MoELayer:
                             mode=L.MODE_GEMM, dev_err=b.dev_err)
         else:
             mx_tc = self.mx_tensor_path()
-            if mx_tc:  # the cache experts' matmuls read gathered rows
+            if self.cache_fp8:  # the cache experts' matmuls read gathered MXFP8 rows
+                self._permute(b, x=x, act_fmt=L.FMT_MXFP8, x_perm=b.x_perm, x_perm_scale=b.x_perm_scale,
+                              dev_err=b.dev_err)
+            elif mx_tc:  # the cache experts' matmuls read gathered rows
                 self._permute(b, x=x, act_fmt=L.FMT_BF16, x_perm=b.x_perm,
                               dev_err=b.dev_err)
             else:
@@ -302,7 +314,7 @@ class MoELayer:
                 return b.out
             # split: 2-bit experts of a mixed layer on gathered rows, single-row groups
             # on the table GEMV, larger ones on the tensor core (one pass over their weights)
-            split = mx_tc and self.split
+            split = mx_tc and self.split and not self.cache_fp8
             w2_mode = (L.MODE_SPLIT if self.mode == L.MODE_AUTO else self.mode) if split else self.mode
             with self._timed("w2_fc1"):
                 if split:
@@ -313,7 +325,13 @@ class MoELayer:
                     L.moe_w2_mm(L.STAGE_FC1_SWIGLU, x, L.FMT_BF16, self.c1k, self.s1k, b.offsets, E, I, H, b.h,
                                 L.FMT_BF16, act_row=b.perm, act_row_div=k, expert_slot=self.expert_slot,
                                 mode=self.mode, ws=b.ws, dev_err=b.dev_err)
-            if self.fmt == "mixed" and mx_tc:
+            if self.cache_fp8:
+                with self._timed("mx_fc1"):
+                    L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_MXFP8, b.offsets, E, I, H, b.h8, L.FMT_MXFP8,
+                                   e2m1=self.q1, e8m0=self.e1, expert_slot=self.expert_slot,
+                                   act_scale=b.x_perm_scale, out_scale=b.h8_scale, mode=L.MODE_GEMM,
+                                   dev_err=b.dev_err)
+            elif self.fmt == "mixed" and mx_tc:
                 with self._timed("mx_fc1"):
                     L.moe_mxfp4_mm(L.STAGE_FC1_SWIGLU, b.x_perm, L.FMT_BF16, b.offsets, E, I, H, b.h, L.FMT_BF16,
                                    e2m1=self.q1, e8m0=self.e1, expert_slot=self.expert_slot, mode=L.MODE_GEMM,
@@ -326,7 +344,12 @@ class MoELayer:
             with self._timed("w2_fc2"):
                 L.moe_w2_mm(L.STAGE_FC2, b.h, L.FMT_BF16, self.c2k, self.s2k, b.offsets, E, H, I, b.y, L.FMT_BF16,
                             expert_slot=self.expert_slot, mode=w2_mode, ws=b.ws, dev_err=b.dev_err)
-            if self.fmt == "mixed":
+            if self.cache_fp8:
+                with self._timed("mx_fc2"):
+                    L.moe_mxfp4_mm(L.STAGE_FC2, b.h8, L.FMT_MXFP8, b.offsets, E, H, I, b.y, L.FMT_BF16,
+                                   e2m1=self.q2, e8m0=self.e2, expert_slot=self.expert_slot,
+                                   act_scale=b.h8_scale, mode=L.MODE_GEMM, dev_err=b.dev_err)
+            elif self.fmt == "mixed":
                 with self._timed("mx_fc2"):
                     L.moe_mxfp4_mm(L.STAGE_FC2, b.h, L.FMT_BF16, b.offsets, E, H, I, b.y, L.FMT_BF16,
                                    e2m1=self.q2, e8m0=self.e2, expert_slot=self.expert_slot,
