@@ -144,6 +144,8 @@ _TRAFFIC = {
                    "src_sha256": "199099f071d7a3ab38caf8a3549320951d23e47266d961c1f7c87ae38c50f77f"},
     "decode_fused": {"bytes": 502.08e6, "src": ['gemv_lut.cu', 'common.cuh', 'internal.cuh'],
                     "src_sha256": "199099f071d7a3ab38caf8a3549320951d23e47266d961c1f7c87ae38c50f77f"},
+    "mixed_decode_fp8cache": {"bytes": 628.21e6, "src": ['gemv_lut.cu', 'gemm_mx.cu', 'tc_common.cuh', 'common.cuh', 'internal.cuh'],
+                             "src_sha256": "8d108c4ae4753f82d88326020f24f50382513c22a3697d619de4017e1820ef55"},
 }
 
 
